@@ -1,0 +1,164 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) fused softmax-attention forward library (libfa.so).
+ *
+ * The operation everywhere is softmax attention computed exactly, blockwise, with an online
+ * softmax (FlashAttention; llama.cpp PR "CUDA: fix FA occupancy, optimize tile kernel",
+ * opening paragraphs; flashinfer PR "perf: FlashAttention-3 style MLA PageAttention",
+ * change list):
+ *
+ *     s_j = scale * <q, k_j> + mask_j,   out = sum_j softmax(s)_j v_j,   lse = ln sum_j e^{s_j}
+ *
+ * Conventions (the pages leave them open; these are the readings this library takes):
+ *   - every pointer argument is a DEVICE pointer unless stated otherwise, to a contiguous,
+ *     row-major array whose last dimension is innermost, aligned to 16 bytes;
+ *   - grouped-query attention: query head h reads kv head h / (Hq / Hkv);
+ *   - causal masking is bottom-right aligned: query i (of Lq) sits at absolute position
+ *     Lkv - Lq + i and sees keys j <= Lkv - Lq + i;
+ *   - lse is the natural log-sum-exp of the scaled, masked scores, stored as fp32;
+ *   - a row that sees no key (fully masked, or seq_len 0) gets out = 0 and lse = -inf;
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous: they enqueue kernels and return without synchronising;
+ *   - the library never allocates device memory during a call.  Split-KV scratch is a
+ *     caller-provided workspace sized by the matching *_workspace_size function;
+ *   - argument errors are detected on the host before anything is enqueued: the call
+ *     returns a nonzero fa_status and fa_last_error() describes it.  Errors found on the
+ *     device (a page id out of range, a wait that ran out) are recorded in a sticky status
+ *     word read by fa_get_device_status(); the kernel skips the offending access.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, inconsistent sizes */
+  FA_ERR_UNSUPPORTED = 2, /* valid but not implemented (head dim, group size, dtype) */
+  FA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than *_workspace_size */
+  FA_ERR_CUDA = 4,        /* a CUDA runtime call failed (no device, launch failure) */
+  FA_ERR_TIMEOUT = 5,     /* device: a bounded wait inside a kernel ran out */
+  FA_ERR_BOUNDS = 6       /* device: a page id or sequence length was out of range */
+} fa_status;
+
+typedef enum fa_dtype { FA_BF16 = 0, FA_FP16 = 1, FA_FP32 = 2 } fa_dtype;
+
+/*
+ * Dense attention (prefill of a query chunk against a KV cache), bf16.
+ * Defined by the formula above over all keys of the batch entry; the query chunk attends
+ * to a cache of Lkv keys (the pp16384 workloads of the llama.cpp PR above process query
+ * micro-batches against a 16K-token context).
+ *   q   [B, Hq,  Lq,  D] bf16        k, v [B, Hkv, Lkv, D] bf16
+ *   out [B, Hq,  Lq,  D] bf16        lse  [B, Hq, Lq] fp32, or NULL
+ *   Hq % Hkv == 0, Hq / Hkv <= 128, D in {64, 128, 256}; Lq, Lkv >= 0; causal 0/1.
+ * No workspace: the KV loop is not split across CTAs (use fa_prefill_ex for that).
+ * Returns FA_OK or an fa_status code.
+ */
+int fa_prefill(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+               int Hq, int Hkv, int Lq, int Lkv, int D, int causal, float scale, void* stream);
+
+/* Extended prefill arguments (zero-initialise, then set the fields you need). */
+typedef struct fa_prefill_args {
+  const void* q;         /* [B, Hq, Lq, D] in dtype */
+  const void* k;         /* [B, Hkv, Lkv, D] in dtype */
+  const void* v;         /* [B, Hkv, Lkv, D] in dtype */
+  void* out;             /* [B, Hq, Lq, D] in dtype */
+  float* lse;            /* [B, Hq, Lq] fp32, or NULL */
+  int B, Hq, Hkv, Lq, Lkv, D;
+  int causal;
+  float scale;
+  fa_dtype dtype;        /* FA_BF16, FA_FP16, or FA_FP32 (fp32 inputs are rounded to fp16
+                            for the tensor cores, accumulation stays fp32; needs workspace) */
+  const void* mask;      /* optional additive mask [mask_batches, Lq, Lkv]; -inf removes a
+                            key; shared by all heads; NULL = none */
+  fa_dtype mask_dtype;   /* FA_FP32 or FA_BF16 */
+  int mask_batches;      /* 1 (broadcast over the batch) or B */
+  int num_splits;        /* 0: the library picks; >= 1: split the KV loop this many ways */
+  void* workspace;       /* device scratch, >= fa_prefill_workspace_size(args) bytes */
+  size_t workspace_bytes;
+} fa_prefill_args;
+
+int fa_prefill_ex(const fa_prefill_args* args, void* stream);
+
+/* Workspace bytes fa_prefill_ex needs for these arguments on the current device (0 when
+ * the plan needs none).  Depends only on sizes, dtype and num_splits. */
+size_t fa_prefill_workspace_size(const fa_prefill_args* args);
+
+/* The split count fa_prefill_ex will use for these arguments on the current device. */
+int fa_prefill_num_splits(const fa_prefill_args* args);
+
+/*
+ * Split-KV paged grouped-query decode: one query token per sequence attends to the
+ * seq_lens[b] tokens of its paged cache (flashinfer PR above, results section: paged KV
+ * cache with a page_size; page_table + seq_lens addressing).
+ *   q        [B, Hq, D] bf16
+ *   k_pages, v_pages [num_pages, Hkv, page_size, D] bf16 (each page holds page_size
+ *            consecutive tokens of every kv head)
+ *   page_table [B, max_pages_per_seq] int32: key t of sequence b is slot t % page_size of
+ *            page page_table[b, t / page_size]; entries past the sequence are not read
+ *   seq_lens [B] int32 (device), each in [0, max_seq_len]
+ *   out [B, Hq, D] bf16;  lse [B, Hq] fp32 or NULL
+ *   D in {64, 128, 256}; page_size a power of two; max_seq_len <= max_pages*page_size is a
+ *   host-side bound used to size the grid (no device-to-host read).
+ *   workspace >= fa_decode_workspace_size(B, Hq, D, max_seq_len) bytes.
+ */
+int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                    const int32_t* page_table, const int32_t* seq_lens, void* out, float* lse,
+                    int B, int Hq, int Hkv, int D, int page_size, int max_pages_per_seq,
+                    int num_pages, int max_seq_len, float scale, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+size_t fa_decode_workspace_size(int B, int Hq, int D, int max_seq_len);
+
+/*
+ * MLA paged decode in the latent (absorbed) form: the compressed ckv matrix serves as both
+ * K and V and a separate rope part kpe adds q_pe . kpe_t to each score (flashinfer PR
+ * above, change list item 4; results section: 64 heads, page_size 1):
+ *   s_t = scale * (q_nope . ckv_t + q_pe . kpe_t),   out = softmax(s) . ckv
+ *   q_nope [B, H, Dc] bf16, q_pe [B, H, Dr] bf16
+ *   ckv_pages [num_pages, page_size, Dc] bf16, kpe_pages [num_pages, page_size, Dr] bf16
+ *   page_table [B, max_pages_per_seq] int32, seq_lens [B] int32
+ *   out [B, H, Dc] bf16 (latent space), lse [B, H] fp32 or NULL
+ *   Dc == 512, Dr == 64, H == 64 (one tensor-core tile of heads).
+ *   workspace >= mla_decode_workspace_size(B, H, Dc, max_seq_len) bytes.
+ */
+int mla_decode_paged(const void* q_nope, const void* q_pe, const void* ckv_pages,
+                     const void* kpe_pages, const int32_t* page_table, const int32_t* seq_lens,
+                     void* out, float* lse, int B, int H, int Dc, int Dr, int page_size,
+                     int max_pages_per_seq, int num_pages, int max_seq_len, float scale,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+size_t mla_decode_workspace_size(int B, int H, int Dc, int max_seq_len);
+
+/*
+ * Merge of attention states over disjoint key sets (the split-KV combine):
+ *   lse = ln sum_s e^{lse_s},   out = sum_s e^{lse_s - lse} o_s
+ *   o_parts [rows, max_splits, D] fp32 (normalised partial outputs), lse_parts
+ *   [rows, max_splits] fp32 (natural log; -inf = empty part); n_splits [rows] int32 or NULL
+ *   (= max_splits for every row); out [rows, D] in out_dtype; lse [rows] fp32 or NULL.
+ *   D a multiple of 4.
+ */
+int fa_merge_states(const float* o_parts, const float* lse_parts, const int32_t* n_splits,
+                    void* out, float* lse, int rows, int D, int max_splits, fa_dtype out_dtype,
+                    void* stream);
+
+/* Synchronises `stream`, returns the sticky device status of the current device (FA_OK,
+ * FA_ERR_TIMEOUT or FA_ERR_BOUNDS; FA_ERR_CUDA if the synchronisation itself failed) and
+ * clears it. */
+int fa_get_device_status(void* stream);
+
+/* Message for the last error returned on the calling thread ("" if none). */
+const char* fa_last_error(void);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

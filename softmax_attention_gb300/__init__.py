@@ -1,0 +1,281 @@
+"""GB300 (sm_103a) fused softmax-attention forward: Python binding of libfa.so.
+
+Argument marshalling only.  Every step of the computation runs in the CUDA kernels behind
+the C ABI in ``include/fa.h``; PyTorch provides device memory and the current stream.  There
+is no fallback: if the library is missing or a call fails, an exception is raised.
+
+Entry points (same names as the C ABI):
+    fa_prefill(q, k, v, causal, scale)                       bf16, spec signature
+    fa_prefill_ex(q, k, v, causal=..., scale=..., mask=..., num_splits=..., dtype from q)
+    fa_decode_paged(q, k_pages, v_pages, page_table, seq_lens, max_seq_len, scale)
+    mla_decode_paged(q_nope, q_pe, ckv, kpe, page_table, seq_lens, max_seq_len, scale)
+    fa_merge_states(o_parts, lse_parts, n_splits=None, out_dtype=torch.bfloat16)
+    fa_get_device_status()
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfa.so")
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_WORKSPACE, FA_ERR_CUDA, FA_ERR_TIMEOUT, \
+    FA_ERR_BOUNDS = range(7)
+FA_BF16, FA_FP16, FA_FP32 = 0, 1, 2
+_DT = {torch.bfloat16: FA_BF16, torch.float16: FA_FP16, torch.float32: FA_FP32}
+
+# Every symbol include/fa.h declares.
+EXPORTS = (
+    "fa_prefill", "fa_prefill_ex", "fa_prefill_workspace_size", "fa_prefill_num_splits",
+    "fa_decode_paged", "fa_decode_workspace_size", "mla_decode_paged",
+    "mla_decode_workspace_size", "fa_merge_states", "fa_get_device_status", "fa_last_error",
+    "fa_version",
+)
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[fa status {code}] {msg}")
+        self.code = code
+
+
+class PrefillArgs(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("Lq", ctypes.c_int),
+        ("Lkv", ctypes.c_int), ("D", ctypes.c_int), ("causal", ctypes.c_int),
+        ("scale", ctypes.c_float), ("dtype", ctypes.c_int), ("mask", ctypes.c_void_p),
+        ("mask_dtype", ctypes.c_int), ("mask_batches", ctypes.c_int),
+        ("num_splits", ctypes.c_int), ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+
+def load_library(path: str | None = None):
+    """Load libfa.so (built by ``softmax_attention_gb300.build``).  Raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise ImportError(f"{p} not found: build it with `python -m softmax_attention_gb300.build`")
+        lib = ctypes.CDLL(p)
+        lib.fa_prefill.restype = _i
+        lib.fa_prefill.argtypes = [_vp, _vp, _vp, _vp, _vp] + [_i] * 7 + [_f, _vp]
+        lib.fa_prefill_ex.restype = _i
+        lib.fa_prefill_ex.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
+        lib.fa_prefill_workspace_size.restype = _sz
+        lib.fa_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs)]
+        lib.fa_prefill_num_splits.restype = _i
+        lib.fa_prefill_num_splits.argtypes = [ctypes.POINTER(PrefillArgs)]
+        lib.fa_decode_paged.restype = _i
+        lib.fa_decode_paged.argtypes = [_vp] * 7 + [_i] * 8 + [_f, _vp, _sz, _vp]
+        lib.fa_decode_workspace_size.restype = _sz
+        lib.fa_decode_workspace_size.argtypes = [_i] * 4
+        lib.mla_decode_paged.restype = _i
+        lib.mla_decode_paged.argtypes = [_vp] * 8 + [_i] * 8 + [_f, _vp, _sz, _vp]
+        lib.mla_decode_workspace_size.restype = _sz
+        lib.mla_decode_workspace_size.argtypes = [_i] * 4
+        lib.fa_merge_states.restype = _i
+        lib.fa_merge_states.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
+        lib.fa_get_device_status.restype = _i
+        lib.fa_get_device_status.argtypes = [_vp]
+        lib.fa_last_error.restype = ctypes.c_char_p
+        lib.fa_last_error.argtypes = []
+        lib.fa_version.restype = _i
+        lib.fa_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != FA_OK:
+        raise FAError(rc, load_library().fa_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def _workspace(nbytes: int, device, workspace):
+    if nbytes == 0:
+        return None
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError(f"workspace needs {nbytes} bytes")
+        return workspace
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------------------------------
+def fa_prefill(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+               stream=None):
+    """bf16 dense attention through the short-form entry point (no KV split)."""
+    lib = load_library()
+    _need_cuda(q, k, v)
+    B, Hq, Lq, D = q.shape
+    Hkv, Lkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, Hq, Lq, dtype=torch.float32, device=q.device)
+    _check(lib.fa_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Lq, Lkv, D,
+                          int(bool(causal)), float(scale), _stream(stream)))
+    return out, lse
+
+
+def prefill_args(q, k, v, *, causal=False, scale=None, out=None, lse=None, mask=None,
+                 num_splits=0, workspace=None) -> PrefillArgs:
+    B, Hq, Lq, D = q.shape
+    Hkv, Lkv = k.shape[1], k.shape[2]
+    a = PrefillArgs()
+    a.q, a.k, a.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    a.out = out.data_ptr() if out is not None else None
+    a.lse = lse.data_ptr() if lse is not None else None
+    a.B, a.Hq, a.Hkv, a.Lq, a.Lkv, a.D = B, Hq, Hkv, Lq, Lkv, D
+    a.causal = int(bool(causal))
+    a.scale = float(scale if scale is not None else 1.0 / math.sqrt(D))
+    if q.dtype not in _DT:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    a.dtype = _DT[q.dtype]
+    if mask is not None:
+        m = mask if mask.dim() == 3 else mask.unsqueeze(0)
+        a.mask = m.data_ptr()
+        a.mask_dtype = _DT[m.dtype]
+        a.mask_batches = m.shape[0]
+    a.num_splits = int(num_splits)
+    if workspace is not None:
+        a.workspace = workspace.data_ptr()
+        a.workspace_bytes = workspace.numel() * workspace.element_size()
+    return a
+
+
+def fa_prefill_ex(q, k, v, *, causal=False, scale=None, mask=None, num_splits=0, out=None,
+                  lse=None, workspace=None, stream=None):
+    """Dense attention, any supported dtype (bf16/fp16/fp32), optional additive mask
+    [1 or B, Lq, Lkv], optional KV split (0 = library's choice)."""
+    lib = load_library()
+    _need_cuda(q, k, v, mask)
+    B, Hq, Lq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, Hq, Lq, dtype=torch.float32, device=q.device)
+    a = prefill_args(q, k, v, causal=causal, scale=scale, out=out, lse=lse, mask=mask,
+                     num_splits=num_splits)
+    need = lib.fa_prefill_workspace_size(ctypes.byref(a))
+    ws = _workspace(need, q.device, workspace)
+    if ws is not None:
+        a.workspace = ws.data_ptr()
+        a.workspace_bytes = ws.numel() * ws.element_size()
+    _check(lib.fa_prefill_ex(ctypes.byref(a), _stream(stream)))
+    return out, lse
+
+
+def prefill_workspace_size(q, k, v, **kw) -> int:
+    return load_library().fa_prefill_workspace_size(ctypes.byref(prefill_args(q, k, v, **kw)))
+
+
+def prefill_num_splits(q, k, v, **kw) -> int:
+    return load_library().fa_prefill_num_splits(ctypes.byref(prefill_args(q, k, v, **kw)))
+
+
+def fa_decode_workspace_size(B, Hq, D, max_seq_len) -> int:
+    return load_library().fa_decode_workspace_size(B, Hq, D, max_seq_len)
+
+
+def fa_decode_paged(q, k_pages, v_pages, page_table, seq_lens, max_seq_len: int,
+                    scale: float | None = None, out=None, lse=None, workspace=None, stream=None):
+    """Split-KV paged GQA decode.  q [B,Hq,D] bf16; pages [num_pages,Hkv,page_size,D];
+    page_table [B,max_pages] int32; seq_lens [B] int32 (device)."""
+    lib = load_library()
+    _need_cuda(q, k_pages, v_pages, page_table, seq_lens)
+    B, Hq, D = q.shape
+    num_pages, Hkv, page_size, _ = k_pages.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    ws = _workspace(lib.fa_decode_workspace_size(B, Hq, D, max_seq_len), q.device, workspace)
+    _check(lib.fa_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                               _ptr(seq_lens), _ptr(out), _ptr(lse), B, Hq, Hkv, D, page_size,
+                               page_table.shape[1], num_pages, int(max_seq_len), float(scale),
+                               _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+    return out, lse
+
+
+def mla_decode_workspace_size(B, H, Dc, max_seq_len) -> int:
+    return load_library().mla_decode_workspace_size(B, H, Dc, max_seq_len)
+
+
+def mla_decode_paged(q_nope, q_pe, ckv, kpe, page_table, seq_lens, max_seq_len: int,
+                     scale: float, out=None, lse=None, workspace=None, stream=None):
+    """MLA paged decode (latent form).  q_nope [B,H,512], q_pe [B,H,64] bf16;
+    ckv [P,page_size,512], kpe [P,page_size,64]; page_table [B,max_pages]; seq_lens [B]."""
+    lib = load_library()
+    _need_cuda(q_nope, q_pe, ckv, kpe, page_table, seq_lens)
+    B, H, Dc = q_nope.shape
+    Dr = q_pe.shape[2]
+    num_pages, page_size = ckv.shape[0], ckv.shape[1]
+    if out is None:
+        out = torch.empty_like(q_nope)
+    if lse is None:
+        lse = torch.empty(B, H, dtype=torch.float32, device=q_nope.device)
+    ws = _workspace(lib.mla_decode_workspace_size(B, H, Dc, max_seq_len), q_nope.device, workspace)
+    _check(lib.mla_decode_paged(_ptr(q_nope), _ptr(q_pe), _ptr(ckv), _ptr(kpe), _ptr(page_table),
+                                _ptr(seq_lens), _ptr(out), _ptr(lse), B, H, Dc, Dr, page_size,
+                                page_table.shape[1], num_pages, int(max_seq_len), float(scale),
+                                _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+    return out, lse
+
+
+def fa_merge_states(o_parts, lse_parts, n_splits=None, out_dtype=torch.bfloat16, out=None,
+                    lse=None, stream=None):
+    """Merge partial states: o_parts [rows,S,D] fp32, lse_parts [rows,S] fp32."""
+    lib = load_library()
+    _need_cuda(o_parts, lse_parts, n_splits)
+    rows, S, D = o_parts.shape
+    if out is None:
+        out = torch.empty(rows, D, dtype=out_dtype, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty(rows, dtype=torch.float32, device=o_parts.device)
+    _check(lib.fa_merge_states(_ptr(o_parts), _ptr(lse_parts), _ptr(n_splits), _ptr(out),
+                               _ptr(lse), rows, D, S, _DT[out.dtype], _stream(stream)))
+    return out, lse
+
+
+def fa_get_device_status(stream=None) -> int:
+    """Synchronise, return and clear the library's sticky device status (0 = OK)."""
+    return load_library().fa_get_device_status(_stream(stream))
+
+
+def fa_last_error() -> str:
+    return load_library().fa_last_error().decode(errors="replace")

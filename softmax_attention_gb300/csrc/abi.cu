@@ -1,0 +1,571 @@
+// abi.cu -- the C ABI declared in include/fa.h: argument validation, planning (split
+// counts, KV chunking, grids sized from the SM count), tensor-map encoding, and launches.
+// Argument errors are reported synchronously; nothing is enqueued for a rejected call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "internal.h"
+#include "sm103.cuh"
+
+namespace fa {
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(const char* where, cudaError_t e) {
+  return fail(FA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Sticky device status word (one per device the library runs on).
+__device__ uint32_t g_device_status;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+uint32_t* device_status_ptr() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+int num_sms() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType t, int rank, const void* base,
+                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                  CUtensorMapSwizzle swz) {
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return false;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+  }
+  cuuint64_t d[5], s[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) s[i] = strides_bytes[i];
+  }
+  return g_encode(map, t, rank, const_cast<void*>(base), d, s, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
+// ---------------------------------------------------------------------------------------
+// Prefill planning
+// ---------------------------------------------------------------------------------------
+struct PrefillPlan {
+  int G, q_per_tile, n_qtiles, n_splits;
+  size_t part_bytes, cast_bytes, total_bytes;
+  size_t off_o, off_lse, off_q, off_k, off_v;
+};
+
+int validate_prefill(const fa_prefill_args* a) {
+  if (!a) return fail(FA_ERR_INVALID_ARG, "fa_prefill: null argument struct");
+  if (a->B < 0 || a->Lq < 0 || a->Lkv < 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_prefill: B, Lq, Lkv must be >= 0 (got %d, %d, %d)", a->B,
+                a->Lq, a->Lkv);
+  if (a->Hq <= 0 || a->Hkv <= 0 || a->Hq % a->Hkv != 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_prefill: need Hq, Hkv > 0 and Hq %% Hkv == 0 (got %d, %d)",
+                a->Hq, a->Hkv);
+  if (a->Hq / a->Hkv > 128)
+    return fail(FA_ERR_UNSUPPORTED, "fa_prefill: query heads per kv head must be <= 128 (got %d)",
+                a->Hq / a->Hkv);
+  if (a->D != 64 && a->D != 128 && a->D != 256)
+    return fail(FA_ERR_UNSUPPORTED, "fa_prefill: D must be 64, 128 or 256 (got %d)", a->D);
+  if (a->dtype != FA_BF16 && a->dtype != FA_FP16 && a->dtype != FA_FP32)
+    return fail(FA_ERR_INVALID_ARG, "fa_prefill: unknown dtype %d", (int)a->dtype);
+  if (a->Hkv > 65535 || a->B > 65535)
+    return fail(FA_ERR_UNSUPPORTED, "fa_prefill: B and Hkv must be <= 65535");
+  if (!(a->scale == a->scale) || isinf(a->scale))
+    return fail(FA_ERR_INVALID_ARG, "fa_prefill: scale must be finite");
+  const bool work = a->B > 0 && a->Lq > 0;
+  if (work) {
+    if (!a->q || !a->out || (a->Lkv > 0 && (!a->k || !a->v)))
+      return fail(FA_ERR_INVALID_ARG, "fa_prefill: null q/k/v/out pointer");
+    if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->out))
+      return fail(FA_ERR_INVALID_ARG, "fa_prefill: q, k, v and out must be 16-byte aligned");
+    if (a->mask) {
+      if (a->mask_batches != 1 && a->mask_batches != a->B)
+        return fail(FA_ERR_INVALID_ARG, "fa_prefill: mask_batches must be 1 or B (got %d)",
+                    a->mask_batches);
+      if (a->mask_dtype != FA_FP32 && a->mask_dtype != FA_BF16)
+        return fail(FA_ERR_UNSUPPORTED, "fa_prefill: mask dtype must be FA_FP32 or FA_BF16");
+    }
+    if (a->num_splits < 0) return fail(FA_ERR_INVALID_ARG, "fa_prefill: num_splits must be >= 0");
+  }
+  return FA_OK;
+}
+
+PrefillPlan plan_prefill(const fa_prefill_args* a) {
+  PrefillPlan pl{};
+  pl.G = a->Hq / a->Hkv;
+  pl.q_per_tile = 128 / pl.G;
+  pl.n_qtiles = a->Lq > 0 ? (a->Lq + pl.q_per_tile - 1) / pl.q_per_tile : 0;
+  const int bn = prefill_block_n(a->D);
+  const int kv_tiles = a->Lkv > 0 ? (a->Lkv + bn - 1) / bn : 0;
+  int s = 1;
+  if (a->num_splits > 0) {
+    s = a->num_splits;
+  } else if (kv_tiles > 0) {
+    const long tiles = (long)pl.n_qtiles * a->Hkv * a->B;
+    const int sms = num_sms() > 0 ? num_sms() : 148;
+    // One CTA per SM fits; split the KV loop only when the tiles cover less than half
+    // the SMs, keeping at least two KV tiles per split.
+    if (tiles > 0 && tiles * 2 <= sms) {
+      s = (int)((sms + tiles - 1) / tiles);
+      s = s < kv_tiles / 2 ? s : (kv_tiles / 2 > 1 ? kv_tiles / 2 : 1);
+    }
+  }
+  if (kv_tiles > 0 && s > kv_tiles) s = kv_tiles;
+  if (s < 1) s = 1;
+  pl.n_splits = s;
+  const size_t rows = (size_t)a->B * a->Hq * a->Lq;
+  size_t off = 0;
+  if (s > 1) {
+    pl.off_o = off;
+    off = align_up(off + rows * s * a->D * sizeof(float), 256);
+    pl.off_lse = off;
+    off = align_up(off + rows * s * sizeof(float), 256);
+  }
+  pl.part_bytes = off;
+  if (a->dtype == FA_FP32) {
+    pl.off_q = off;
+    off = align_up(off + (size_t)a->B * a->Hq * a->Lq * a->D * 2, 256);
+    pl.off_k = off;
+    off = align_up(off + (size_t)a->B * a->Hkv * a->Lkv * a->D * 2, 256);
+    pl.off_v = off;
+    off = align_up(off + (size_t)a->B * a->Hkv * a->Lkv * a->D * 2, 256);
+  }
+  pl.cast_bytes = off - pl.part_bytes;
+  pl.total_bytes = off;
+  return pl;
+}
+
+int run_prefill(const fa_prefill_args* a, cudaStream_t stream) {
+  int rc = validate_prefill(a);
+  if (rc != FA_OK) return rc;
+  if (a->B == 0 || a->Lq == 0) return FA_OK;
+  const PrefillPlan pl = plan_prefill(a);
+  if (pl.total_bytes > 0) {
+    if (!a->workspace || a->workspace_bytes < pl.total_bytes)
+      return fail(FA_ERR_WORKSPACE, "fa_prefill: workspace of %zu bytes needed (got %zu)",
+                  pl.total_bytes, a->workspace ? a->workspace_bytes : (size_t)0);
+    if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0)
+      return fail(FA_ERR_INVALID_ARG, "fa_prefill: workspace must be 256-byte aligned");
+  }
+  uint32_t* status = device_status_ptr();
+  if (!status) return fail(FA_ERR_CUDA, "fa_prefill: no usable CUDA device");
+  uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+  PrefillParams p{};
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  Dtype operand = static_cast<Dtype>(a->dtype);
+  if (a->dtype == FA_FP32) {
+    const size_t nq = (size_t)a->B * a->Hq * a->Lq * a->D;
+    const size_t nk = (size_t)a->B * a->Hkv * a->Lkv * a->D;
+    cudaError_t e = launch_f32_to_f16(static_cast<const float*>(a->q), ws + pl.off_q, nq, stream);
+    if (e == cudaSuccess) e = launch_f32_to_f16(static_cast<const float*>(a->k), ws + pl.off_k, nk, stream);
+    if (e == cudaSuccess) e = launch_f32_to_f16(static_cast<const float*>(a->v), ws + pl.off_v, nk, stream);
+    if (e != cudaSuccess) return cuda_fail("fa_prefill (fp32 staging)", e);
+    p.q = ws + pl.off_q;
+    p.k = ws + pl.off_k;
+    p.v = ws + pl.off_v;
+    operand = Dtype::FP16;
+  }
+  if (a->Lkv == 0) {  // keep the tensor maps valid; the kernel reads no key
+    p.k = p.q;
+    p.v = p.q;
+  }
+  p.out = a->out;
+  p.lse = a->lse;
+  p.mask = a->mask;
+  p.mask_is_bf16 = a->mask && a->mask_dtype == FA_BF16;
+  p.mask_batches = a->mask_batches > 0 ? a->mask_batches : 1;
+  p.B = a->B;
+  p.Hq = a->Hq;
+  p.Hkv = a->Hkv;
+  p.G = pl.G;
+  p.Lq = a->Lq;
+  p.Lkv = a->Lkv;
+  p.D = a->D;
+  p.causal = a->causal ? 1 : 0;
+  p.scale_log2 = a->scale * 1.44269504088896340736f;
+  p.q_per_tile = pl.q_per_tile;
+  p.n_qtiles = pl.n_qtiles;
+  p.n_splits = pl.n_splits;
+  p.o_part = pl.n_splits > 1 ? reinterpret_cast<float*>(ws + pl.off_o) : nullptr;
+  p.lse_part = pl.n_splits > 1 ? reinterpret_cast<float*>(ws + pl.off_lse) : nullptr;
+  p.out_dtype = static_cast<Dtype>(a->dtype);
+  p.status = status;
+  cudaError_t e = launch_prefill(p, operand, stream);
+  if (e != cudaSuccess) return cuda_fail("fa_prefill (attention kernel)", e);
+  if (pl.n_splits > 1) {
+    MergeParams m{};
+    m.o_part = p.o_part;
+    m.lse_part = p.lse_part;
+    m.out = a->out;
+    m.lse = a->lse;
+    m.rows = a->B * a->Hq * a->Lq;
+    m.D = a->D;
+    m.max_splits = pl.n_splits;
+    m.out_dtype = static_cast<Dtype>(a->dtype);
+    e = launch_merge(m, stream);
+    if (e != cudaSuccess) return cuda_fail("fa_prefill (merge kernel)", e);
+  }
+  return FA_OK;
+}
+
+// ---------------------------------------------------------------------------------------
+// Decode planning: fixed-size KV chunks, one partial state per (row, chunk)
+// ---------------------------------------------------------------------------------------
+int decode_chunk(int B, int Hq, int max_seq_len) {
+  // 512-token chunks keep the partial-state traffic small next to the K/V stream; with
+  // few sequences the chunk shrinks (to 128) so the grid still covers the SMs.
+  const int sms = num_sms() > 0 ? num_sms() : 148;
+  int chunk = 512;
+  while (chunk > 128) {
+    const long ctas = (long)B * (Hq >= 4 ? Hq / 4 : 1) * ((max_seq_len + chunk - 1) / chunk);
+    if (ctas >= 4L * sms) break;
+    chunk /= 2;
+  }
+  return chunk;
+}
+
+size_t split_ws_bytes(long rows, int n_chunks, int D) {
+  return align_up((size_t)rows * n_chunks * D * sizeof(float), 256) +
+         align_up((size_t)rows * n_chunks * sizeof(float), 256);
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_prefill(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+               int Hkv, int Lq, int Lkv, int D, int causal, float scale, void* stream) {
+  fa_prefill_args a;
+  memset(&a, 0, sizeof a);
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Lq = Lq;
+  a.Lkv = Lkv;
+  a.D = D;
+  a.causal = causal;
+  a.scale = scale;
+  a.dtype = FA_BF16;
+  a.num_splits = 1;
+  return run_prefill(&a, static_cast<cudaStream_t>(stream));
+}
+
+int fa_prefill_ex(const fa_prefill_args* args, void* stream) {
+  return run_prefill(args, static_cast<cudaStream_t>(stream));
+}
+
+size_t fa_prefill_workspace_size(const fa_prefill_args* args) {
+  if (validate_prefill(args) != FA_OK) return 0;
+  if (args->B == 0 || args->Lq == 0) return 0;
+  return plan_prefill(args).total_bytes;
+}
+
+int fa_prefill_num_splits(const fa_prefill_args* args) {
+  if (validate_prefill(args) != FA_OK) return 0;
+  if (args->B == 0 || args->Lq == 0) return 1;
+  return plan_prefill(args).n_splits;
+}
+
+size_t fa_decode_workspace_size(int B, int Hq, int D, int max_seq_len) {
+  if (B <= 0 || Hq <= 0 || D <= 0 || max_seq_len <= 0) return 0;
+  const int chunk = decode_chunk(B, Hq, max_seq_len);
+  return split_ws_bytes((long)B * Hq, (max_seq_len + chunk - 1) / chunk, D);
+}
+
+int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                    const int32_t* page_table, const int32_t* seq_lens, void* out, float* lse,
+                    int B, int Hq, int Hkv, int D, int page_size, int max_pages_per_seq,
+                    int num_pages, int max_seq_len, float scale, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: need B >= 0, Hq, Hkv > 0, Hq %% Hkv == 0");
+  const int G = Hq / Hkv;
+  if (D != 64 && D != 128 && D != 256)
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: D must be 64, 128 or 256 (got %d)", D);
+  if (G > 16 || (G & (G - 1)) != 0 || G * D > 1024)
+    return fail(FA_ERR_UNSUPPORTED,
+                "fa_decode_paged: query heads per kv head must be a power of two with "
+                "G*D <= 1024 (got G=%d, D=%d)", G, D);
+  if (page_size <= 0 || (page_size & (page_size - 1)) != 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: page_size must be a power of two (got %d)",
+                page_size);
+  if (max_pages_per_seq < 0 || num_pages < 0 || max_seq_len < 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: negative size");
+  if ((long)max_pages_per_seq * page_size < max_seq_len)
+    return fail(FA_ERR_INVALID_ARG,
+                "fa_decode_paged: max_seq_len %d exceeds max_pages_per_seq*page_size", max_seq_len);
+  if (Hkv > 65535 || B > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: B, Hkv <= 65535");
+  if (!(scale == scale) || isinf(scale)) return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: scale must be finite");
+  if (B == 0) return FA_OK;
+  if (!q || !out || !seq_lens || (max_seq_len > 0 && (!k_pages || !v_pages || !page_table)))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: null pointer");
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k_pages) || !aligned16(v_pages))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: q, out, k_pages, v_pages must be 16-byte aligned");
+  const int chunk = decode_chunk(B, Hq, max_seq_len > 0 ? max_seq_len : 1);
+  const int n_chunks = max_seq_len > 0 ? (max_seq_len + chunk - 1) / chunk : 1;
+  const size_t need = split_ws_bytes((long)B * Hq, n_chunks, D);
+  if (!workspace || workspace_bytes < need)
+    return fail(FA_ERR_WORKSPACE, "fa_decode_paged: workspace of %zu bytes needed (got %zu)", need,
+                workspace ? workspace_bytes : (size_t)0);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: workspace must be 256-byte aligned");
+  uint32_t* status = device_status_ptr();
+  if (!status) return fail(FA_ERR_CUDA, "fa_decode_paged: no usable CUDA device");
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                             align_up((size_t)B * Hq * n_chunks * D * sizeof(float), 256));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (max_seq_len > 0) {
+    DecodeParams p{};
+    p.q = q;
+    p.k_pages = k_pages;
+    p.v_pages = v_pages;
+    p.page_table = page_table;
+    p.seq_lens = seq_lens;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = G;
+    p.D = D;
+    p.page_size = page_size;
+    p.max_pages = max_pages_per_seq;
+    p.num_pages = num_pages;
+    p.chunk = chunk;
+    p.n_chunks = n_chunks;
+    p.scale_log2 = scale * 1.44269504088896340736f;
+    p.o_part = o_part;
+    p.lse_part = lse_part;
+    p.status = status;
+    cudaError_t e = launch_decode(p, st);
+    if (e != cudaSuccess) return cuda_fail("fa_decode_paged (decode kernel)", e);
+  }
+  MergeParams m{};
+  m.o_part = o_part;
+  m.lse_part = lse_part;
+  m.seq_lens = max_seq_len > 0 ? seq_lens : nullptr;
+  m.n_splits = nullptr;
+  m.rows_per_seq = Hq;
+  m.chunk = chunk;
+  m.out = out;
+  m.lse = lse;
+  m.rows = B * Hq;
+  m.D = D;
+  m.max_splits = max_seq_len > 0 ? n_chunks : 0;
+  m.out_dtype = Dtype::BF16;
+  if (max_seq_len == 0) m.max_splits = 0;
+  cudaError_t e = launch_merge(m, st);
+  if (e != cudaSuccess) return cuda_fail("fa_decode_paged (merge kernel)", e);
+  return FA_OK;
+}
+
+size_t mla_decode_workspace_size(int B, int H, int Dc, int max_seq_len) {
+  if (B <= 0 || H <= 0 || Dc <= 0 || max_seq_len <= 0) return 0;
+  const int chunk = mla_chunk_tokens();
+  return split_ws_bytes((long)B * H, (max_seq_len + chunk - 1) / chunk, Dc);
+}
+
+int mla_decode_paged(const void* q_nope, const void* q_pe, const void* ckv_pages,
+                     const void* kpe_pages, const int32_t* page_table, const int32_t* seq_lens,
+                     void* out, float* lse, int B, int H, int Dc, int Dr, int page_size,
+                     int max_pages_per_seq, int num_pages, int max_seq_len, float scale,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || H <= 0 || Dc <= 0 || Dr < 0)
+    return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: need B >= 0, H, Dc > 0, Dr >= 0");
+  if (Dc != 512 || Dr != 64 || H != 64)
+    return fail(FA_ERR_UNSUPPORTED, "mla_decode_paged: supports Dc=512, Dr=64, H=64 (got %d, %d, %d)",
+                Dc, Dr, H);
+  if (page_size <= 0) return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: page_size must be > 0");
+  if (max_pages_per_seq < 0 || num_pages < 0 || max_seq_len < 0)
+    return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: negative size");
+  if ((long)max_pages_per_seq * page_size < max_seq_len)
+    return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: max_seq_len exceeds max_pages_per_seq*page_size");
+  if (B > 65535) return fail(FA_ERR_UNSUPPORTED, "mla_decode_paged: B <= 65535");
+  if (!(scale == scale) || isinf(scale)) return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: scale must be finite");
+  if (B == 0) return FA_OK;
+  if (!q_nope || !q_pe || !out || !seq_lens ||
+      (max_seq_len > 0 && (!ckv_pages || !kpe_pages || !page_table)))
+    return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: null pointer");
+  if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(out) || !aligned16(ckv_pages) ||
+      !aligned16(kpe_pages))
+    return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: tensors must be 16-byte aligned");
+  const int chunk = mla_chunk_tokens();
+  const int n_chunks = max_seq_len > 0 ? (max_seq_len + chunk - 1) / chunk : 1;
+  const size_t need = split_ws_bytes((long)B * H, n_chunks, Dc);
+  if (!workspace || workspace_bytes < need)
+    return fail(FA_ERR_WORKSPACE, "mla_decode_paged: workspace of %zu bytes needed (got %zu)", need,
+                workspace ? workspace_bytes : (size_t)0);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: workspace must be 256-byte aligned");
+  uint32_t* status = device_status_ptr();
+  if (!status) return fail(FA_ERR_CUDA, "mla_decode_paged: no usable CUDA device");
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                             align_up((size_t)B * H * n_chunks * Dc * sizeof(float), 256));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (max_seq_len > 0) {
+    MlaParams p{};
+    p.q_nope = q_nope;
+    p.q_pe = q_pe;
+    p.ckv = ckv_pages;
+    p.kpe = kpe_pages;
+    p.page_table = page_table;
+    p.seq_lens = seq_lens;
+    p.B = B;
+    p.H = H;
+    p.Dc = Dc;
+    p.Dr = Dr;
+    p.page_size = page_size;
+    p.max_pages = max_pages_per_seq;
+    p.num_pages = num_pages;
+    p.chunk = chunk;
+    p.n_chunks = n_chunks;
+    p.scale_log2 = scale * 1.44269504088896340736f;
+    p.o_part = o_part;
+    p.lse_part = lse_part;
+    p.status = status;
+    cudaError_t e = launch_mla(p, st);
+    if (e != cudaSuccess) return cuda_fail("mla_decode_paged (MLA kernel)", e);
+  }
+  MergeParams m{};
+  m.o_part = o_part;
+  m.lse_part = lse_part;
+  m.seq_lens = max_seq_len > 0 ? seq_lens : nullptr;
+  m.rows_per_seq = H;
+  m.chunk = chunk;
+  m.out = out;
+  m.lse = lse;
+  m.rows = B * H;
+  m.D = Dc;
+  m.max_splits = max_seq_len > 0 ? n_chunks : 0;
+  m.out_dtype = Dtype::BF16;
+  cudaError_t e = launch_merge(m, st);
+  if (e != cudaSuccess) return cuda_fail("mla_decode_paged (merge kernel)", e);
+  return FA_OK;
+}
+
+int fa_merge_states(const float* o_parts, const float* lse_parts, const int32_t* n_splits,
+                    void* out, float* lse, int rows, int D, int max_splits, fa_dtype out_dtype,
+                    void* stream) {
+  if (rows < 0 || D <= 0 || D % 4 != 0 || max_splits < 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_merge_states: need rows >= 0, D > 0 with D %% 4 == 0, max_splits >= 0");
+  if (out_dtype != FA_BF16 && out_dtype != FA_FP16 && out_dtype != FA_FP32)
+    return fail(FA_ERR_INVALID_ARG, "fa_merge_states: unknown out dtype %d", (int)out_dtype);
+  if (rows == 0) return FA_OK;
+  if (!out || (max_splits > 0 && (!o_parts || !lse_parts)))
+    return fail(FA_ERR_INVALID_ARG, "fa_merge_states: null pointer");
+  if (!aligned16(o_parts) || !aligned16(out))
+    return fail(FA_ERR_INVALID_ARG, "fa_merge_states: o_parts and out must be 16-byte aligned");
+  if (!device_status_ptr()) return fail(FA_ERR_CUDA, "fa_merge_states: no usable CUDA device");
+  MergeParams m{};
+  m.o_part = o_parts;
+  m.lse_part = lse_parts;
+  m.n_splits = n_splits;
+  m.out = out;
+  m.lse = lse;
+  m.rows = rows;
+  m.D = D;
+  m.max_splits = max_splits;
+  m.out_dtype = static_cast<Dtype>(out_dtype);
+  cudaError_t e = launch_merge(m, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("fa_merge_states", e);
+  return FA_OK;
+}
+
+int fa_get_device_status(void* stream) {
+  uint32_t* st = device_status_ptr();
+  if (!st) return fail(FA_ERR_CUDA, "fa_get_device_status: no usable CUDA device");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("fa_get_device_status (synchronize)", e);
+  uint32_t v = 0;
+  e = cudaMemcpy(&v, st, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail("fa_get_device_status (read)", e);
+  const uint32_t zero = 0;
+  e = cudaMemcpy(st, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail("fa_get_device_status (clear)", e);
+  if (v == kDevTimeout) return fail(FA_ERR_TIMEOUT, "a bounded wait inside a kernel ran out");
+  if (v == kDevBounds) return fail(FA_ERR_BOUNDS, "a page id or sequence length was out of range");
+  return FA_OK;
+}
+
+const char* fa_last_error(void) { return g_err; }
+
+int fa_version(void) { return 100; }
+
+}  // extern "C"

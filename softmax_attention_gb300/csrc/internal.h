@@ -1,0 +1,114 @@
+// internal.h -- host-side interfaces between the C ABI (abi.cu) and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fa {
+
+// Element types of the public ABI (same numbering as fa_dtype in include/fa.h).
+enum class Dtype : int { BF16 = 0, FP16 = 1, FP32 = 2 };
+
+// ---------------------------------------------------------------------------------------
+// Dense prefill
+// ---------------------------------------------------------------------------------------
+struct PrefillParams {
+  // q [B,Hq,Lq,D], k/v [B,Hkv,Lkv,D] in bf16 or fp16 (the kernel's operand type).
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;            // [B,Hq,Lq,D] in out_dtype
+  float* lse;           // [B,Hq,Lq] or nullptr
+  const void* mask;     // additive [mask_batches,Lq,Lkv] or nullptr
+  int mask_is_bf16;     // else fp32
+  int mask_batches;     // 1 or B
+  int B, Hq, Hkv, G, Lq, Lkv, D;
+  int causal;
+  float scale_log2;     // scale * log2(e)
+  int q_per_tile;       // queries per 128-row tile (floor(128 / G))
+  int n_qtiles;
+  int n_splits;         // > 1: write partial states to o_part / lse_part
+  float* o_part;        // [rows, n_splits, D] fp32
+  float* lse_part;      // [rows, n_splits] fp32 (natural log)
+  Dtype out_dtype;
+  uint32_t* status;
+};
+
+// Launch on `stream`; returns a CUDA error code (cudaSuccess on launch success).
+cudaError_t launch_prefill(const PrefillParams& p, Dtype operand, cudaStream_t stream);
+
+// Tensor-core tile shape for a given head dimension (exposed for the planner).
+int prefill_block_n(int D);
+
+// ---------------------------------------------------------------------------------------
+// Paged decode
+// ---------------------------------------------------------------------------------------
+struct DecodeParams {
+  const void* q;          // [B,Hq,D] bf16
+  const void* k_pages;    // [num_pages,Hkv,page_size,D]
+  const void* v_pages;
+  const int32_t* page_table;  // [B,max_pages]
+  const int32_t* seq_lens;    // [B]
+  int B, Hq, Hkv, G, D, page_size, max_pages, num_pages;
+  int chunk;              // tokens per split (multiple of page_size)
+  int n_chunks;           // ceil(max_seq_len / chunk)
+  float scale_log2;
+  float* o_part;          // [B*Hq, n_chunks, D]
+  float* lse_part;        // [B*Hq, n_chunks]
+  uint32_t* status;
+};
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------------------
+// MLA paged decode
+// ---------------------------------------------------------------------------------------
+struct MlaParams {
+  const void* q_nope;     // [B,H,Dc]
+  const void* q_pe;       // [B,H,Dr]
+  const void* ckv;        // [num_pages,page_size,Dc]
+  const void* kpe;        // [num_pages,page_size,Dr]
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  int B, H, Dc, Dr, page_size, max_pages, num_pages;
+  int chunk, n_chunks;
+  float scale_log2;
+  float* o_part;          // [B*H, n_chunks, Dc]
+  float* lse_part;        // [B*H, n_chunks]
+  uint32_t* status;
+};
+cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream);
+int mla_chunk_tokens();
+
+// ---------------------------------------------------------------------------------------
+// Merge of split states
+// ---------------------------------------------------------------------------------------
+struct MergeParams {
+  const float* o_part;     // [rows, max_splits, D]
+  const float* lse_part;   // [rows, max_splits]
+  const int32_t* n_splits; // per-row split count or nullptr (= max_splits)
+  // Alternative to n_splits for paged decode: the valid count of row r is
+  // ceil(seq_lens[r / rows_per_seq] / chunk).
+  const int32_t* seq_lens;
+  int rows_per_seq, chunk;
+  void* out;               // [rows, D] in out_dtype
+  float* lse;              // [rows] or nullptr
+  int rows, D, max_splits;
+  Dtype out_dtype;
+};
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+
+// fp32 -> fp16 element conversion (used for fp32 prefill inputs).
+cudaError_t launch_f32_to_f16(const float* src, void* dst, size_t n, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------------------
+// Shared host helpers
+// ---------------------------------------------------------------------------------------
+uint32_t* device_status_ptr();  // the library's sticky device status word on this device
+int num_sms();                  // SM count of the current device (cached)
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType t, int rank, const void* base,
+                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                  CUtensorMapSwizzle swz);
+
+}  // namespace fa

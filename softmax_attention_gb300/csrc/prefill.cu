@@ -1,0 +1,400 @@
+// prefill.cu -- fused attention forward for dense (prefill) inputs on sm_103a.
+//
+// One CTA computes one 128-row tile of packed (query head, query) rows against one range of
+// KV tiles of one kv head.  Grouped-query heads are packed into the tile ("GQA optimization",
+// llama.cpp PR "CUDA: fix FA occupancy, optimize tile kernel", second paragraph), so K, V and
+// the mask are read once per kv head.  The loop is FlashAttention's: S = Q K^T on the tensor
+// cores, an online softmax on the CUDA cores, O += P V on the tensor cores, with the softmax
+// overlapping the next tile's Q K^T (the FA3 software pipeline described in flashinfer PR
+// "perf: FlashAttention-3 style MLA PageAttention", change list items 1-3), rebuilt for
+// Blackwell: TMA loads into a multi-stage shared-memory ring, tcgen05.mma accumulating in
+// tensor memory, S/P double-buffered in tensor memory with P (16-bit) written over S, and O
+// resident in tensor memory for the whole KV loop.
+//
+// Warp roles (192 threads): warps 0-3 softmax + epilogue (thread t owns row t), warp 4 TMA
+// producer, warp 5 MMA issuer (one elected thread) and tensor-memory owner.
+#include <math.h>
+
+#include "internal.h"
+#include "sm103.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kRows = 128;
+constexpr int kThreads = 192;
+constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the running max grows by > 2^8
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+template <int D, int BN, int STAGES>
+struct Layout {
+  static constexpr int kQBytes = kRows * D * 2;
+  static constexpr int kKVBytes = BN * D * 2;  // one K (or V) stage
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQBytes;
+  static constexpr int kVOff = kKOff + STAGES * kKVBytes;
+  static constexpr int kBarOff = kVOff + STAGES * kKVBytes;
+  // q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full, o_full, mma_done
+  static constexpr int kNumBars = 1 + 3 * STAGES + 2 + 3;
+  static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
+  static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 bytes
+  static_assert(D + 2 * BN <= 512, "tensor memory budget");
+};
+
+template <int D, int BN, int STAGES, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  using L = Layout<D, BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t s_base = smem_addr(smem);
+  const uint32_t sQ = s_base + L::kQOff, sK = s_base + L::kKOff, sV = s_base + L::kVOff;
+  const uint32_t bars = s_base + L::kBarOff;
+  const uint32_t bar_q = bars;
+  auto bar_k = [&](int s) { return bars + 8u * (1 + s); };
+  auto bar_v = [&](int s) { return bars + 8u * (1 + STAGES + s); };
+  auto bar_e = [&](int s) { return bars + 8u * (1 + 2 * STAGES + s); };
+  auto bar_s = [&](int b) { return bars + 8u * (1 + 3 * STAGES + b); };
+  const uint32_t bar_p = bars + 8u * (3 + 3 * STAGES);
+  const uint32_t bar_o = bars + 8u * (4 + 3 * STAGES);
+  const uint32_t bar_done = bars + 8u * (5 + 3 * STAGES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBarOff + L::kNumBars * 8);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  // ---- work item: (query tile, split) x kv head x batch; heavier (later) tiles first ----
+  const int split = blockIdx.x % p.n_splits;
+  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x) / p.n_splits;
+  const int hk = blockIdx.y, b = blockIdx.z;
+  const int q0 = qt * p.q_per_tile;
+  const int q_last = min(p.Lq, q0 + p.q_per_tile) - 1;
+  int kv_end = p.Lkv;
+  if (p.causal) kv_end = min(p.Lkv, q_last + (p.Lkv - p.Lq) + 1);
+  const int n_kv_tiles = kv_end > 0 ? (kv_end + BN - 1) / BN : 0;
+  const int per_split = (n_kv_tiles + p.n_splits - 1) / p.n_splits;
+  const int t_begin = min(n_kv_tiles, split * per_split);
+  const int t_end = min(n_kv_tiles, t_begin + per_split);
+  const int n = t_end - t_begin;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_k(s), 1);
+      mbar_init(bar_v(s), 1);
+      mbar_init(bar_e(s), 1);
+    }
+    mbar_init(bar_s(0), 1);
+    mbar_init(bar_s(1), 1);
+    mbar_init(bar_p, 4 * 32);
+    mbar_init(bar_o, 1);
+    mbar_init(bar_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tm_o = tmem;           // O: columns [0, D)
+  const uint32_t tm_s0 = tmem + D;      // S/P buffer b: columns [D + b*BN, D + (b+1)*BN)
+
+  if (warp == 4) {
+    // ------------------------------- TMA producer ---------------------------------------
+    if (lane == 0 && n > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(bar_q, static_cast<uint32_t>(D * 2 * p.q_per_tile * p.G));
+      for (int kb = 0; kb < D / 64; ++kb)
+        tma_load_4d(sQ + kb * (kRows * 128), &tm_q, bar_q, kb * 64, q0, hk * p.G, b);
+      const int kv_row = b * p.Hkv + hk;
+      int issued = 0;
+      for (int jj = 0; jj < n; ++jj) {
+        const int stage = jj % STAGES;
+        if (jj >= STAGES && !mbar_wait(bar_e(stage), ((jj / STAGES) - 1) & 1, p.status)) break;
+        const int key0 = (t_begin + jj) * BN;
+        mbar_arrive_expect_tx(bar_k(stage), L::kKVBytes);
+        for (int kb = 0; kb < D / 64; ++kb)
+          tma_load_3d(sK + stage * L::kKVBytes + kb * (BN * 128), &tm_k, bar_k(stage), kb * 64,
+                      key0, kv_row);
+        mbar_arrive_expect_tx(bar_v(stage), L::kKVBytes);
+        for (int kb = 0; kb < D / 64; ++kb)
+          tma_load_3d(sV + stage * L::kKVBytes + kb * (BN * 128), &tm_v, bar_v(stage), kb * 64,
+                      key0, kv_row);
+        issued = jj + 1;
+      }
+      if (issued < n) {
+        // A wait ran out: let the copies already in flight land before the CTA exits.
+        mbar_wait(bar_q, 0, nullptr);
+        for (int jj = max(0, issued - STAGES); jj < issued; ++jj) {
+          mbar_wait(bar_k(jj % STAGES), (jj / STAGES) & 1, nullptr);
+          mbar_wait(bar_v(jj % STAGES), (jj / STAGES) & 1, nullptr);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------- MMA issuer -----------------------------------------
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idesc_s = idesc_f16(BF16, kRows, BN, false, false);
+      constexpr uint32_t idesc_o = idesc_f16(BF16, kRows, D, false, true);
+      auto issue_s = [&](int jj) {
+        const uint32_t kbase = sK + (jj % STAGES) * L::kKVBytes;
+        const uint32_t d_s = tm_s0 + (jj & 1) * BN;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk % 4) * 32;
+          const uint64_t ad = sdesc_sw128(sQ + (kk / 4) * (kRows * 128) + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(kbase + (kk / 4) * (BN * 128) + off, 16, 1024);
+          mma_ss(d_s, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bar_s(jj & 1));
+      };
+      bool ok = mbar_wait(bar_q, 0, p.status) && mbar_wait(bar_k(0), 0, p.status);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int jj = 0; ok && jj < n; ++jj) {
+        if (jj + 1 < n) {
+          const int s1 = (jj + 1) % STAGES;
+          if (!(ok = mbar_wait(bar_k(s1), ((jj + 1) / STAGES) & 1, p.status))) break;
+          tc_fence_after();
+          issue_s(jj + 1);
+        }
+        if (!(ok = mbar_wait(bar_p, jj & 1, p.status))) break;
+        const int stage = jj % STAGES;
+        if (!(ok = mbar_wait(bar_v(stage), (jj / STAGES) & 1, p.status))) break;
+        tc_fence_after();
+        const uint32_t vbase = sV + stage * L::kKVBytes;
+        const uint32_t a_p = tm_s0 + (jj & 1) * BN;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t bd = sdesc_sw128(vbase + kk * (16 * 128), BN * 128, 1024);
+          mma_ts(tm_o, a_p + kk * 8, bd, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(bar_o);
+        tc_commit(bar_e(stage));
+      }
+      // Every MMA this thread issued must finish before tensor memory is released.
+      tc_commit(bar_done);
+      mbar_wait(bar_done, 0, nullptr);
+    }
+  } else {
+    // ------------------------- softmax + epilogue (row per thread) ----------------------
+    const int r = threadIdx.x;
+    const int g = r / p.q_per_tile, il = r % p.q_per_tile;
+    const int i = q0 + il;
+    const bool row_valid = (g < p.G) && (i < p.Lq);
+    const int h = hk * p.G + g;
+    int key_lim = 0;  // keys j < key_lim are visible before the additive mask
+    if (row_valid) key_lim = p.causal ? min(p.Lkv, i + (p.Lkv - p.Lq) + 1) : p.Lkv;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const char* mask_row = nullptr;
+    if (p.mask && row_valid) {
+      const int mb = p.mask_batches == 1 ? 0 : b;
+      const size_t off = (static_cast<size_t>(mb) * p.Lq + i) * static_cast<size_t>(p.Lkv);
+      mask_row = static_cast<const char*>(p.mask) + off * (p.mask_is_bf16 ? 2 : 4);
+    }
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int jj = 0; jj < n; ++jj) {
+      const int buf = jj & 1;
+      const uint32_t t_s = tm_s0 + lane_off + buf * BN;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_s(buf), (jj >> 1) & 1, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t raw[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c)
+        tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&raw[c * 32]));
+      tmem_ld_wait();
+      const int key0 = (t_begin + jj) * BN;
+      float s[BN];
+      float row_max = -INFINITY;
+      if (mask_row) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          const int key = key0 + c;
+          float x = -INFINITY;
+          if (key < key_lim) {
+            const float mv = p.mask_is_bf16
+                                 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(mask_row)[key])
+                                 : reinterpret_cast<const float*>(mask_row)[key];
+            x = fmaf(__uint_as_float(raw[c]), p.scale_log2, mv * kLog2e);
+          }
+          s[c] = x;
+          row_max = fmaxf(row_max, x);
+        }
+      } else if (key0 + BN <= key_lim) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          s[c] = __uint_as_float(raw[c]) * p.scale_log2;
+          row_max = fmaxf(row_max, s[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          s[c] = (key0 + c < key_lim) ? __uint_as_float(raw[c]) * p.scale_log2 : -INFINITY;
+          row_max = fmaxf(row_max, s[c]);
+        }
+      }
+      const float m_new = fmaxf(m_run, row_max);
+      // O must hold every earlier P V product before it is rescaled; waiting on each
+      // phase in turn also keeps this warp at most one tile ahead of the MMA issuer.
+      if (jj > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (jj - 1) & 1, p.status));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      const bool need = m_new > m_run + kRescaleLog2;
+      if (__any_sync(0xffffffffu, need)) {
+        float alpha = 1.f;
+        if (need) {
+          alpha = exp2_approx(m_run - m_new);  // 0 when m_run is -inf
+          m_run = m_new;
+          l_run *= alpha;
+        }
+        if (jj > 0) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tm_o + lane_off + c * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tm_o + lane_off + c * 32, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      float sum = 0.f;
+      uint32_t pk[BN / 2];
+#pragma unroll
+      for (int c = 0; c < BN / 2; ++c) {
+        const float p0 = exp2_approx(s[2 * c] - m_use);
+        const float p1 = exp2_approx(s[2 * c + 1] - m_use);
+        sum += p0 + p1;
+        pk[c] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+      }
+      l_run += sum;
+#pragma unroll
+      for (int c = 0; c < BN / 2; c += 16)
+        tmem_st16(t_s + c, *reinterpret_cast<uint32_t(*)[16]>(&pk[c]));
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_p);
+    }
+    if (ok && n > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (n - 1) & 1, p.status));
+      tc_fence_after();
+    }
+    if (ok) {
+      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      const size_t row_flat = (static_cast<size_t>(b) * p.Hq + h) * p.Lq + i;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (n > 0) {
+          tmem_ld32(tm_o + lane_off + c * 32, o);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        if (!row_valid) continue;
+        float v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv_l;
+        if (p.n_splits > 1) {
+          float4* dst = reinterpret_cast<float4*>(
+              p.o_part + (row_flat * p.n_splits + split) * D + c * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        } else if (p.out_dtype == Dtype::FP32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + row_flat * D + c * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        } else {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = (p.out_dtype == Dtype::BF16) ? pack_bf16x2(v[2 * e], v[2 * e + 1])
+                                                : pack_f16x2(v[2 * e], v[2 * e + 1]);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row_flat * D + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        }
+      }
+      if (row_valid) {
+        if (p.n_splits > 1) p.lse_part[row_flat * p.n_splits + split] = lse_v;
+        else if (p.lse) p.lse[row_flat] = lse_v;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int BN, int STAGES, bool BF16>
+cudaError_t launch_impl(const PrefillParams& p, cudaStream_t stream) {
+  using L = Layout<D, BN, STAGES>;
+  const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap tq, tk, tv;
+  const uint64_t lkv = p.Lkv > 0 ? p.Lkv : 1;
+  {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)p.Lq, (uint64_t)p.Hq, (uint64_t)p.B};
+    const uint64_t str[3] = {(uint64_t)D * 2, (uint64_t)p.Lq * D * 2, (uint64_t)p.Hq * p.Lq * D * 2};
+    const uint32_t box[4] = {64, (uint32_t)p.q_per_tile, (uint32_t)p.G, 1};
+    if (!encode_tiled(&tq, dt, 4, p.q, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)D, lkv, (uint64_t)p.Hkv * p.B};
+    const uint64_t str[2] = {(uint64_t)D * 2, lkv * D * 2};
+    const uint32_t box[3] = {64, (uint32_t)BN, 1};
+    if (!encode_tiled(&tk, dt, 3, p.k, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled(&tv, dt, 3, p.v, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  auto kern = prefill_kernel<D, BN, STAGES, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.n_qtiles * p.n_splits, p.Hkv, p.B);
+  kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int prefill_block_n(int D) { return D == 256 ? 64 : 128; }
+
+cudaError_t launch_prefill(const PrefillParams& p, Dtype operand, cudaStream_t stream) {
+  const bool bf16 = operand == Dtype::BF16;
+  switch (p.D) {
+    case 64:
+      return bf16 ? launch_impl<64, 128, 4, true>(p, stream) : launch_impl<64, 128, 4, false>(p, stream);
+    case 128:
+      return bf16 ? launch_impl<128, 128, 2, true>(p, stream) : launch_impl<128, 128, 2, false>(p, stream);
+    case 256:
+      return bf16 ? launch_impl<256, 64, 2, true>(p, stream) : launch_impl<256, 64, 2, false>(p, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fa

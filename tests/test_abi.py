@@ -1,0 +1,124 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every symbol that
+include/fa.h declares, and rejects malformed arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import softmax_attention_gb300 as fa
+from softmax_attention_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return fa.load_library()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "fa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared()
+    assert len(declared) >= 12
+    assert sorted(fa.EXPORTS) == declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_version(lib):
+    assert lib.fa_version() >= 100
+
+
+def _args(**kw):
+    a = fa.PrefillArgs()
+    a.B, a.Hq, a.Hkv, a.Lq, a.Lkv, a.D = 1, 4, 2, 8, 8, 128
+    a.scale = 0.1
+    a.dtype = fa.FA_BF16
+    a.q = a.k = a.v = a.out = 4096
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(Hq=6, Hkv=4), fa.FA_ERR_INVALID_ARG),
+    (dict(Hq=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Lq=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(Hq=256, Hkv=1), fa.FA_ERR_UNSUPPORTED),
+    (dict(q=4097), fa.FA_ERR_INVALID_ARG),
+    (dict(out=None), fa.FA_ERR_INVALID_ARG),
+    (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
+    (dict(mask=8192, mask_batches=3, B=2), fa.FA_ERR_INVALID_ARG),
+    (dict(num_splits=-2), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+])
+def test_prefill_rejects_bad_arguments(lib, kw, code):
+    a = _args(**kw)
+    rc = lib.fa_prefill_ex(ctypes.byref(a), None)
+    assert rc == code, (rc, lib.fa_last_error())
+    assert lib.fa_last_error()
+
+
+def test_prefill_short_form_rejects_bad_head_dim(lib):
+    rc = lib.fa_prefill(4096, 4096, 4096, 4096, None, 1, 2, 2, 4, 4, 80, 0, 0.1, None)
+    assert rc == fa.FA_ERR_UNSUPPORTED
+    assert b"D must be" in lib.fa_last_error()
+
+
+def test_empty_work_is_ok_without_device(lib):
+    a = _args(B=0)
+    assert lib.fa_prefill_ex(ctypes.byref(a), None) == fa.FA_OK
+    a = _args(Lq=0)
+    assert lib.fa_prefill_ex(ctypes.byref(a), None) == fa.FA_OK
+    assert lib.fa_prefill_workspace_size(ctypes.byref(a)) == 0
+
+
+def test_workspace_sizes_are_consistent(lib):
+    # fp32 inputs need fp16 staging; forced splits need partial states
+    a = _args(dtype=fa.FA_FP32)
+    assert lib.fa_prefill_workspace_size(ctypes.byref(a)) >= (1 * 4 * 8 + 2 * 1 * 2 * 8) * 128 * 2
+    a = _args(num_splits=4, Lkv=4096)
+    assert lib.fa_prefill_num_splits(ctypes.byref(a)) == 4
+    assert lib.fa_prefill_workspace_size(ctypes.byref(a)) >= 1 * 4 * 8 * 4 * (128 + 1) * 4
+    assert lib.fa_decode_workspace_size(128, 32, 128, 4096) >= 128 * 32 * (128 + 1) * 4
+    assert lib.fa_decode_workspace_size(0, 32, 128, 4096) == 0
+    assert lib.mla_decode_workspace_size(128, 64, 512, 2048) >= 128 * 64 * (512 + 1) * 4
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(D=80), fa.FA_ERR_UNSUPPORTED),
+    (dict(Hq=32, Hkv=1), fa.FA_ERR_UNSUPPORTED),    # G=32 > 16
+    (dict(Hq=12, Hkv=4), fa.FA_ERR_UNSUPPORTED),    # G=3 not a power of two
+    (dict(page_size=12), fa.FA_ERR_INVALID_ARG),
+    (dict(max_seq_len=5000), fa.FA_ERR_INVALID_ARG),  # > max_pages * page_size
+    (dict(ws_bytes=16), fa.FA_ERR_WORKSPACE),
+])
+def test_decode_rejects_bad_arguments(lib, args, code):
+    p = dict(B=2, Hq=8, Hkv=2, D=128, page_size=16, max_pages=256, num_pages=600,
+             max_seq_len=4096, ws_bytes=1 << 30)
+    p.update(args)
+    rc = lib.fa_decode_paged(4096, 4096, 4096, 4096, 4096, 4096, None, p["B"], p["Hq"], p["Hkv"],
+                             p["D"], p["page_size"], p["max_pages"], p["num_pages"],
+                             p["max_seq_len"], 0.1, 4096 if p["ws_bytes"] > 16 else 4096,
+                             p["ws_bytes"], None)
+    assert rc == code, (rc, lib.fa_last_error())
+
+
+def test_mla_rejects_unsupported_shapes(lib):
+    rc = lib.mla_decode_paged(*([4096] * 7), None, 2, 128, 512, 64, 1, 16, 32, 16, 0.1, 4096,
+                              1 << 30, None)
+    assert rc == fa.FA_ERR_UNSUPPORTED
+
+
+def test_merge_rejects_bad_arguments(lib):
+    assert lib.fa_merge_states(4096, 4096, None, 4096, None, 4, 6, 2, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_merge_states(4096, 4096, None, 4096, None, 4, 8, 2, 9, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_merge_states(None, None, None, 4096, None, 0, 8, 2, 0, None) == fa.FA_OK

@@ -1,0 +1,136 @@
+"""GPU parity of the dense prefill kernel against the fp64 oracle, through the C ABI.
+
+Shapes span several 128-row tiles and KV tiles with ragged tails, every supported head
+dimension, grouped-query packings, causal alignment with Lq < Lkv and Lq > Lkv (empty rows),
+forced KV splits (merge path), additive masks, fp16 and fp32 inputs, and the two full-size
+workloads on sampled rows.
+"""
+import math
+
+import pytest
+import torch
+
+import oracle
+import softmax_attention_gb300 as fa
+import workloads
+from tests._parity import check
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fa.load_library()
+    yield
+    assert fa.fa_get_device_status() == fa.FA_OK, fa.fa_last_error()
+
+
+def _run(c: workloads.DenseCase, *, mask=None, num_splits=0, short_form=False, rows=None):
+    q, k, v = workloads.dense_inputs(c)
+    dev = torch.device("cuda")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    md = None if mask is None else mask.to(dev)
+    if short_form:
+        out, lse = fa.fa_prefill(qd, kd, vd, causal=c.causal, scale=c.sm_scale)
+    else:
+        out, lse = fa.fa_prefill_ex(qd, kd, vd, causal=c.causal, scale=c.sm_scale, mask=md,
+                                    num_splits=num_splits)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.attention(q, k, v, causal=c.causal, scale=c.sm_scale, mask=mask,
+                                    rows=rows)
+    if rows is not None:
+        out = out.reshape(-1, c.dv)[torch.as_tensor(rows, device=dev)]
+        lse = lse.reshape(-1)[torch.as_tensor(rows, device=dev)]
+    return out, lse, ref_o, ref_l
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_fp32(causal):
+    """B=1, Hq=Hkv=2, Lq=Lkv=64, D=64, fp32 N(0,1), scale 1/8."""
+    c = workloads.tiny_dense(causal)
+    out, lse, ro, rl = _run(c)
+    assert out.dtype == torch.float32
+    check(out, lse, ro, rl, what=f"tiny causal={causal}")
+
+
+CASES = [
+    # B, Hq, Hkv, Lq, Lkv, D, causal
+    (1, 4, 4, 200, 333, 64, False),
+    (2, 8, 2, 130, 260, 128, True),     # GQA 4, ragged q and kv tails
+    (1, 32, 8, 96, 1100, 128, True),    # Llama-like packing, chunk at the end of context
+    (1, 8, 1, 40, 700, 256, True),      # MQA, D=256
+    (2, 6, 3, 77, 77, 128, True),       # G=2, square causal
+    (1, 12, 4, 50, 129, 64, False),     # G=3: 42 queries per tile, 126 rows
+    (1, 2, 2, 300, 40, 128, True),      # Lq > Lkv: the first 260 rows see no key
+    (1, 16, 1, 33, 515, 128, False),    # G=16
+    (3, 2, 1, 1, 513, 128, True),       # single query per sequence
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lkv,D,causal", CASES)
+def test_parity_shapes(B, Hq, Hkv, Lq, Lkv, D, causal):
+    c = workloads.DenseCase(B=B, Hq=Hq, Hkv=Hkv, Lq=Lq, Lkv=Lkv, D=D, causal=causal,
+                            sigma=0.5, seed=B * 7 + Lq)
+    out, lse, ro, rl = _run(c)
+    check(out, lse, ro, rl, what=str(c))
+
+
+@pytest.mark.parametrize("splits", [2, 3, 7])
+def test_forced_splits(splits):
+    c = workloads.DenseCase(B=1, Hq=8, Hkv=2, Lq=100, Lkv=900, D=128, causal=True, sigma=0.5,
+                            seed=3)
+    out, lse, ro, rl = _run(c, num_splits=splits)
+    check(out, lse, ro, rl, what=f"splits={splits}")
+
+
+def test_short_form_matches_oracle():
+    c = workloads.DenseCase(B=1, Hq=8, Hkv=2, Lq=256, Lkv=1024, D=128, causal=True, sigma=0.5)
+    out, lse, ro, rl = _run(c, short_form=True)
+    check(out, lse, ro, rl, what="fa_prefill short form")
+
+
+@pytest.mark.parametrize("mask_dtype,mask_b", [(torch.float32, 1), (torch.bfloat16, 2)])
+def test_additive_mask(mask_dtype, mask_b):
+    c = workloads.DenseCase(B=2, Hq=4, Hkv=2, Lq=70, Lkv=300, D=128, causal=False, sigma=0.5)
+    mask = workloads.additive_mask(mask_b, c.Lq, c.Lkv, seed=9, p_masked=0.3, dtype=mask_dtype)
+    mask[..., 5, :] = float("-inf")  # a fully masked query row
+    out, lse, ro, rl = _run(c, mask=mask)
+    check(out, lse, ro, rl, what="mask")
+
+
+def test_fp16_inputs():
+    c = workloads.DenseCase(B=1, Hq=4, Hkv=1, Lq=150, Lkv=400, D=128, causal=True,
+                            dtype=torch.float16, sigma=0.5)
+    out, lse, ro, rl = _run(c)
+    assert out.dtype == torch.float16
+    check(out, lse, ro, rl, what="fp16")
+
+
+def test_empty_kv():
+    c = workloads.DenseCase(B=1, Hq=2, Hkv=2, Lq=5, Lkv=0, D=64, causal=False)
+    out, lse, ro, rl = _run(c)
+    assert torch.all(out == 0) and torch.all(lse == -math.inf)
+
+
+def _sample_rows(total, n, seed):
+    g = torch.Generator().manual_seed(seed)
+    rows = torch.randperm(total, generator=g)[:n]
+    return torch.sort(rows).values.tolist()
+
+
+def test_gqa_prefill_chunk_full_size_sampled():
+    """Llama-8B-like chunk: Hq=32, Hkv=8, D=128, Lq=512 at 15872..16383 of a 16K cache."""
+    c = workloads.gqa_prefill_chunk()
+    total = c.B * c.Hq * c.Lq
+    rows = _sample_rows(total, 192, seed=21) + [0, total - 1]
+    out, lse, ro, rl = _run(c, rows=rows)
+    check(out, lse, ro, rl, what="gqa prefill chunk (sampled)")
+
+
+@pytest.mark.parametrize("Lq", workloads.MQA_SWEEP_LQ)
+def test_mqa_sweep_full_size_sampled(Lq):
+    c = workloads.mqa_prefill(Lq)
+    total = c.B * c.Hq * c.Lq
+    rows = _sample_rows(total, min(total, 96), seed=Lq)
+    out, lse, ro, rl = _run(c, rows=rows)
+    check(out, lse, ro, rl, what=f"mqa Lq={Lq} (sampled)")
