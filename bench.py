@@ -1,0 +1,519 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused softmax-attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--quick]
+
+One step = one call of the Llama-8B-like grouped-query prefill chunk (B=1, Hq=32, Hkv=8,
+D=128, Lq=512 queries at positions 15872..16383 of a 16K-token bf16 KV cache, causal) through
+the C ABI.  `value` is attention TFLOP/s (4*D flops per visible query-key pair per head, the
+convention the pages' FlashAttention numbers imply) over K timed steps with inputs resident
+in HBM and L2 flushed (a 512 MB write) before every step; the step is replayed from a CUDA
+graph of the C-ABI call so host enqueue time stays out of the device timing.  `e2e` is the
+same metric through the same call with pinned HOST buffers: the host-to-device copy of
+q/k/v and the device-to-host copy of out/lse are inside its timed region.
+
+The other hot paths are measured in the same run and reported under "paths": paged GQA
+decode (KV GB/s), MLA paged decode at batch 128 x 2048 and 768 x 1024 (KV GB/s), and the
+Gemma-2B-like multi-query prefill sweep (TFLOP/s).  Each carries its dominant kernel's
+roofline against MEASURED_PEAKS.json.
+
+--impl reference times the fp64 CPU oracle on the host cores on bounded samples of the same
+workload (the reference arm: this project's reference implementation is that oracle).
+With torchrun (N > 1) every rank runs its own replica of the workload (weak scaling; the
+path needs no exchange), times are max-reduced over ranks and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "attention TFLOP/s (prefill) and KV GB/s (decode) + % of GB300 roofline"
+FLUSH_BYTES = 512 << 20
+
+
+# ------------------------------------------------------------------------------------------
+# helpers
+# ------------------------------------------------------------------------------------------
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm": float(d["hbm_gbs"]), "bf16": float(d["bf16_tflops"]),
+                "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def src_hash(name: str) -> str:
+    with open(os.path.join(ROOT, "softmax_attention_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(profile: str, source: str):
+    """DRAM bytes per launch from a committed ncu summary, or None if the summary is absent
+    or was taken on a different version of the kernel source."""
+    path = os.path.join(ROOT, "profiles", profile)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_t = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    m_h = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    if not m_t or not m_h or m_h.group(1) != src_hash(source):
+        return None
+    return int(m_t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling while the timed loops run."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        max_mhz = max(r[1] for r in rows)
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max_mhz,
+                "reasons": reasons, "samples": len(loaded)}
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        dev = torch.device("cuda", self.local) if torch.cuda.is_available() else torch.device("cpu")
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def time_graph(fn, steps: int, warmup: int, flush, dist: Dist):
+    """W eager warm-up calls, then K steps: flush L2 (untimed), replay a CUDA graph of `fn`
+    between two events on the current stream.  Returns (per-step ms list, wall seconds,
+    launch mode)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    mode = "graph"
+    graph = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(graph):
+            fn()
+        torch.cuda.synchronize()
+        run = graph.replay
+    except Exception:  # noqa: BLE001 - fall back to eager launches
+        mode = "eager"
+        torch.cuda.synchronize()
+        run = fn
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s, e in ev:
+        flush()
+        s.record()
+        run()
+        e.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    wall = time.perf_counter() - t0
+    return [s.elapsed_time(e) for s, e in ev], wall, mode
+
+
+def roofline(bound, achieved, peak, unit, traffic, pk):
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "peak_source": f"{pk['source']} ({'burst' if unit == 'TFLOP/s' else 'copy'})"}
+
+
+# ------------------------------------------------------------------------------------------
+# workloads on the GPU
+# ------------------------------------------------------------------------------------------
+def prefill_flops(c: workloads.DenseCase) -> float:
+    pairs = workloads.causal_pairs(c.Lq, c.Lkv) if c.causal else c.Lq * c.Lkv
+    return 4.0 * c.D * pairs * c.Hq * c.B
+
+
+def bench_prefill(fa, c, steps, warmup, flush, dist, pk, e2e=False):
+    dev = torch.device("cuda")
+    q, k, v = workloads.dense_inputs(c)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    out = torch.empty_like(qd)
+    lse = torch.empty(c.B, c.Hq, c.Lq, dtype=torch.float32, device=dev)
+    nbytes = fa.prefill_workspace_size(qd, kd, vd, causal=c.causal, scale=c.sm_scale)
+    splits = fa.prefill_num_splits(qd, kd, vd, causal=c.causal, scale=c.sm_scale)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+
+    def call():
+        fa.fa_prefill_ex(qd, kd, vd, causal=c.causal, scale=c.sm_scale, out=out, lse=lse,
+                         workspace=ws)
+
+    ms, wall, mode = time_graph(call, steps, warmup, flush, dist)
+    flops = prefill_flops(c)
+    mean_ms = dist.max(statistics.mean(ms))
+    res = {"ms": mean_ms, "tflops": flops / (mean_ms * 1e-3) / 1e12, "flops": flops,
+           "splits": splits, "launches_per_step": 1 + (splits > 1), "mode": mode,
+           "wall_s": dist.max(wall), "p10_ms": sorted(ms)[len(ms) // 10],
+           "p90_ms": sorted(ms)[(9 * len(ms)) // 10]}
+    if e2e:
+        qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(max(3, steps // 4))]
+        for i in range(warmup + len(evs)):
+            timed = i >= warmup
+            if timed:
+                s, e = evs[i - warmup]
+                flush()
+                s.record()
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            call()
+            oh.copy_(out, non_blocking=True)
+            lh.copy_(lse, non_blocking=True)
+            if timed:
+                e.record()
+        torch.cuda.synchronize()
+        e2e_ms = dist.max(statistics.mean(s.elapsed_time(e) for s, e in evs))
+        res["e2e"] = {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                      "ms_per_step": round(e2e_ms, 4),
+                      "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (q, k, v)),
+                      "d2h_bytes_per_step": out.numel() * out.element_size() + lse.numel() * 4}
+    torch.cuda.synchronize()
+    del qd, kd, vd, out, lse, ws
+    return res
+
+
+def decode_bytes(c: workloads.PagedCase, lens) -> dict:
+    L = lens.long()
+    kv = int(L.sum()) * c.Hkv * c.D * 2 * 2
+    pages = int(((L + c.page_size - 1) // c.page_size).sum()) * 4
+    q = c.B * c.Hq * c.D * 2
+    out = c.B * c.Hq * c.D * 2 + c.B * c.Hq * 4
+    return {"kv": kv, "kernel": kv + pages + q + c.B * 4, "total": kv + pages + q + out + c.B * 4}
+
+
+def bench_decode(fa, c, steps, warmup, flush, dist, pk):
+    dev = torch.device("cuda")
+    q, kp, vp, table, lens = workloads.paged_inputs(c)
+    qd, kd, vd, td, ld = (t.to(dev) for t in (q, kp, vp, table, lens))
+    max_len = int(lens.max())
+    out = torch.empty_like(qd)
+    lse = torch.empty(c.B, c.Hq, dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.fa_decode_workspace_size(c.B, c.Hq, c.D, max_len), dtype=torch.uint8,
+                     device=dev)
+    chunk = fa.fa_decode_chunk_tokens(c.B, c.Hq, max_len)
+    n_chunks = -(-max_len // chunk)
+    op = torch.empty(c.B * c.Hq, n_chunks, c.D, dtype=torch.float32, device=dev)
+    ol = torch.empty(c.B * c.Hq, n_chunks, dtype=torch.float32, device=dev)
+
+    def full():
+        fa.fa_decode_paged(qd, kd, vd, td, ld, max_len, c.sm_scale, out=out, lse=lse, workspace=ws)
+
+    def states():
+        fa.fa_decode_paged_states(qd, kd, vd, td, ld, max_len, c.sm_scale, o_parts=op, lse_parts=ol)
+
+    b = decode_bytes(c, lens)
+    ms_k, _, _ = time_graph(states, steps, warmup, flush, dist)
+    ms_f, _, mode = time_graph(full, steps, warmup, flush, dist)
+    k_ms, f_ms = dist.max(statistics.mean(ms_k)), dist.max(statistics.mean(ms_f))
+    res = {"value": round(b["total"] / (f_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+           "ms": round(f_ms, 4), "bytes": b["total"], "chunk": chunk, "mode": mode,
+           "launches_per_step": 2,
+           "roofline": roofline("hbm", b["kernel"] / (k_ms * 1e-3) / 1e9, pk["hbm"], "GB/s",
+                                profiled_traffic("decode_paged_gqa.md", "decode.cu"), pk),
+           "kernel_ms": round(k_ms, 4)}
+    del qd, kd, vd, td, ld, out, lse, ws, op, ol
+    torch.cuda.empty_cache()
+    return res
+
+
+def mla_bytes(c: workloads.MlaCase) -> dict:
+    T = sum(c.lens())
+    kv = T * (c.Dc + c.Dr) * 2
+    pages = sum(-(-n // c.page_size) for n in c.lens()) * 4
+    q = c.B * c.H * (c.Dc + c.Dr) * 2
+    out = c.B * c.H * c.Dc * 2 + c.B * c.H * 4
+    return {"kv": kv, "kernel": kv + pages + q + c.B * 4, "total": kv + pages + q + out + c.B * 4}
+
+
+def bench_mla(fa, c, steps, warmup, flush, dist, pk):
+    dev = torch.device("cuda")
+    qn, qp, ckv, kpe, table, lens = workloads.mla_inputs(c)
+    qnd, qpd, cd, kd, td, ld = (t.to(dev) for t in (qn, qp, ckv, kpe, table, lens))
+    max_len = c.max_len
+    out = torch.empty_like(qnd)
+    lse = torch.empty(c.B, c.H, dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.mla_decode_workspace_size(c.B, c.H, c.Dc, max_len), dtype=torch.uint8,
+                     device=dev)
+    chunk = fa.mla_decode_chunk_tokens(c.B, c.H, max_len)
+    n_chunks = -(-max_len // chunk)
+    op = torch.empty(c.B * c.H, n_chunks, c.Dc, dtype=torch.float32, device=dev)
+    ol = torch.empty(c.B * c.H, n_chunks, dtype=torch.float32, device=dev)
+
+    def full():
+        fa.mla_decode_paged(qnd, qpd, cd, kd, td, ld, max_len, c.scale, out=out, lse=lse,
+                            workspace=ws)
+
+    def states():
+        fa.mla_decode_paged_states(qnd, qpd, cd, kd, td, ld, max_len, c.scale, o_parts=op,
+                                   lse_parts=ol)
+
+    b = mla_bytes(c)
+    ms_k, _, _ = time_graph(states, steps, warmup, flush, dist)
+    ms_f, _, mode = time_graph(full, steps, warmup, flush, dist)
+    k_ms, f_ms = dist.max(statistics.mean(ms_k)), dist.max(statistics.mean(ms_f))
+    res = {"value": round(b["total"] / (f_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+           "ms": round(f_ms, 4), "bytes": b["total"], "chunk": chunk, "mode": mode,
+           "launches_per_step": 2,
+           "roofline": roofline("hbm", b["kernel"] / (k_ms * 1e-3) / 1e9, pk["hbm"], "GB/s",
+                                profiled_traffic(f"mla_decode_b{c.B}.md", "mla.cu"), pk),
+           "kernel_ms": round(k_ms, 4)}
+    del qnd, qpd, cd, kd, td, ld, out, lse, ws, op, ol
+    torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ------------------------------------------------------------------------------------------
+def oracle_rate(c: workloads.DenseCase, q, k, v, n_rows: int, offset: int = 0):
+    """Time the fp64 oracle on n_rows query rows of the workload (spread over heads and
+    queries); returns (seconds, flops)."""
+    import oracle
+    total = c.B * c.Hq * c.Lq
+    stride = max(1, total // max(1, n_rows))
+    rows = [((offset + r * stride) % total) for r in range(n_rows)]
+    off = c.Lkv - c.Lq
+    flops = 0.0
+    for r in rows:
+        i = r % c.Lq
+        keys = min(c.Lkv, i + off + 1) if c.causal else c.Lkv
+        flops += 4.0 * c.D * max(0, keys)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, causal=c.causal, scale=c.sm_scale, rows=rows)
+    return time.perf_counter() - t0, flops
+
+
+def cpu_baseline(c, budget_s: float = 12.0):
+    import oracle
+    q, k, v = workloads.dense_inputs(c)
+    dt, fl = oracle_rate(c, q, k, v, 32)
+    n = int(max(32, min(8192, 32 * budget_s / max(dt, 1e-3))))
+    dt, fl = oracle_rate(c, q, k, v, n, offset=7)
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n} of {c.B * c.Hq * c.Lq} query rows (strided over heads and "
+                      f"queries), all their visible keys; {dt:.1f} s"}
+
+
+def run_reference(args, dist: Dist):
+    if dist.rank != 0:
+        return
+    import oracle
+    c = workloads.gqa_prefill_chunk()
+    q, k, v = workloads.dense_inputs(c)
+    dt, fl = oracle_rate(c, q, k, v, 16)
+    per_row = dt / 16
+    total_steps = args.steps + args.warmup
+    rows_per_step = int(max(1, min(4096, 120.0 / max(1e-6, per_row) / total_steps)))
+    for w in range(args.warmup):
+        oracle_rate(c, q, k, v, rows_per_step, offset=w)
+    t_sum, f_sum = 0.0, 0.0
+    for s in range(args.steps):
+        dt, fl = oracle_rate(c, q, k, v, rows_per_step, offset=1000 + s * 13)
+        t_sum += dt
+        f_sum += fl
+    value = f_sum / t_sum / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t_sum / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "gqa_prefill_chunk: B=1 Hq=32 Hkv=8 D=128 Lq=512 Lkv=16384 "
+                               "causal bf16 inputs", "sample_rows_per_step": rows_per_step},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{rows_per_step} query rows per step of "
+                                   f"{c.B * c.Hq * c.Lq}, all their visible keys"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--quick", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist)
+            return
+        import softmax_attention_gb300 as fa
+        torch.cuda.set_device(dist.local)
+        fa.load_library()
+        pk = peaks()
+        flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+        def flush():
+            flush_buf.zero_()
+
+        clocks = ClockSampler(dist.local)
+        clocks.start()
+        c = workloads.gqa_prefill_chunk(seed=1 + dist.rank)
+        head = bench_prefill(fa, c, args.steps, args.warmup, flush, dist, pk, e2e=True)
+        paths = {}
+        if not args.quick:
+            sub = max(20, args.steps // 4)
+            pc = workloads.paged_gqa_decode(seed=1 + dist.rank)
+            paths["paged_gqa_decode"] = bench_decode(fa, pc, sub, args.warmup, flush, dist, pk)
+            for batch, seq in ((128, 2048), (768, 1024)):
+                mc = workloads.mla_decode(batch, seq, seed=1 + dist.rank)
+                try:
+                    paths[f"mla_decode_b{batch}_s{seq}"] = bench_mla(fa, mc, sub, args.warmup,
+                                                                      flush, dist, pk)
+                except fa.FAError as e:
+                    paths[f"mla_decode_b{batch}_s{seq}"] = {"unavailable": str(e)}
+            sweep = {}
+            for lq in workloads.MQA_SWEEP_LQ:
+                mc = workloads.mqa_prefill(lq, seed=1 + dist.rank)
+                r = bench_prefill(fa, mc, sub, args.warmup, flush, dist, pk)
+                bytes_ = (mc.Lq * mc.Hq * 2 + 2 * mc.Lkv * mc.Hkv) * mc.D * 2 + mc.Lq * mc.Hq * 4
+                ai = r["flops"] / bytes_
+                bound = "hbm" if ai < pk["bf16"] * 1e3 / pk["hbm"] else "tensor"
+                ach = (bytes_ / (r["ms"] * 1e-3) / 1e9) if bound == "hbm" else r["tflops"]
+                sweep[str(lq)] = {"value": round(r["tflops"], 2), "unit": "TFLOP/s",
+                                  "ms": round(r["ms"], 4), "splits": r["splits"],
+                                  "roofline": roofline(bound, ach,
+                                                       pk["hbm"] if bound == "hbm" else pk["bf16"],
+                                                       "GB/s" if bound == "hbm" else "TFLOP/s",
+                                                       None, pk)}
+            paths["mqa_prefill_sweep"] = sweep
+        clk = clocks.stop() if dist.rank == 0 else None
+        flops = head["flops"]
+        total_tflops = dist.world * flops / (head["ms"] * 1e-3) / 1e12
+        cpu = None
+        if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
+            cpu = cpu_baseline(c)
+        if dist.rank == 0:
+            traffic = profiled_traffic("prefill_gqa_chunk.md", "prefill.cu")
+            line = {
+                "metric": METRIC, "value": round(total_tflops, 2), "unit": "TFLOP/s",
+                "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(head["ms"], 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": "gqa_prefill_chunk: B=1 Hq=32 Hkv=8 D=128 Lq=512 "
+                                       "(positions 15872..16383) Lkv=16384 causal, bf16 "
+                                       "N(0,1)*0.5, scale 1/sqrt(128)",
+                           "flops_per_step": flops, "kv_splits": head["splits"],
+                           "l2": "flushed (512 MB write) before every timed step",
+                           "launch": head["mode"], "parallelism": f"replica x{dist.world}"},
+                "roofline": roofline("tensor", flops / (head["ms"] * 1e-3) / 1e12, pk["bf16"],
+                                     "TFLOP/s", traffic, pk),
+                "cpu_baseline": cpu,
+                "e2e": head["e2e"],
+                "gpu_launches": head["launches_per_step"] * args.steps,
+                "clocks": clk,
+                "p10_ms": round(head["p10_ms"], 4), "p90_ms": round(head["p90_ms"], 4),
+                "paths": paths,
+            }
+            print(json.dumps(line), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -85,7 +85,8 @@ typedef struct fa_prefill_args {
 int fa_prefill_ex(const fa_prefill_args* args, void* stream);
 
 /* Workspace bytes fa_prefill_ex needs for these arguments on the current device (0 when
- * the plan needs none).  Depends only on sizes, dtype and num_splits. */
+ * the plan needs none).  Depends only on sizes, dtype and num_splits; the pointer fields
+ * are not read. */
 size_t fa_prefill_workspace_size(const fa_prefill_args* args);
 
 /* The split count fa_prefill_ex will use for these arguments on the current device. */
@@ -114,6 +115,27 @@ int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
 
 size_t fa_decode_workspace_size(int B, int Hq, int D, int max_seq_len);
 
+/* Tokens per split-KV chunk that fa_decode_paged uses for these sizes on the current device
+ * (a multiple of 64; depends only on B, Hq, max_seq_len and the SM count). */
+int fa_decode_chunk_tokens(int B, int Hq, int max_seq_len);
+
+/*
+ * fa_decode_paged without the final merge: writes the split-KV state of every query row
+ * r = b*Hq + h and chunk c (tokens [c*chunk, (c+1)*chunk) of the sequence, chunk =
+ * fa_decode_chunk_tokens(B, Hq, max_seq_len)): the normalised partial output
+ * o_parts[r, c, :] (fp32) and its log-sum-exp lse_parts[r, c] (natural log).  Chunks at or
+ * past seq_lens[b] are not written.  fa_merge_states with n_splits[r] =
+ * ceil(seq_lens[b] / chunk) combines them; these states are also what a merge across
+ * devices holding different key ranges would exchange.
+ *   o_parts [B*Hq, n_chunks, D] fp32, lse_parts [B*Hq, n_chunks] fp32 with
+ *   n_chunks = ceil(max_seq_len / chunk), passed for checking.
+ */
+int fa_decode_paged_states(const void* q, const void* k_pages, const void* v_pages,
+                           const int32_t* page_table, const int32_t* seq_lens, float* o_parts,
+                           float* lse_parts, int n_chunks, int B, int Hq, int Hkv, int D,
+                           int page_size, int max_pages_per_seq, int num_pages, int max_seq_len,
+                           float scale, void* stream);
+
 /*
  * MLA paged decode in the latent (absorbed) form: the compressed ckv matrix serves as both
  * K and V and a separate rope part kpe adds q_pe . kpe_t to each score (flashinfer PR
@@ -133,6 +155,19 @@ int mla_decode_paged(const void* q_nope, const void* q_pe, const void* ckv_pages
                      void* workspace, size_t workspace_bytes, void* stream);
 
 size_t mla_decode_workspace_size(int B, int H, int Dc, int max_seq_len);
+
+/* Tokens per split-KV chunk that mla_decode_paged uses (a multiple of the kernel's tile). */
+int mla_decode_chunk_tokens(int B, int H, int max_seq_len);
+
+/* mla_decode_paged without the final merge (same contract as fa_decode_paged_states):
+ *   o_parts [B*H, n_chunks, Dc] fp32, lse_parts [B*H, n_chunks] fp32,
+ *   n_chunks = ceil(max_seq_len / mla_decode_chunk_tokens(B, H, max_seq_len)). */
+int mla_decode_paged_states(const void* q_nope, const void* q_pe, const void* ckv_pages,
+                            const void* kpe_pages, const int32_t* page_table,
+                            const int32_t* seq_lens, float* o_parts, float* lse_parts,
+                            int n_chunks, int B, int H, int Dc, int Dr, int page_size,
+                            int max_pages_per_seq, int num_pages, int max_seq_len, float scale,
+                            void* stream);
 
 /*
  * Merge of attention states over disjoint key sets (the split-KV combine):

@@ -32,9 +32,10 @@ _DT = {torch.bfloat16: FA_BF16, torch.float16: FA_FP16, torch.float32: FA_FP32}
 # Every symbol include/fa.h declares.
 EXPORTS = (
     "fa_prefill", "fa_prefill_ex", "fa_prefill_workspace_size", "fa_prefill_num_splits",
-    "fa_decode_paged", "fa_decode_workspace_size", "mla_decode_paged",
-    "mla_decode_workspace_size", "fa_merge_states", "fa_get_device_status", "fa_last_error",
-    "fa_version",
+    "fa_decode_paged", "fa_decode_workspace_size", "fa_decode_chunk_tokens",
+    "fa_decode_paged_states", "mla_decode_paged", "mla_decode_workspace_size",
+    "mla_decode_chunk_tokens", "mla_decode_paged_states", "fa_merge_states",
+    "fa_get_device_status", "fa_last_error", "fa_version",
 )
 
 
@@ -84,6 +85,14 @@ def load_library(path: str | None = None):
         lib.fa_decode_paged.argtypes = [_vp] * 7 + [_i] * 8 + [_f, _vp, _sz, _vp]
         lib.fa_decode_workspace_size.restype = _sz
         lib.fa_decode_workspace_size.argtypes = [_i] * 4
+        lib.fa_decode_chunk_tokens.restype = _i
+        lib.fa_decode_chunk_tokens.argtypes = [_i] * 3
+        lib.fa_decode_paged_states.restype = _i
+        lib.fa_decode_paged_states.argtypes = [_vp] * 7 + [_i] * 9 + [_f, _vp]
+        lib.mla_decode_chunk_tokens.restype = _i
+        lib.mla_decode_chunk_tokens.argtypes = [_i] * 3
+        lib.mla_decode_paged_states.restype = _i
+        lib.mla_decode_paged_states.argtypes = [_vp] * 8 + [_i] * 9 + [_f, _vp]
         lib.mla_decode_paged.restype = _i
         lib.mla_decode_paged.argtypes = [_vp] * 8 + [_i] * 8 + [_f, _vp, _sz, _vp]
         lib.mla_decode_workspace_size.restype = _sz
@@ -230,6 +239,60 @@ def fa_decode_paged(q, k_pages, v_pages, page_table, seq_lens, max_seq_len: int,
                                page_table.shape[1], num_pages, int(max_seq_len), float(scale),
                                _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
     return out, lse
+
+
+def fa_decode_chunk_tokens(B, Hq, max_seq_len) -> int:
+    return load_library().fa_decode_chunk_tokens(B, Hq, max_seq_len)
+
+
+def fa_decode_paged_states(q, k_pages, v_pages, page_table, seq_lens, max_seq_len: int,
+                           scale: float | None = None, o_parts=None, lse_parts=None, stream=None):
+    """Per-chunk split-KV states of paged decode (no merge).  Returns (o_parts
+    [B*Hq, n_chunks, D] fp32, lse_parts [B*Hq, n_chunks] fp32, chunk)."""
+    lib = load_library()
+    _need_cuda(q, k_pages, v_pages, page_table, seq_lens)
+    B, Hq, D = q.shape
+    num_pages, Hkv, page_size, _ = k_pages.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    chunk = lib.fa_decode_chunk_tokens(B, Hq, max_seq_len)
+    n = -(-max_seq_len // chunk)
+    if o_parts is None:
+        o_parts = torch.empty(B * Hq, n, D, dtype=torch.float32, device=q.device)
+    if lse_parts is None:
+        lse_parts = torch.empty(B * Hq, n, dtype=torch.float32, device=q.device)
+    _check(lib.fa_decode_paged_states(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                      _ptr(seq_lens), _ptr(o_parts), _ptr(lse_parts), n, B, Hq,
+                                      Hkv, D, page_size, page_table.shape[1], num_pages,
+                                      int(max_seq_len), float(scale), _stream(stream)))
+    return o_parts, lse_parts, chunk
+
+
+def mla_decode_chunk_tokens(B, H, max_seq_len) -> int:
+    return load_library().mla_decode_chunk_tokens(B, H, max_seq_len)
+
+
+def mla_decode_paged_states(q_nope, q_pe, ckv, kpe, page_table, seq_lens, max_seq_len: int,
+                            scale: float, o_parts=None, lse_parts=None, stream=None):
+    """Per-chunk split-KV states of MLA decode (no merge).  Returns (o_parts, lse_parts,
+    chunk)."""
+    lib = load_library()
+    _need_cuda(q_nope, q_pe, ckv, kpe, page_table, seq_lens)
+    B, H, Dc = q_nope.shape
+    Dr = q_pe.shape[2]
+    num_pages, page_size = ckv.shape[0], ckv.shape[1]
+    chunk = lib.mla_decode_chunk_tokens(B, H, max_seq_len)
+    n = -(-max_seq_len // chunk)
+    if o_parts is None:
+        o_parts = torch.empty(B * H, n, Dc, dtype=torch.float32, device=q_nope.device)
+    if lse_parts is None:
+        lse_parts = torch.empty(B * H, n, dtype=torch.float32, device=q_nope.device)
+    _check(lib.mla_decode_paged_states(_ptr(q_nope), _ptr(q_pe), _ptr(ckv), _ptr(kpe),
+                                       _ptr(page_table), _ptr(seq_lens), _ptr(o_parts),
+                                       _ptr(lse_parts), n, B, H, Dc, Dr, page_size,
+                                       page_table.shape[1], num_pages, int(max_seq_len),
+                                       float(scale), _stream(stream)))
+    return o_parts, lse_parts, chunk
 
 
 def mla_decode_workspace_size(B, H, Dc, max_seq_len) -> int:

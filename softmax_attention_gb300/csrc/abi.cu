@@ -9,6 +9,8 @@
 #include <string.h>
 
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "../../include/fa.h"
 #include "internal.h"
@@ -69,6 +71,19 @@ uint32_t* device_status_ptr() {
   return g_status_ptr[dev];
 }
 
+int current_device_index() { return current_device(); }
+
+cudaError_t ensure_smem_limit_fn(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({kernel, dev})) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({kernel, dev});
+  return e;
+}
+
 int num_sms() {
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return 0;
@@ -120,7 +135,7 @@ struct PrefillPlan {
   size_t off_o, off_lse, off_q, off_k, off_v;
 };
 
-int validate_prefill(const fa_prefill_args* a) {
+int validate_prefill(const fa_prefill_args* a, bool check_pointers = true) {
   if (!a) return fail(FA_ERR_INVALID_ARG, "fa_prefill: null argument struct");
   if (a->B < 0 || a->Lq < 0 || a->Lkv < 0)
     return fail(FA_ERR_INVALID_ARG, "fa_prefill: B, Lq, Lkv must be >= 0 (got %d, %d, %d)", a->B,
@@ -140,19 +155,20 @@ int validate_prefill(const fa_prefill_args* a) {
   if (!(a->scale == a->scale) || isinf(a->scale))
     return fail(FA_ERR_INVALID_ARG, "fa_prefill: scale must be finite");
   const bool work = a->B > 0 && a->Lq > 0;
-  if (work) {
+  if (work && a->mask) {
+    if (a->mask_batches != 1 && a->mask_batches != a->B)
+      return fail(FA_ERR_INVALID_ARG, "fa_prefill: mask_batches must be 1 or B (got %d)",
+                  a->mask_batches);
+    if (a->mask_dtype != FA_FP32 && a->mask_dtype != FA_BF16)
+      return fail(FA_ERR_UNSUPPORTED, "fa_prefill: mask dtype must be FA_FP32 or FA_BF16");
+  }
+  if (work && a->num_splits < 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_prefill: num_splits must be >= 0");
+  if (work && check_pointers) {
     if (!a->q || !a->out || (a->Lkv > 0 && (!a->k || !a->v)))
       return fail(FA_ERR_INVALID_ARG, "fa_prefill: null q/k/v/out pointer");
     if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->out))
       return fail(FA_ERR_INVALID_ARG, "fa_prefill: q, k, v and out must be 16-byte aligned");
-    if (a->mask) {
-      if (a->mask_batches != 1 && a->mask_batches != a->B)
-        return fail(FA_ERR_INVALID_ARG, "fa_prefill: mask_batches must be 1 or B (got %d)",
-                    a->mask_batches);
-      if (a->mask_dtype != FA_FP32 && a->mask_dtype != FA_BF16)
-        return fail(FA_ERR_UNSUPPORTED, "fa_prefill: mask dtype must be FA_FP32 or FA_BF16");
-    }
-    if (a->num_splits < 0) return fail(FA_ERR_INVALID_ARG, "fa_prefill: num_splits must be >= 0");
   }
   return FA_OK;
 }
@@ -332,13 +348,13 @@ int fa_prefill_ex(const fa_prefill_args* args, void* stream) {
 }
 
 size_t fa_prefill_workspace_size(const fa_prefill_args* args) {
-  if (validate_prefill(args) != FA_OK) return 0;
+  if (validate_prefill(args, false) != FA_OK) return 0;
   if (args->B == 0 || args->Lq == 0) return 0;
   return plan_prefill(args).total_bytes;
 }
 
 int fa_prefill_num_splits(const fa_prefill_args* args) {
-  if (validate_prefill(args) != FA_OK) return 0;
+  if (validate_prefill(args, false) != FA_OK) return 0;
   if (args->B == 0 || args->Lq == 0) return 1;
   return plan_prefill(args).n_splits;
 }
@@ -349,11 +365,18 @@ size_t fa_decode_workspace_size(int B, int Hq, int D, int max_seq_len) {
   return split_ws_bytes((long)B * Hq, (max_seq_len + chunk - 1) / chunk, D);
 }
 
-int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
-                    const int32_t* page_table, const int32_t* seq_lens, void* out, float* lse,
-                    int B, int Hq, int Hkv, int D, int page_size, int max_pages_per_seq,
-                    int num_pages, int max_seq_len, float scale, void* workspace,
-                    size_t workspace_bytes, void* stream) {
+int fa_decode_chunk_tokens(int B, int Hq, int max_seq_len) {
+  return decode_chunk(B > 0 ? B : 1, Hq > 0 ? Hq : 1, max_seq_len > 0 ? max_seq_len : 1);
+}
+
+}  // extern "C"
+
+namespace fa {
+namespace {
+
+int check_decode(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                 const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int page_size,
+                 int max_pages_per_seq, int num_pages, int max_seq_len, float scale) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
     return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: need B >= 0, Hq, Hkv > 0, Hq %% Hkv == 0");
   const int G = Hq / Hkv;
@@ -372,80 +395,47 @@ int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
     return fail(FA_ERR_INVALID_ARG,
                 "fa_decode_paged: max_seq_len %d exceeds max_pages_per_seq*page_size", max_seq_len);
   if (Hkv > 65535 || B > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: B, Hkv <= 65535");
-  if (!(scale == scale) || isinf(scale)) return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: scale must be finite");
+  if (!(scale == scale) || isinf(scale))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: scale must be finite");
   if (B == 0) return FA_OK;
-  if (!q || !out || !seq_lens || (max_seq_len > 0 && (!k_pages || !v_pages || !page_table)))
+  if (!q || !seq_lens || (max_seq_len > 0 && (!k_pages || !v_pages || !page_table)))
     return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: null pointer");
-  if (!aligned16(q) || !aligned16(out) || !aligned16(k_pages) || !aligned16(v_pages))
-    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: q, out, k_pages, v_pages must be 16-byte aligned");
-  const int chunk = decode_chunk(B, Hq, max_seq_len > 0 ? max_seq_len : 1);
-  const int n_chunks = max_seq_len > 0 ? (max_seq_len + chunk - 1) / chunk : 1;
-  const size_t need = split_ws_bytes((long)B * Hq, n_chunks, D);
-  if (!workspace || workspace_bytes < need)
-    return fail(FA_ERR_WORKSPACE, "fa_decode_paged: workspace of %zu bytes needed (got %zu)", need,
-                workspace ? workspace_bytes : (size_t)0);
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: workspace must be 256-byte aligned");
-  uint32_t* status = device_status_ptr();
-  if (!status) return fail(FA_ERR_CUDA, "fa_decode_paged: no usable CUDA device");
-  float* o_part = static_cast<float*>(workspace);
-  float* lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                             align_up((size_t)B * Hq * n_chunks * D * sizeof(float), 256));
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (max_seq_len > 0) {
-    DecodeParams p{};
-    p.q = q;
-    p.k_pages = k_pages;
-    p.v_pages = v_pages;
-    p.page_table = page_table;
-    p.seq_lens = seq_lens;
-    p.B = B;
-    p.Hq = Hq;
-    p.Hkv = Hkv;
-    p.G = G;
-    p.D = D;
-    p.page_size = page_size;
-    p.max_pages = max_pages_per_seq;
-    p.num_pages = num_pages;
-    p.chunk = chunk;
-    p.n_chunks = n_chunks;
-    p.scale_log2 = scale * 1.44269504088896340736f;
-    p.o_part = o_part;
-    p.lse_part = lse_part;
-    p.status = status;
-    cudaError_t e = launch_decode(p, st);
-    if (e != cudaSuccess) return cuda_fail("fa_decode_paged (decode kernel)", e);
-  }
-  MergeParams m{};
-  m.o_part = o_part;
-  m.lse_part = lse_part;
-  m.seq_lens = max_seq_len > 0 ? seq_lens : nullptr;
-  m.n_splits = nullptr;
-  m.rows_per_seq = Hq;
-  m.chunk = chunk;
-  m.out = out;
-  m.lse = lse;
-  m.rows = B * Hq;
-  m.D = D;
-  m.max_splits = max_seq_len > 0 ? n_chunks : 0;
-  m.out_dtype = Dtype::BF16;
-  if (max_seq_len == 0) m.max_splits = 0;
-  cudaError_t e = launch_merge(m, st);
-  if (e != cudaSuccess) return cuda_fail("fa_decode_paged (merge kernel)", e);
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: q, k_pages, v_pages must be 16-byte aligned");
   return FA_OK;
 }
 
-size_t mla_decode_workspace_size(int B, int H, int Dc, int max_seq_len) {
-  if (B <= 0 || H <= 0 || Dc <= 0 || max_seq_len <= 0) return 0;
-  const int chunk = mla_chunk_tokens();
-  return split_ws_bytes((long)B * H, (max_seq_len + chunk - 1) / chunk, Dc);
+cudaError_t decode_states(const void* q, const void* k_pages, const void* v_pages,
+                          const int32_t* page_table, const int32_t* seq_lens, float* o_part,
+                          float* lse_part, int chunk, int n_chunks, int B, int Hq, int Hkv, int D,
+                          int page_size, int max_pages_per_seq, int num_pages, float scale,
+                          uint32_t* status, cudaStream_t st) {
+  DecodeParams p{};
+  p.q = q;
+  p.k_pages = k_pages;
+  p.v_pages = v_pages;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.D = D;
+  p.page_size = page_size;
+  p.max_pages = max_pages_per_seq;
+  p.num_pages = num_pages;
+  p.chunk = chunk;
+  p.n_chunks = n_chunks;
+  p.scale_log2 = scale * 1.44269504088896340736f;
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  p.status = status;
+  return launch_decode(p, st);
 }
 
-int mla_decode_paged(const void* q_nope, const void* q_pe, const void* ckv_pages,
-                     const void* kpe_pages, const int32_t* page_table, const int32_t* seq_lens,
-                     void* out, float* lse, int B, int H, int Dc, int Dr, int page_size,
-                     int max_pages_per_seq, int num_pages, int max_seq_len, float scale,
-                     void* workspace, size_t workspace_bytes, void* stream) {
+int check_mla(const void* q_nope, const void* q_pe, const void* ckv_pages, const void* kpe_pages,
+              const int32_t* page_table, const int32_t* seq_lens, int B, int H, int Dc, int Dr,
+              int page_size, int max_pages_per_seq, int num_pages, int max_seq_len, float scale) {
   if (B < 0 || H <= 0 || Dc <= 0 || Dr < 0)
     return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: need B >= 0, H, Dc > 0, Dr >= 0");
   if (Dc != 512 || Dr != 64 || H != 64)
@@ -457,66 +447,197 @@ int mla_decode_paged(const void* q_nope, const void* q_pe, const void* ckv_pages
   if ((long)max_pages_per_seq * page_size < max_seq_len)
     return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: max_seq_len exceeds max_pages_per_seq*page_size");
   if (B > 65535) return fail(FA_ERR_UNSUPPORTED, "mla_decode_paged: B <= 65535");
-  if (!(scale == scale) || isinf(scale)) return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: scale must be finite");
+  if (!(scale == scale) || isinf(scale))
+    return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: scale must be finite");
   if (B == 0) return FA_OK;
-  if (!q_nope || !q_pe || !out || !seq_lens ||
-      (max_seq_len > 0 && (!ckv_pages || !kpe_pages || !page_table)))
+  if (!q_nope || !q_pe || !seq_lens || (max_seq_len > 0 && (!ckv_pages || !kpe_pages || !page_table)))
     return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: null pointer");
-  if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(out) || !aligned16(ckv_pages) ||
-      !aligned16(kpe_pages))
+  if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(ckv_pages) || !aligned16(kpe_pages))
     return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: tensors must be 16-byte aligned");
-  const int chunk = mla_chunk_tokens();
-  const int n_chunks = max_seq_len > 0 ? (max_seq_len + chunk - 1) / chunk : 1;
-  const size_t need = split_ws_bytes((long)B * H, n_chunks, Dc);
-  if (!workspace || workspace_bytes < need)
-    return fail(FA_ERR_WORKSPACE, "mla_decode_paged: workspace of %zu bytes needed (got %zu)", need,
-                workspace ? workspace_bytes : (size_t)0);
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: workspace must be 256-byte aligned");
-  uint32_t* status = device_status_ptr();
-  if (!status) return fail(FA_ERR_CUDA, "mla_decode_paged: no usable CUDA device");
-  float* o_part = static_cast<float*>(workspace);
-  float* lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                             align_up((size_t)B * H * n_chunks * Dc * sizeof(float), 256));
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (max_seq_len > 0) {
-    MlaParams p{};
-    p.q_nope = q_nope;
-    p.q_pe = q_pe;
-    p.ckv = ckv_pages;
-    p.kpe = kpe_pages;
-    p.page_table = page_table;
-    p.seq_lens = seq_lens;
-    p.B = B;
-    p.H = H;
-    p.Dc = Dc;
-    p.Dr = Dr;
-    p.page_size = page_size;
-    p.max_pages = max_pages_per_seq;
-    p.num_pages = num_pages;
-    p.chunk = chunk;
-    p.n_chunks = n_chunks;
-    p.scale_log2 = scale * 1.44269504088896340736f;
-    p.o_part = o_part;
-    p.lse_part = lse_part;
-    p.status = status;
-    cudaError_t e = launch_mla(p, st);
-    if (e != cudaSuccess) return cuda_fail("mla_decode_paged (MLA kernel)", e);
-  }
+  return FA_OK;
+}
+
+cudaError_t mla_states(const void* q_nope, const void* q_pe, const void* ckv_pages,
+                       const void* kpe_pages, const int32_t* page_table, const int32_t* seq_lens,
+                       float* o_part, float* lse_part, int chunk, int n_chunks, int B, int H,
+                       int Dc, int Dr, int page_size, int max_pages_per_seq, int num_pages,
+                       float scale, uint32_t* status, cudaStream_t st) {
+  MlaParams p{};
+  p.q_nope = q_nope;
+  p.q_pe = q_pe;
+  p.ckv = ckv_pages;
+  p.kpe = kpe_pages;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.B = B;
+  p.H = H;
+  p.Dc = Dc;
+  p.Dr = Dr;
+  p.page_size = page_size;
+  p.max_pages = max_pages_per_seq;
+  p.num_pages = num_pages;
+  p.chunk = chunk;
+  p.n_chunks = n_chunks;
+  p.scale_log2 = scale * 1.44269504088896340736f;
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  p.status = status;
+  return launch_mla(p, st);
+}
+
+// Splits a caller workspace into the partial-output and partial-lse arrays.
+void carve(void* ws, long rows, int n_chunks, int D, float** o, float** l) {
+  *o = static_cast<float*>(ws);
+  *l = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                align_up((size_t)rows * n_chunks * D * sizeof(float), 256));
+}
+
+int merge_chunks(float* o_part, float* lse_part, const int32_t* seq_lens, int rows_per_seq,
+                 int chunk, int n_chunks, void* out, float* lse, int rows, int D, cudaStream_t st,
+                 const char* who) {
   MergeParams m{};
   m.o_part = o_part;
   m.lse_part = lse_part;
-  m.seq_lens = max_seq_len > 0 ? seq_lens : nullptr;
-  m.rows_per_seq = H;
+  m.seq_lens = n_chunks > 0 ? seq_lens : nullptr;
+  m.rows_per_seq = rows_per_seq;
   m.chunk = chunk;
   m.out = out;
   m.lse = lse;
-  m.rows = B * H;
-  m.D = Dc;
-  m.max_splits = max_seq_len > 0 ? n_chunks : 0;
+  m.rows = rows;
+  m.D = D;
+  m.max_splits = n_chunks;
   m.out_dtype = Dtype::BF16;
   cudaError_t e = launch_merge(m, st);
-  if (e != cudaSuccess) return cuda_fail("mla_decode_paged (merge kernel)", e);
+  if (e != cudaSuccess) return cuda_fail(who, e);
+  return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                    const int32_t* page_table, const int32_t* seq_lens, void* out, float* lse,
+                    int B, int Hq, int Hkv, int D, int page_size, int max_pages_per_seq,
+                    int num_pages, int max_seq_len, float scale, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  int rc = check_decode(q, k_pages, v_pages, page_table, seq_lens, B, Hq, Hkv, D, page_size,
+                        max_pages_per_seq, num_pages, max_seq_len, scale);
+  if (rc != FA_OK || B == 0) return rc;
+  if (!out || !aligned16(out)) return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: out must be a 16-byte aligned pointer");
+  const int chunk = decode_chunk(B, Hq, max_seq_len > 0 ? max_seq_len : 1);
+  const int n_chunks = max_seq_len > 0 ? (max_seq_len + chunk - 1) / chunk : 0;
+  const size_t need = n_chunks > 0 ? split_ws_bytes((long)B * Hq, n_chunks, D) : 0;
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(FA_ERR_WORKSPACE, "fa_decode_paged: workspace of %zu bytes needed (got %zu)", need,
+                workspace ? workspace_bytes : (size_t)0);
+  if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: workspace must be 256-byte aligned");
+  uint32_t* status = device_status_ptr();
+  if (!status) return fail(FA_ERR_CUDA, "fa_decode_paged: no usable CUDA device");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float *o_part = nullptr, *lse_part = nullptr;
+  if (n_chunks > 0) {
+    carve(workspace, (long)B * Hq, n_chunks, D, &o_part, &lse_part);
+    cudaError_t e = decode_states(q, k_pages, v_pages, page_table, seq_lens, o_part, lse_part,
+                                  chunk, n_chunks, B, Hq, Hkv, D, page_size, max_pages_per_seq,
+                                  num_pages, scale, status, st);
+    if (e != cudaSuccess) return cuda_fail("fa_decode_paged (decode kernel)", e);
+  }
+  return merge_chunks(o_part, lse_part, seq_lens, Hq, chunk, n_chunks, out, lse, B * Hq, D, st,
+                      "fa_decode_paged (merge kernel)");
+}
+
+int fa_decode_paged_states(const void* q, const void* k_pages, const void* v_pages,
+                           const int32_t* page_table, const int32_t* seq_lens, float* o_parts,
+                           float* lse_parts, int n_chunks, int B, int Hq, int Hkv, int D,
+                           int page_size, int max_pages_per_seq, int num_pages, int max_seq_len,
+                           float scale, void* stream) {
+  int rc = check_decode(q, k_pages, v_pages, page_table, seq_lens, B, Hq, Hkv, D, page_size,
+                        max_pages_per_seq, num_pages, max_seq_len, scale);
+  if (rc != FA_OK || B == 0 || max_seq_len == 0) return rc;
+  const int chunk = decode_chunk(B, Hq, max_seq_len);
+  const int want = (max_seq_len + chunk - 1) / chunk;
+  if (n_chunks != want)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged_states: n_chunks must be %d (got %d)", want,
+                n_chunks);
+  if (!o_parts || !lse_parts || !aligned16(o_parts))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged_states: o_parts/lse_parts missing or misaligned");
+  uint32_t* status = device_status_ptr();
+  if (!status) return fail(FA_ERR_CUDA, "fa_decode_paged_states: no usable CUDA device");
+  cudaError_t e = decode_states(q, k_pages, v_pages, page_table, seq_lens, o_parts, lse_parts,
+                                chunk, n_chunks, B, Hq, Hkv, D, page_size, max_pages_per_seq,
+                                num_pages, scale, status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("fa_decode_paged_states", e);
+  return FA_OK;
+}
+
+size_t mla_decode_workspace_size(int B, int H, int Dc, int max_seq_len) {
+  if (B <= 0 || H <= 0 || Dc <= 0 || max_seq_len <= 0) return 0;
+  const int chunk = mla_chunk_tokens(B, H, max_seq_len);
+  return split_ws_bytes((long)B * H, (max_seq_len + chunk - 1) / chunk, Dc);
+}
+
+int mla_decode_chunk_tokens(int B, int H, int max_seq_len) {
+  return mla_chunk_tokens(B > 0 ? B : 1, H > 0 ? H : 1, max_seq_len > 0 ? max_seq_len : 1);
+}
+
+int mla_decode_paged(const void* q_nope, const void* q_pe, const void* ckv_pages,
+                     const void* kpe_pages, const int32_t* page_table, const int32_t* seq_lens,
+                     void* out, float* lse, int B, int H, int Dc, int Dr, int page_size,
+                     int max_pages_per_seq, int num_pages, int max_seq_len, float scale,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_mla(q_nope, q_pe, ckv_pages, kpe_pages, page_table, seq_lens, B, H, Dc, Dr,
+                     page_size, max_pages_per_seq, num_pages, max_seq_len, scale);
+  if (rc != FA_OK || B == 0) return rc;
+  if (!out || !aligned16(out)) return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: out must be a 16-byte aligned pointer");
+  const int chunk = mla_chunk_tokens(B, H, max_seq_len > 0 ? max_seq_len : 1);
+  const int n_chunks = max_seq_len > 0 ? (max_seq_len + chunk - 1) / chunk : 0;
+  const size_t need = n_chunks > 0 ? split_ws_bytes((long)B * H, n_chunks, Dc) : 0;
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(FA_ERR_WORKSPACE, "mla_decode_paged: workspace of %zu bytes needed (got %zu)", need,
+                workspace ? workspace_bytes : (size_t)0);
+  if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: workspace must be 256-byte aligned");
+  uint32_t* status = device_status_ptr();
+  if (!status) return fail(FA_ERR_CUDA, "mla_decode_paged: no usable CUDA device");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float *o_part = nullptr, *lse_part = nullptr;
+  if (n_chunks > 0) {
+    carve(workspace, (long)B * H, n_chunks, Dc, &o_part, &lse_part);
+    cudaError_t e = mla_states(q_nope, q_pe, ckv_pages, kpe_pages, page_table, seq_lens, o_part,
+                               lse_part, chunk, n_chunks, B, H, Dc, Dr, page_size,
+                               max_pages_per_seq, num_pages, scale, status, st);
+    if (e != cudaSuccess) return cuda_fail("mla_decode_paged (MLA kernel)", e);
+  }
+  return merge_chunks(o_part, lse_part, seq_lens, H, chunk, n_chunks, out, lse, B * H, Dc, st,
+                      "mla_decode_paged (merge kernel)");
+}
+
+int mla_decode_paged_states(const void* q_nope, const void* q_pe, const void* ckv_pages,
+                            const void* kpe_pages, const int32_t* page_table,
+                            const int32_t* seq_lens, float* o_parts, float* lse_parts,
+                            int n_chunks, int B, int H, int Dc, int Dr, int page_size,
+                            int max_pages_per_seq, int num_pages, int max_seq_len, float scale,
+                            void* stream) {
+  int rc = check_mla(q_nope, q_pe, ckv_pages, kpe_pages, page_table, seq_lens, B, H, Dc, Dr,
+                     page_size, max_pages_per_seq, num_pages, max_seq_len, scale);
+  if (rc != FA_OK || B == 0 || max_seq_len == 0) return rc;
+  const int chunk = mla_chunk_tokens(B, H, max_seq_len);
+  const int want = (max_seq_len + chunk - 1) / chunk;
+  if (n_chunks != want)
+    return fail(FA_ERR_INVALID_ARG, "mla_decode_paged_states: n_chunks must be %d (got %d)", want,
+                n_chunks);
+  if (!o_parts || !lse_parts || !aligned16(o_parts))
+    return fail(FA_ERR_INVALID_ARG, "mla_decode_paged_states: o_parts/lse_parts missing or misaligned");
+  uint32_t* status = device_status_ptr();
+  if (!status) return fail(FA_ERR_CUDA, "mla_decode_paged_states: no usable CUDA device");
+  cudaError_t e = mla_states(q_nope, q_pe, ckv_pages, kpe_pages, page_table, seq_lens, o_parts,
+                             lse_parts, chunk, n_chunks, B, H, Dc, Dr, page_size,
+                             max_pages_per_seq, num_pages, scale, status,
+                             static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("mla_decode_paged_states", e);
   return FA_OK;
 }
 

@@ -310,7 +310,7 @@ cudaError_t launch_impl(const DecodeParams& p, cudaStream_t stream) {
   using L = DecLayout<D>;
   auto kern = decode_kernel<D, G>;
   const int smem = L::kRing;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem_limit(kern, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_chunks, p.Hkv, p.B);
   kern<<<grid, kThreads, smem, stream>>>(p);

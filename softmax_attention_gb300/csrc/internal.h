@@ -79,7 +79,7 @@ struct MlaParams {
   uint32_t* status;
 };
 cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream);
-int mla_chunk_tokens();
+int mla_chunk_tokens(int B, int H, int max_seq_len);
 
 // ---------------------------------------------------------------------------------------
 // Merge of split states
@@ -106,6 +106,15 @@ cudaError_t launch_f32_to_f16(const float* src, void* dst, size_t n, cudaStream_
 // Shared host helpers
 // ---------------------------------------------------------------------------------------
 uint32_t* device_status_ptr();  // the library's sticky device status word on this device
+int current_device_index();      // cudaGetDevice, or -1
+
+// Sets a kernel's dynamic shared-memory limit once per (kernel, device): the first launch
+// on each device does it; later launches, including ones captured into a CUDA graph, do not.
+cudaError_t ensure_smem_limit_fn(const void* kernel, int bytes);
+template <typename Kernel>
+cudaError_t ensure_smem_limit(Kernel k, int bytes) {
+  return ensure_smem_limit_fn(reinterpret_cast<const void*>(k), bytes);
+}
 int num_sms();                  // SM count of the current device (cached)
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType t, int rank, const void* base,
                   const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,

@@ -4,7 +4,7 @@
 
 namespace fa {
 
-int mla_chunk_tokens() { return 256; }
+int mla_chunk_tokens(int, int, int) { return 256; }
 
 cudaError_t launch_mla(const MlaParams&, cudaStream_t) { return cudaErrorNotSupported; }
 

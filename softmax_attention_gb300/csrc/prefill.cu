@@ -372,7 +372,7 @@ cudaError_t launch_impl(const PrefillParams& p, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   }
   auto kern = prefill_kernel<D, BN, STAGES, BF16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  cudaError_t e = ensure_smem_limit(kern, L::kAlloc);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_qtiles * p.n_splits, p.Hkv, p.B);
   kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, p);

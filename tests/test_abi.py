@@ -122,3 +122,10 @@ def test_merge_rejects_bad_arguments(lib):
     assert lib.fa_merge_states(4096, 4096, None, 4096, None, 4, 6, 2, 0, None) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_merge_states(4096, 4096, None, 4096, None, 4, 8, 2, 9, None) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_merge_states(None, None, None, 4096, None, 0, 8, 2, 0, None) == fa.FA_OK
+
+
+def test_size_queries_ignore_pointers(lib):
+    a = _args(dtype=fa.FA_FP32, q=None, k=None, v=None, out=None)
+    assert lib.fa_prefill_workspace_size(ctypes.byref(a)) > 0
+    a = _args(num_splits=3, Lkv=4096, q=None, out=None)
+    assert lib.fa_prefill_num_splits(ctypes.byref(a)) == 3

@@ -101,3 +101,17 @@ def test_out_of_range_page_is_reported_not_read():
     fa.fa_decode_paged(*_gpu(q, kp, vp, bad, lens), 200, c.sm_scale)
     assert fa.fa_get_device_status() == fa.FA_ERR_BOUNDS
     assert fa.fa_get_device_status() == fa.FA_OK  # the status is cleared by reading it
+
+
+def test_states_then_merge_equals_full_call():
+    c = workloads.PagedCase(B=5, Hq=16, Hkv=4, D=128, page_size=16, num_pages=900, min_len=0,
+                            max_len=2500, seed=11)
+    q, kp, vp, table, lens = workloads.paged_inputs(c)
+    args = _gpu(q, kp, vp, table, lens)
+    max_len = int(lens.max())
+    out, lse = fa.fa_decode_paged(*args, max_len, c.sm_scale)
+    op, ol, chunk = fa.fa_decode_paged_states(*args, max_len, c.sm_scale)
+    n = torch.repeat_interleave((lens.long() + chunk - 1) // chunk, c.Hq).to(torch.int32)
+    out2, lse2 = fa.fa_merge_states(op, ol, n.cuda(), out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert torch.equal(out.reshape(-1, c.D), out2) and torch.equal(lse.reshape(-1), lse2)
