@@ -434,6 +434,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--only", choices=("decode", "mla", "mqa"), default=None,
+                    help="run the headline plus only this path (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -458,9 +460,11 @@ def main():
         paths = {}
         if not args.quick:
             sub = max(20, args.steps // 4)
-            pc = workloads.paged_gqa_decode(seed=1 + dist.rank)
-            paths["paged_gqa_decode"] = bench_decode(fa, pc, sub, args.warmup, flush, dist, pk)
-            for batch, seq in ((128, 2048), (768, 1024)):
+            want = (lambda name: args.only in (None, name))
+            if want("decode"):
+                pc = workloads.paged_gqa_decode(seed=1 + dist.rank)
+                paths["paged_gqa_decode"] = bench_decode(fa, pc, sub, args.warmup, flush, dist, pk)
+            for batch, seq in (((128, 2048), (768, 1024)) if want("mla") else ()):
                 mc = workloads.mla_decode(batch, seq, seed=1 + dist.rank)
                 try:
                     paths[f"mla_decode_b{batch}_s{seq}"] = bench_mla(fa, mc, sub, args.warmup,
@@ -468,7 +472,7 @@ def main():
                 except fa.FAError as e:
                     paths[f"mla_decode_b{batch}_s{seq}"] = {"unavailable": str(e)}
             sweep = {}
-            for lq in workloads.MQA_SWEEP_LQ:
+            for lq in (workloads.MQA_SWEEP_LQ if want("mqa") else ()):
                 mc = workloads.mqa_prefill(lq, seed=1 + dist.rank)
                 r = bench_prefill(fa, mc, sub, args.warmup, flush, dist, pk)
                 bytes_ = (mc.Lq * mc.Hq * 2 + 2 * mc.Lkv * mc.Hkv) * mc.D * 2 + mc.Lq * mc.Hq * 4
@@ -481,7 +485,8 @@ def main():
                                                        pk["hbm"] if bound == "hbm" else pk["bf16"],
                                                        "GB/s" if bound == "hbm" else "TFLOP/s",
                                                        None, pk)}
-            paths["mqa_prefill_sweep"] = sweep
+            if sweep:
+                paths["mqa_prefill_sweep"] = sweep
         clk = clocks.stop() if dist.rank == 0 else None
         flops = head["flops"]
         total_tflops = dist.world * flops / (head["ms"] * 1e-3) / 1e12
