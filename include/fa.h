@@ -115,6 +115,28 @@ int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
 
 size_t fa_decode_workspace_size(int B, int Hq, int D, int max_seq_len);
 
+/*
+ * fa_decode_paged for callers that cannot allocate device memory (the pages describe no
+ * such entry point; it has no counterpart there).  Same arguments and results as
+ * fa_decode_paged minus the workspace: the split-KV scratch comes from a fixed 32 MiB
+ * device array inside the library, which every GPU that loads the library keeps reserved
+ * until the process exits.  Use it where allocating is not possible, e.g. a runtime whose
+ * arena allocator owns all device memory, or a serving loop that must not allocate.
+ *   - Problems whose fa_decode_workspace_size(B, Hq, D, max_seq_len) exceeds 32 MiB are
+ *     rejected with FA_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on each device looks up the array's device address (a
+ *     cudaGetSymbolAddress call); make that first call before any stream capture.
+ *   - Calls make no allocation of any kind.
+ *   - Every call uses the same array: two calls whose kernels overlap on the GPU (different
+ *     streams, or different threads without ordering) race on it and give wrong results.
+ *     Calls ordered on one stream are safe; the array needs no clearing between calls.
+ */
+int fa_decode_paged_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                            const int32_t* page_table, const int32_t* seq_lens, void* out,
+                            float* lse, int B, int Hq, int Hkv, int D, int page_size,
+                            int max_pages_per_seq, int num_pages, int max_seq_len, float scale,
+                            void* stream);
+
 /* Tokens per split-KV chunk that fa_decode_paged uses for these sizes on the current device
  * (a multiple of 64; depends only on B, Hq, max_seq_len and the SM count). */
 int fa_decode_chunk_tokens(int B, int Hq, int max_seq_len);

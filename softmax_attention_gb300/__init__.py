@@ -33,6 +33,7 @@ _DT = {torch.bfloat16: FA_BF16, torch.float16: FA_FP16, torch.float32: FA_FP32}
 EXPORTS = (
     "fa_prefill", "fa_prefill_ex", "fa_prefill_workspace_size", "fa_prefill_num_splits",
     "fa_decode_paged", "fa_decode_workspace_size", "fa_decode_chunk_tokens",
+    "fa_decode_paged_noalloc",
     "fa_decode_paged_states", "mla_decode_paged", "mla_decode_workspace_size",
     "mla_decode_chunk_tokens", "mla_decode_paged_states", "fa_merge_states",
     "fa_get_device_status", "fa_last_error", "fa_version",
@@ -85,6 +86,8 @@ def load_library(path: str | None = None):
         lib.fa_decode_paged.argtypes = [_vp] * 7 + [_i] * 8 + [_f, _vp, _sz, _vp]
         lib.fa_decode_workspace_size.restype = _sz
         lib.fa_decode_workspace_size.argtypes = [_i] * 4
+        lib.fa_decode_paged_noalloc.restype = _i
+        lib.fa_decode_paged_noalloc.argtypes = [_vp] * 7 + [_i] * 8 + [_f, _vp]
         lib.fa_decode_chunk_tokens.restype = _i
         lib.fa_decode_chunk_tokens.argtypes = [_i] * 3
         lib.fa_decode_paged_states.restype = _i
@@ -238,6 +241,28 @@ def fa_decode_paged(q, k_pages, v_pages, page_table, seq_lens, max_seq_len: int,
                                _ptr(seq_lens), _ptr(out), _ptr(lse), B, Hq, Hkv, D, page_size,
                                page_table.shape[1], num_pages, int(max_seq_len), float(scale),
                                _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+    return out, lse
+
+
+def fa_decode_paged_noalloc(q, k_pages, v_pages, page_table, seq_lens, max_seq_len: int,
+                            scale: float | None = None, out=None, lse=None, stream=None):
+    """fa_decode_paged without a workspace, for callers that cannot allocate: the library's
+    fixed device scratch is used instead (problems needing more than it holds are refused).
+    Calls that overlap on the GPU share that scratch and race."""
+    lib = load_library()
+    _need_cuda(q, k_pages, v_pages, page_table, seq_lens, out, lse)
+    B, Hq, D = q.shape
+    num_pages, Hkv, page_size, _ = k_pages.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    _check(lib.fa_decode_paged_noalloc(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                       _ptr(seq_lens), _ptr(out), _ptr(lse), B, Hq, Hkv, D,
+                                       page_size, page_table.shape[1], num_pages,
+                                       int(max_seq_len), float(scale), _stream(stream)))
     return out, lse
 
 

@@ -73,6 +73,8 @@ uint32_t* device_status_ptr() {
 
 int current_device_index() { return current_device(); }
 
+int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
 cudaError_t ensure_smem_limit_fn(const void* kernel, int bytes) {
   static std::mutex mu;
   static std::set<std::pair<const void*, int>> done;

@@ -106,6 +106,7 @@ cudaError_t launch_f32_to_f16(const float* src, void* dst, size_t n, cudaStream_
 // Shared host helpers
 // ---------------------------------------------------------------------------------------
 uint32_t* device_status_ptr();  // the library's sticky device status word on this device
+int set_error(int code, const char* msg);  // sets fa_last_error() text; returns code
 int current_device_index();      // cudaGetDevice, or -1
 
 // Sets a kernel's dynamic shared-memory limit once per (kernel, device): the first launch
