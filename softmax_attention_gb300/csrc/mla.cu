@@ -1,11 +1,429 @@
-// mla.cu -- MLA paged decode (latent form); see launch_mla.
+// mla.cu -- MLA paged decode in the latent (absorbed) form on sm_103a.
+//
+// One compressed matrix ckv serves as both K and V and a separate rope part kpe adds
+// q_pe . kpe_t to every score (flashinfer PR "perf: FlashAttention-3 style MLA
+// PageAttention", change list item 4):
+//   s_t = scale * (q_nope . ckv_t + q_pe . kpe_t),   out = softmax(s) . ckv
+// with 64 query heads sharing one latent head (Dc = 512, Dr = 64).
+//
+// One CTA handles one chunk of one sequence's tokens.  Token rows are gathered through the
+// page table with TMA tile::gather4 (four rows per instruction, any page size) into a ring
+// of 32-token stages; each stage holds the 576-wide [ckv | kpe] rows of its tokens as nine
+// 128-byte-swizzled 64-column blocks.  Like the flashinfer design the ring is shared by the
+// K and V roles (one pipeline, small tiles, several stages in flight), but the MMAs are
+// Blackwell's:
+//   S  = Q [64 heads x 576] . KV^T         tcgen05 M=64 (heads), N=32 tokens, S in TMEM
+//   O^T += ckv^T [512 x tokens] . P^T       tcgen05 M=128 (latent dims, four blocks),
+//                                           N=64 heads, A = the same ckv stage read
+//                                           MN-major, B = P^T staged in shared memory
+// so O (64 x 512 fp32) lives in 256 tensor-memory columns as four 128-lane blocks and the
+// PV product runs at full tensor rate.  Softmax: one thread per head row (the M=64 S layout
+// puts heads 16q..16q+15 in lanes 32q..32q+15), online max/sum with O rescaled only when a
+// head's running max grows by more than 2^8.  The CTA writes the chunk's normalised partial
+// output and log-sum-exp; merge.cu combines chunks.
+//
+// Warp roles (192 threads): warps 0-3 softmax + epilogue, warp 4 producer (row indices on
+// all lanes, TMA issue), warp 5 MMA issuer and tensor-memory owner.
+#include <math.h>
+
 #include "internal.h"
 #include "sm103.cuh"
 
 namespace fa {
+namespace {
 
-int mla_chunk_tokens(int, int, int) { return 256; }
+constexpr int kH = 64;
+constexpr int kDc = 512;
+constexpr int kDr = 64;
+constexpr int kBlocks = (kDc + kDr) / 64;  // nine 64-column blocks per token row
+constexpr int kHalf = 32;                  // tokens per ring stage
+constexpr int kTile = 64;                  // tokens per softmax tile (two stages)
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kChunk = 512;                // tokens per CTA (multiple of kTile)
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLn2 = 0.69314718055994530942f;
 
-cudaError_t launch_mla(const MlaParams&, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int kQBytes = kH * (kDc + kDr) * 2;    // 73728
+constexpr int kBlk = kHalf * 128;                // one 64-column block of one stage
+constexpr int kStageBytes = kBlocks * kBlk;      // 36864
+constexpr int kPBytes = kH * kTile * 2;          // 8192
+constexpr int kQOff = 0;
+constexpr int kKVOff = kQOff + kQBytes;
+constexpr int kPOff = kKVOff + kStages * kStageBytes;
+constexpr int kBarOff = kPOff + kPBytes;
+// q_full, kv_full[S], kv_empty[S], s_full[2], p_full, o_full, mma_done
+constexpr int kNumBars = 1 + 2 * kStages + 2 + 3;
+constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 64 * 4 * 2 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr uint32_t kTmemO = 0;      // O^T: 4 blocks x 64 columns
+constexpr uint32_t kTmemS = 256;    // S buffers: 2 x 64 columns
+
+__device__ __forceinline__ bool softmax_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t col, int32_t r0, int32_t r1, int32_t r2,
+                                            int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(bar)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_kernel(const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qp,
+               const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
+               const MlaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t s_base = smem_addr(smem);
+  const uint32_t sQ = s_base + kQOff, sKV = s_base + kKVOff, sP = s_base + kPOff;
+  const uint32_t bars = s_base + kBarOff;
+  const uint32_t bar_q = bars;
+  auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
+  auto bar_empty = [&](int s) { return bars + 8u * (1 + kStages + s); };
+  auto bar_s = [&](int b) { return bars + 8u * (1 + 2 * kStages + b); };
+  const uint32_t bar_p = bars + 8u * (3 + 2 * kStages);
+  const uint32_t bar_o = bars + 8u * (4 + 2 * kStages);
+  const uint32_t bar_done = bars + 8u * (5 + 2 * kStages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + kNumBars * 8);
+  float* alpha_s = reinterpret_cast<float*>(smem + kBarOff + kNumBars * 8 + 16);
+  float* stat_s = alpha_s + 64;  // [0..63]: l per head (epilogue)
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int c = blockIdx.x, b = blockIdx.y;
+  const int len = p.seq_lens[b];
+  if (len < 0 || len > p.max_pages * p.page_size) {
+    if (threadIdx.x == 0) record_error(p.status, kDevBounds);
+    return;
+  }
+  const int t_start = c * p.chunk;
+  if (t_start >= len) return;
+  const int t_stop = min(len, t_start + p.chunk);
+  const int n_tiles = (t_stop - t_start + kTile - 1) / kTile;
+  const int n_stages = 2 * n_tiles;  // every tile is two 32-token stages
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    mbar_init(bar_s(0), 1);
+    mbar_init(bar_s(1), 1);
+    mbar_init(bar_p, 128);
+    mbar_init(bar_o, 1);
+    mbar_init(bar_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ----------------------------------- producer ----------------------------------------
+    const int32_t* table = p.page_table + static_cast<size_t>(b) * p.max_pages;
+    const int n_rows = p.num_pages * p.page_size;
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_qn);
+      tma_prefetch_desc(&tm_ckv);
+      tma_prefetch_desc(&tm_kpe);
+      mbar_arrive_expect_tx(bar_q, kQBytes);
+      for (int kb = 0; kb < kDc / 64; ++kb)
+        tma_load_2d(sQ + kb * (kH * 128), &tm_qn, bar_q, kb * 64, b * kH);
+      tma_load_2d(sQ + (kDc / 64) * (kH * 128), &tm_qp, bar_q, 0, b * kH);
+    }
+    // first valid row of the chunk: stands in for tokens past the end (masked later)
+    int fill_row = 0;
+    {
+      const int page = table[t_start / p.page_size];
+      if (page >= 0 && page < p.num_pages) fill_row = page * p.page_size + t_start % p.page_size;
+    }
+    int issued = 0;
+    bool ok = true;
+    for (int n = 0; n < n_stages; ++n) {
+      const int stage = n % kStages;
+      if (n >= kStages) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_empty(stage), ((n / kStages) - 1) & 1, p.status));
+        if (!ok) break;
+      }
+      // lane i computes the row of token i of this stage
+      const int tok = t_start + n * kHalf + lane;
+      int row = fill_row;
+      if (tok < t_stop) {
+        const int page = table[tok / p.page_size];
+        if (page >= 0 && page < p.num_pages) {
+          row = page * p.page_size + tok % p.page_size;
+        } else {
+          record_error(p.status, kDevBounds);
+        }
+      }
+      if (row < 0 || row >= n_rows) row = 0;
+      const uint32_t dst = sKV + stage * kStageBytes;
+      if (lane == 0) mbar_arrive_expect_tx(bar_full(stage), kStageBytes);
+      __syncwarp();
+      const int r0 = __shfl_sync(0xffffffffu, row, (lane & 7) * 4 + 0);
+      const int r1 = __shfl_sync(0xffffffffu, row, (lane & 7) * 4 + 1);
+      const int r2 = __shfl_sync(0xffffffffu, row, (lane & 7) * 4 + 2);
+      const int r3 = __shfl_sync(0xffffffffu, row, (lane & 7) * 4 + 3);
+      if (lane < 8) {
+        const uint32_t gdst = dst + lane * (4 * 128);
+        for (int kb = 0; kb < kDc / 64; ++kb)
+          tma_gather4(gdst + kb * kBlk, &tm_ckv, bar_full(stage), kb * 64, r0, r1, r2, r3);
+        tma_gather4(gdst + (kDc / 64) * kBlk, &tm_kpe, bar_full(stage), 0, r0, r1, r2, r3);
+      }
+      issued = n + 1;
+    }
+    if (!ok && lane == 0) {
+      mbar_wait(bar_q, 0, nullptr);
+      for (int n = max(0, issued - kStages); n < issued; ++n)
+        mbar_wait(bar_full(n % kStages), (n / kStages) & 1, nullptr);
+    }
+  } else if (warp == 5) {
+    // ----------------------------------- MMA issuer --------------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_f16(true, 64, kHalf, false, false);
+      constexpr uint32_t idesc_o = idesc_f16(true, 128, kH, true, false);
+      // S of tile j: two N=32 halves, one per stage, into S buffer j & 1
+      auto issue_s = [&](int j) -> bool {
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          const int n = 2 * j + h, stage = n % kStages;
+          if (!mbar_wait(bar_full(stage), (n / kStages) & 1, p.status)) return false;
+          tc_fence_after();
+          const uint32_t kv = sKV + stage * kStageBytes;
+          const uint32_t d = tmem + kTmemS + (j & 1) * kTile + h * kHalf;
+#pragma unroll
+          for (int kk = 0; kk < kBlocks * 4; ++kk) {
+            const uint32_t off = (kk % 4) * 32;
+            const uint64_t ad = sdesc_sw128(sQ + (kk / 4) * (kH * 128) + off, 16, 1024);
+            const uint64_t bd = sdesc_sw128(kv + (kk / 4) * kBlk + off, 16, 1024);
+            mma_ss(d, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+          }
+        }
+        tc_commit(bar_s(j & 1));
+        return true;
+      };
+      bool ok = mbar_wait(bar_q, 0, p.status);
+      if (ok) {
+        tc_fence_after();
+        ok = issue_s(0);
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j + 1 < n_tiles && !(ok = issue_s(j + 1))) break;
+        if (!(ok = mbar_wait(bar_p, j & 1, p.status))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          const int n = 2 * j + h, stage = n % kStages;
+          const uint32_t kv = sKV + stage * kStageBytes;
+#pragma unroll
+          for (int db = 0; db < kDc / 128; ++db) {
+#pragma unroll
+            for (int ks = 0; ks < kHalf / 16; ++ks) {
+              const uint64_t ad = sdesc_sw128(kv + (2 * db) * kBlk + ks * (16 * 128), kBlk, 1024);
+              const uint64_t bd = sdesc_sw128(sP + (h * 2 + ks) * 32, 16, 1024);
+              mma_ss(tmem + kTmemO + db * kH, ad, bd, idesc_o, (j > 0 || h > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
+        }
+        tc_commit(bar_o);
+        tc_commit(bar_empty((2 * j) % kStages));
+        tc_commit(bar_empty((2 * j + 1) % kStages));
+      }
+      tc_commit(bar_done);
+      mbar_wait(bar_done, 0, nullptr);
+    }
+  } else {
+    // ---------------------- softmax (thread per head) + epilogue ---------------------------
+    const bool owner = lane < 16;          // lanes 32w..32w+15 hold heads 16w..16w+15
+    const int h = warp * 16 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    // No early exit from this loop: the four softmax warps meet at named barriers, so after
+    // a failed wait a warp keeps going without waiting (its results are discarded).
+    for (int j = 0; j < n_tiles; ++j) {
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_s(j & 1), (j >> 1) & 1, p.status));
+      tc_fence_after();
+      uint32_t raw[kTile];
+      tmem_ld32(tmem + kTmemS + lane_off + (j & 1) * kTile, *reinterpret_cast<uint32_t(*)[32]>(&raw[0]));
+      tmem_ld32(tmem + kTmemS + lane_off + (j & 1) * kTile + 32, *reinterpret_cast<uint32_t(*)[32]>(&raw[32]));
+      tmem_ld_wait();
+      const int tok0 = t_start + j * kTile;
+      const int n_valid = min(kTile, t_stop - tok0);
+      float s[kTile];
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int e = 0; e < kTile; ++e) {
+        s[e] = (e < n_valid) ? __uint_as_float(raw[e]) * p.scale_log2 : -INFINITY;
+        mx[e & 3] = fmaxf(mx[e & 3], s[e]);
+      }
+      float m_new = fmaxf(m_run, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
+      if (!owner) m_new = m_run;
+      if (j > 0 && ok) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (j - 1) & 1, p.status));
+        tc_fence_after();
+      }
+      const bool need = owner && (m_new > m_run + kRescaleLog2);
+      if (softmax_any(need)) {
+        float alpha = 1.f;
+        if (need) {
+          alpha = exp2_approx(m_run - m_new);
+          m_run = m_new;
+          l_run *= alpha;
+        }
+        if (owner) alpha_s[h] = alpha;
+        softmax_sync();
+        if (j > 0) {
+          // O^T column h belongs to head h; every lane holds one latent dim of every head
+#pragma unroll 1
+          for (int db = 0; db < kDc / 128; ++db) {
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+              uint32_t o[32];
+              const uint32_t ta = tmem + kTmemO + lane_off + db * kH + half * 32;
+              tmem_ld32(ta, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha_s[half * 32 + e]);
+              tmem_st32(ta, o);
+            }
+          }
+          tmem_st_wait();
+        }
+        softmax_sync();  // alpha_s may be rewritten on the next tile
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[kTile / 2];
+#pragma unroll
+      for (int e = 0; e < kTile / 2; ++e) {
+        const float p0 = exp2_approx(s[2 * e] - m_use);
+        const float p1 = exp2_approx(s[2 * e + 1] - m_use);
+        sum[e & 3] += p0 + p1;
+        pk[e] = pack_bf16x2(p0, p1);
+      }
+      if (owner) {
+        l_run += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+        // P^T row h: 64 tokens x bf16 = 128 bytes, 16-byte chunks swizzled by h % 8
+        uint8_t* prow = smem + kPOff + h * 128;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8)
+          *reinterpret_cast<uint4*>(prow + ((c8 ^ (h & 7)) * 16)) =
+              make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_p);
+    }
+    if (ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (n_tiles - 1) & 1, p.status));
+      tc_fence_after();
+    }
+    // every softmax thread must reach this barrier, even after a failed wait
+    if (owner) stat_s[h] = l_run;
+    softmax_sync();
+    if (ok) {
+      const size_t row0 = static_cast<size_t>(b) * kH;
+#pragma unroll 1
+      for (int db = 0; db < kDc / 128; ++db) {
+        const int d = db * 128 + warp * 32 + lane;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t o[32];
+          tmem_ld32(tmem + kTmemO + lane_off + db * kH + half * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int hh = half * 32 + e;
+            const float l = stat_s[hh];
+            const float v = l > 0.f ? __uint_as_float(o[e]) / l : 0.f;
+            p.o_part[((row0 + hh) * p.n_chunks + c) * kDc + d] = v;
+          }
+        }
+      }
+      if (owner)
+        p.lse_part[(row0 + h) * p.n_chunks + c] =
+            l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+int mla_chunk_tokens(int, int, int) { return kChunk; }
+
+cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream) {
+  if (p.H != kH || p.Dc != kDc || p.Dr != kDr || p.chunk != kChunk) return cudaErrorInvalidValue;
+  CUtensorMap tqn, tqp, tckv, tkpe;
+  const uint64_t rows = static_cast<uint64_t>(p.num_pages) * p.page_size;
+  const uint64_t qrows = static_cast<uint64_t>(p.B) * kH;
+  {
+    const uint64_t dims[2] = {kDc, qrows};
+    const uint64_t str[1] = {kDc * 2};
+    const uint32_t box[2] = {64, kH};
+    if (!encode_tiled(&tqn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.q_nope, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {kDr, qrows};
+    const uint64_t str[1] = {kDr * 2};
+    const uint32_t box[2] = {64, kH};
+    if (!encode_tiled(&tqp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.q_pe, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {kDc, rows > 0 ? rows : 1};
+    const uint64_t str[1] = {kDc * 2};
+    const uint32_t box[2] = {64, 1};  // gather4 reads four one-row boxes
+    if (!encode_tiled(&tckv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.ckv, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {kDr, rows > 0 ? rows : 1};
+    const uint64_t str[1] = {kDr * 2};
+    const uint32_t box[2] = {64, 1};
+    if (!encode_tiled(&tkpe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.kpe, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = ensure_smem_limit(mla_kernel, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.n_chunks, p.B);
+  mla_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tqn, tqp, tckv, tkpe, p);
+  return cudaGetLastError();
+}
 
 }  // namespace fa

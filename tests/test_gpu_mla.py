@@ -1,0 +1,95 @@
+"""GPU parity of MLA paged decode (latent form: ckv is K and V, kpe adds the rope term)
+against the fp64 oracle, through the C ABI; bit-exact paging; the bounds-error path."""
+import math
+
+import pytest
+import torch
+
+import oracle
+import softmax_attention_gb300 as fa
+import workloads
+from tests._parity import check
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fa.load_library()
+    yield
+    assert fa.fa_get_device_status() == fa.FA_OK, fa.fa_last_error()
+
+
+def _run(c: workloads.MlaCase, rows=None):
+    qn, qp, ckv, kpe, table, lens = workloads.mla_inputs(c)
+    dev = [t.cuda() for t in (qn, qp, ckv, kpe, table, lens)]
+    out, lse = fa.mla_decode_paged(*dev, c.max_len, c.scale)
+    torch.cuda.synchronize()
+    ro, rl = oracle.mla_decode_paged(qn, qp, ckv, kpe, table, lens, scale=c.scale, rows=rows)
+    if rows is not None:
+        idx = torch.as_tensor(rows, device="cuda")
+        out, lse = out.reshape(-1, c.Dc)[idx], lse.reshape(-1)[idx]
+    return out, lse, ro, rl
+
+
+@pytest.mark.parametrize("lens,ps", [
+    ([1, 31, 32, 33], 1),
+    ([63, 64, 65, 700], 1),
+    ([511, 512, 513, 1500], 1),
+    ([0, 5, 1024], 1),
+    ([17, 300, 1030], 16),
+    ([200, 64], 64),
+])
+def test_parity_shapes(lens, ps):
+    c = workloads.MlaCase(B=len(lens), H=64, seq_len=None, seq_lens=lens, page_size=ps,
+                          seed=len(lens) + ps)
+    out, lse, ro, rl = _run(c)
+    check(out, lse, ro, rl, what=f"mla {lens} ps={ps}")
+
+
+@pytest.mark.parametrize("batch,seq", [(128, 2048), (768, 1024)])
+def test_mla_full_size_sampled(batch, seq):
+    c = workloads.mla_decode(batch, seq)
+    rows = list(range(0, c.B * c.H, 97 if batch == 768 else 41))
+    out, lse, ro, rl = _run(c, rows=rows)
+    check(out, lse, ro, rl, what=f"mla b{batch} s{seq} (sampled)")
+
+
+def test_paged_equals_dense_gathered_bit_exact():
+    c = workloads.MlaCase(B=4, H=64, seq_len=None, seq_lens=[900, 1, 1025, 333], seed=7)
+    qn, qp, ckv, kpe, table, lens = workloads.mla_inputs(c)
+    order, id_table, pos = [], torch.full_like(table, -1), 0
+    for b in range(c.B):
+        n = int(lens[b])
+        order.append(table[b, :n].long())
+        id_table[b, :n] = torch.arange(pos, pos + n, dtype=torch.int32)
+        pos += n
+    order = torch.cat(order)
+    o1, l1 = fa.mla_decode_paged(*[t.cuda() for t in (qn, qp, ckv, kpe, table, lens)],
+                                 c.max_len, c.scale)
+    o2, l2 = fa.mla_decode_paged(*[t.cuda() for t in (qn, qp, ckv[order].contiguous(),
+                                                      kpe[order].contiguous(), id_table, lens)],
+                                 c.max_len, c.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_states_then_merge_equals_full_call():
+    c = workloads.MlaCase(B=3, H=64, seq_len=None, seq_lens=[1300, 40, 0], seed=9)
+    dev = [t.cuda() for t in workloads.mla_inputs(c)]
+    out, lse = fa.mla_decode_paged(*dev, c.max_len, c.scale)
+    op, ol, chunk = fa.mla_decode_paged_states(*dev, c.max_len, c.scale)
+    lens = dev[5].long().cpu()
+    n = torch.repeat_interleave((lens + chunk - 1) // chunk, c.H).to(torch.int32)
+    out2, lse2 = fa.fa_merge_states(op, ol, n.cuda(), out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert torch.equal(out.reshape(-1, c.Dc), out2) and torch.equal(lse.reshape(-1), lse2)
+
+
+def test_out_of_range_page_is_reported():
+    c = workloads.MlaCase(B=2, H=64, seq_len=None, seq_lens=[100, 50], seed=3)
+    qn, qp, ckv, kpe, table, lens = workloads.mla_inputs(c)
+    table[0, 10] = 10 ** 7
+    fa.mla_decode_paged(*[t.cuda() for t in (qn, qp, ckv, kpe, table, lens)], c.max_len, c.scale)
+    assert fa.fa_get_device_status() == fa.FA_ERR_BOUNDS
+    assert fa.fa_get_device_status() == fa.FA_OK
