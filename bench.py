@@ -458,8 +458,8 @@ def main():
         c = workloads.gqa_prefill_chunk(seed=1 + dist.rank)
         head = bench_prefill(fa, c, args.steps, args.warmup, flush, dist, pk, e2e=True)
         paths = {}
-        if not args.quick:
-            sub = max(20, args.steps // 4)
+        if not args.quick or args.only:
+            sub = max(20, args.steps // 4) if not args.quick else 3
             want = (lambda name: args.only in (None, name))
             if want("decode"):
                 pc = workloads.paged_gqa_decode(seed=1 + dist.rank)

@@ -7,9 +7,11 @@
 // with 64 query heads sharing one latent head (Dc = 512, Dr = 64).
 //
 // One CTA handles one chunk of one sequence's tokens.  Token rows are gathered through the
-// page table with TMA tile::gather4 (four rows per instruction, any page size) into a ring
-// of 32-token stages; each stage holds the 576-wide [ckv | kpe] rows of its tokens as nine
-// 128-byte-swizzled 64-column blocks.  Like the flashinfer design the ring is shared by the
+// page table with 16-byte cp.async copies by a producer warpgroup (LDGSTS-style gathers, the
+// page_size=1 choice of the flashinfer PR's results section; measured on GB300 they move
+// these 1152-byte rows faster than TMA tile::gather4) into a ring of 32-token stages; each
+// stage holds the 576-wide [ckv | kpe] rows of its tokens as nine 128-byte-swizzled
+// 64-column blocks, written at their swizzled addresses by the copying threads.  Like the flashinfer design the ring is shared by the
 // K and V roles (one pipeline, small tiles, several stages in flight), but the MMAs are
 // Blackwell's:
 //   S  = Q [64 heads x 576] . KV^T         tcgen05 M=64 (heads), N=32 tokens, S in TMEM
@@ -22,8 +24,8 @@
 // head's running max grows by more than 2^8.  The CTA writes the chunk's normalised partial
 // output and log-sum-exp; merge.cu combines chunks.
 //
-// Warp roles (192 threads): warps 0-3 softmax + epilogue, warp 4 producer (row indices on
-// all lanes, TMA issue), warp 5 MMA issuer and tensor-memory owner.
+// Warp roles (288 threads): warps 0-3 softmax + epilogue, warps 4-7 producer (row ids and
+// cp.async gathers), warp 8 MMA issuer and tensor-memory owner.
 #include <math.h>
 
 #include "internal.h"
@@ -39,7 +41,10 @@ constexpr int kBlocks = (kDc + kDr) / 64;  // nine 64-column blocks per token ro
 constexpr int kHalf = 32;                  // tokens per ring stage
 constexpr int kTile = 64;                  // tokens per softmax tile (two stages)
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 288;
+constexpr int kProducerThreads = 128;
+constexpr int kMmaWarp = 8;
+
 constexpr int kChunk = 512;                // tokens per CTA (multiple of kTile)
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -47,6 +52,9 @@ constexpr float kLn2 = 0.69314718055994530942f;
 constexpr int kQBytes = kH * (kDc + kDr) * 2;    // 73728
 constexpr int kBlk = kHalf * 128;                // one 64-column block of one stage
 constexpr int kStageBytes = kBlocks * kBlk;      // 36864
+// The ring is laid out block-major, [9 blocks][4 stages][32 rows][128 B], so the two stages
+// of a tile (2t, 2t+1) are 64 contiguous rows in every block: one N=64 MMA covers a tile.
+constexpr int kBlockStride = kStages * kBlk;     // 16384
 constexpr int kPBytes = kH * kTile * 2;          // 8192
 constexpr int kQOff = 0;
 constexpr int kKVOff = kQOff + kQBytes;
@@ -73,20 +81,8 @@ __device__ __forceinline__ bool softmax_any(bool v) {
 }
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int32_t col, int32_t r0, int32_t r1, int32_t r2,
-                                            int32_t r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(bar)
-      : "memory");
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     mla_kernel(const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qp,
-               const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
                const MlaParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -121,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar_full(s), 1);
+      mbar_init(bar_full(s), kProducerThreads);
       mbar_init(bar_empty(s), 1);
     }
     mbar_init(bar_s(0), 1);
@@ -131,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_done, 1);
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -140,116 +136,170 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp >= 4 && warp < kMmaWarp) {
     // ----------------------------------- producer ----------------------------------------
+    // Producer warp pw copies tokens 8pw..8pw+7 of every 32-token stage: per token two
+    // 512-byte halves of the ckv row (lane l copies 16-byte chunk l of the half, so a warp
+    // instruction reads 512 contiguous bytes) and its 128-byte kpe row.
+    const int pw = warp - 4;
     const int32_t* table = p.page_table + static_cast<size_t>(b) * p.max_pages;
     const int n_rows = p.num_pages * p.page_size;
-    if (lane == 0) {
+    if (threadIdx.x == 4 * 32) {
       tma_prefetch_desc(&tm_qn);
-      tma_prefetch_desc(&tm_ckv);
-      tma_prefetch_desc(&tm_kpe);
+      tma_prefetch_desc(&tm_qp);
       mbar_arrive_expect_tx(bar_q, kQBytes);
       for (int kb = 0; kb < kDc / 64; ++kb)
         tma_load_2d(sQ + kb * (kH * 128), &tm_qn, bar_q, kb * 64, b * kH);
       tma_load_2d(sQ + (kDc / 64) * (kH * 128), &tm_qp, bar_q, 0, b * kH);
     }
-    // first valid row of the chunk: stands in for tokens past the end (masked later)
-    int fill_row = 0;
-    {
-      const int page = table[t_start / p.page_size];
-      if (page >= 0 && page < p.num_pages) fill_row = page * p.page_size + t_start % p.page_size;
+    // Row ids, read once with independent loads: lane l holds the row of token
+    // 32n + 8pw + (l & 7) for the stages n = (l >> 3) + 4m, m < 4.
+    int pages[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int tok = t_start + 32 * ((lane >> 3) + 4 * m) + 8 * pw + (lane & 7);
+      pages[m] = tok < t_stop ? __ldg(table + tok / p.page_size) : -1;
     }
-    int issued = 0;
-    bool ok = true;
-    for (int n = 0; n < n_stages; ++n) {
-      const int stage = n % kStages;
-      if (n >= kStages) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_empty(stage), ((n / kStages) - 1) & 1, p.status));
-        if (!ok) break;
-      }
-      // lane i computes the row of token i of this stage
-      const int tok = t_start + n * kHalf + lane;
-      int row = fill_row;
+    const int first_page = __ldg(table + t_start / p.page_size);
+    int fill_row = (first_page >= 0 && first_page < p.num_pages)
+                       ? first_page * p.page_size + t_start % p.page_size : 0;
+    if (fill_row >= n_rows) fill_row = 0;
+    int rows[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int tok = t_start + 32 * ((lane >> 3) + 4 * m) + 8 * pw + (lane & 7);
+      int row = fill_row;  // tokens past the end read a valid row; their scores are masked
       if (tok < t_stop) {
-        const int page = table[tok / p.page_size];
-        if (page >= 0 && page < p.num_pages) {
-          row = page * p.page_size + tok % p.page_size;
+        if (pages[m] >= 0 && pages[m] < p.num_pages) {
+          row = pages[m] * p.page_size + tok % p.page_size;
         } else {
           record_error(p.status, kDevBounds);
         }
       }
-      if (row < 0 || row >= n_rows) row = 0;
-      const uint32_t dst = sKV + stage * kStageBytes;
-      if (lane == 0) mbar_arrive_expect_tx(bar_full(stage), kStageBytes);
-      __syncwarp();
-      const int r0 = __shfl_sync(0xffffffffu, row, (lane & 7) * 4 + 0);
-      const int r1 = __shfl_sync(0xffffffffu, row, (lane & 7) * 4 + 1);
-      const int r2 = __shfl_sync(0xffffffffu, row, (lane & 7) * 4 + 2);
-      const int r3 = __shfl_sync(0xffffffffu, row, (lane & 7) * 4 + 3);
-      if (lane < 8) {
-        const uint32_t gdst = dst + lane * (4 * 128);
-        for (int kb = 0; kb < kDc / 64; ++kb)
-          tma_gather4(gdst + kb * kBlk, &tm_ckv, bar_full(stage), kb * 64, r0, r1, r2, r3);
-        tma_gather4(gdst + (kDc / 64) * kBlk, &tm_kpe, bar_full(stage), 0, r0, r1, r2, r3);
+      rows[m] = (row >= 0 && row < n_rows) ? row : fill_row;
+    }
+    const uint8_t* ckv = static_cast<const uint8_t*>(p.ckv);
+    const uint8_t* kpe = static_cast<const uint8_t*>(p.kpe);
+    // Issue a stage whenever its ring slot is free; otherwise publish the oldest issued
+    // stage once this thread's copies for it have landed (wait, then fence so the tensor
+    // core's async-proxy reads see them, then arrive).  Publishing never waits on a slot.
+    int issued = 0, published = 0;
+    uint64_t t_last = global_timer_ns();
+    while (published < n_stages) {
+      bool can_issue = issued < n_stages;
+      if (can_issue && issued >= kStages) {
+        const bool free_slot = mbar_test_wait(bar_empty(issued % kStages),
+                                              ((issued / kStages) - 1) & 1);
+        can_issue = __shfl_sync(0xffffffffu, free_slot ? 1 : 0, 0) != 0;
+        if (can_issue) mbar_wait(bar_empty(issued % kStages), ((issued / kStages) - 1) & 1, nullptr);
       }
-      issued = n + 1;
-    }
-    if (!ok && lane == 0) {
-      mbar_wait(bar_q, 0, nullptr);
-      for (int n = max(0, issued - kStages); n < issued; ++n)
-        mbar_wait(bar_full(n % kStages), (n / kStages) & 1, nullptr);
-    }
-  } else if (warp == 5) {
-    // ----------------------------------- MMA issuer --------------------------------------
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16(true, 64, kHalf, false, false);
-      constexpr uint32_t idesc_o = idesc_f16(true, 128, kH, true, false);
-      // S of tile j: two N=32 halves, one per stage, into S buffer j & 1
-      auto issue_s = [&](int j) -> bool {
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          const int n = 2 * j + h, stage = n % kStages;
-          if (!mbar_wait(bar_full(stage), (n / kStages) & 1, p.status)) return false;
-          tc_fence_after();
-          const uint32_t kv = sKV + stage * kStageBytes;
-          const uint32_t d = tmem + kTmemS + (j & 1) * kTile + h * kHalf;
+      if (can_issue) {
+        const int n = issued;
+        const uint32_t dst = sKV + (n % kStages) * kBlk;
+        // rows[n >> 2] needs a compile-time index: select it
+        const int rsel = (n >> 2) == 0 ? rows[0] : (n >> 2) == 1 ? rows[1] : (n >> 2) == 2 ? rows[2] : rows[3];
 #pragma unroll
-          for (int kk = 0; kk < kBlocks * 4; ++kk) {
-            const uint32_t off = (kk % 4) * 32;
-            const uint64_t ad = sdesc_sw128(sQ + (kk / 4) * (kH * 128) + off, 16, 1024);
-            const uint64_t bd = sdesc_sw128(kv + (kk / 4) * kBlk + off, 16, 1024);
-            mma_ss(d, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+        for (int t8 = 0; t8 < 8; ++t8) {
+          const int tok = 8 * pw + t8;
+          const int row = __shfl_sync(0xffffffffu, rsel, ((n & 3) << 3) + t8);
+          const uint8_t* src = ckv + static_cast<size_t>(row) * (kDc * 2);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int q = hf * 32 + lane;  // 16-byte chunk of the ckv row
+            cp_async_16(dst + (q >> 3) * kBlockStride + tok * 128 + (((q & 7) ^ (tok & 7)) * 16),
+                        src + q * 16);
           }
         }
-        tc_commit(bar_s(j & 1));
-        return true;
-      };
-      bool ok = mbar_wait(bar_q, 0, p.status);
-      if (ok) {
-        tc_fence_after();
-        ok = issue_s(0);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int idx = k * 32 + lane, t8 = idx >> 3, cc = idx & 7, tok = 8 * pw + t8;
+          const int row = __shfl_sync(0xffffffffu, rsel, ((n & 3) << 3) + t8);
+          cp_async_16(dst + (kDc / 64) * kBlockStride + tok * 128 + ((cc ^ (tok & 7)) * 16),
+                      kpe + static_cast<size_t>(row) * (kDr * 2) + cc * 16);
+        }
+        cp_async_commit();
+        ++issued;
+        t_last = global_timer_ns();
+      } else if (published < issued) {
+        cp_async_wait_dyn(issued - published - 1);
+        fence_proxy_async_smem();
+        mbar_arrive(bar_full(published % kStages));
+        ++published;
+        t_last = global_timer_ns();
+      } else if (global_timer_ns() - t_last > kWaitLimitNs) {
+        record_error(p.status, kDevTimeout);
+        break;
       }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        if (j + 1 < n_tiles && !(ok = issue_s(j + 1))) break;
-        if (!(ok = mbar_wait(bar_p, j & 1, p.status))) break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          const int n = 2 * j + h, stage = n % kStages;
-          const uint32_t kv = sKV + stage * kStageBytes;
+    }
+    cp_async_wait<0>();
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------- MMA issuer --------------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_f16(true, 64, kTile, false, false);
+      constexpr uint32_t idesc_o = idesc_f16(true, 128, kH, true, false);
+      // S of tile j: two N=32 halves, one per stage, into S buffer j & 1
+      // (the two halves' accumulation chains are interleaved so the tensor core always
+      // has an independent MMA to start)
+      const uint64_t q_desc = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t kv_desc = sdesc_sw128(sKV, 16, 1024);
+      const uint64_t kv_desc_mn = sdesc_sw128(sKV, kBlockStride, 1024);
+      const uint64_t p_desc = sdesc_sw128(sP, 16, 1024);
+      auto issue_s = [&](int j) {
+        const uint64_t b0 = sdesc_add(kv_desc, ((2 * j) % kStages) * kBlk);
+        const uint32_t d0 = tmem + kTmemS + (j & 1) * kTile;
 #pragma unroll
-          for (int db = 0; db < kDc / 128; ++db) {
+        for (int kk = 0; kk < kBlocks * 4; ++kk) {
+          const uint32_t off = (kk % 4) * 32;
+          mma_ss(d0, sdesc_add(q_desc, (kk / 4) * (kH * 128) + off),
+                 sdesc_add(b0, (kk / 4) * kBlockStride + off), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bar_s(j & 1));
+      };
+      // O^T += ckv^T P^T for tile j, then release its two stages
+      auto issue_pv = [&](int j) {
+        const uint64_t kv = sdesc_add(kv_desc_mn, ((2 * j) % kStages) * kBlk);
 #pragma unroll
-            for (int ks = 0; ks < kHalf / 16; ++ks) {
-              const uint64_t ad = sdesc_sw128(kv + (2 * db) * kBlk + ks * (16 * 128), kBlk, 1024);
-              const uint64_t bd = sdesc_sw128(sP + (h * 2 + ks) * 32, 16, 1024);
-              mma_ss(tmem + kTmemO + db * kH, ad, bd, idesc_o, (j > 0 || h > 0 || ks > 0) ? 1u : 0u);
-            }
+        for (int ks = 0; ks < kTile / 16; ++ks) {
+          const uint64_t bd = sdesc_add(p_desc, ks * 32);
+#pragma unroll
+          for (int db = 0; db < kDc / 128; ++db) {  // four independent accumulators
+            const uint64_t ad = sdesc_add(kv, (2 * db) * kBlockStride + ks * (16 * 128));
+            mma_ss(tmem + kTmemO + db * kH, ad, bd, idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
           }
         }
         tc_commit(bar_o);
         tc_commit(bar_empty((2 * j) % kStages));
         tc_commit(bar_empty((2 * j + 1) % kStages));
+      };
+      auto stage_landed = [&](int n) {
+        return mbar_test_wait(bar_full(n % kStages), (n / kStages) & 1);
+      };
+      // Issue whichever MMA is ready: S_j once tile j has landed (and S buffer j & 1 is
+      // free, i.e. PV_{j-2} has been issued), PV_j once P_j is written.  PV never waits for
+      // the next tile's data, so stages are released as soon as their tile is done.
+      bool ok = mbar_wait(bar_q, 0, p.status);
+      if (ok) tc_fence_after();
+      int next_s = 0, next_pv = 0;
+      uint64_t t_last = global_timer_ns();
+      while (ok && next_pv < n_tiles) {
+        bool progress = false;
+        if (next_s < n_tiles && next_s <= next_pv + 1 && stage_landed(2 * next_s) &&
+            stage_landed(2 * next_s + 1)) {
+          tc_fence_after();
+          issue_s(next_s++);
+          progress = true;
+        }
+        if (next_pv < next_s && mbar_test_wait(bar_p, next_pv & 1)) {
+          tc_fence_after();
+          issue_pv(next_pv++);
+          progress = true;
+        }
+        if (progress) {
+          t_last = global_timer_ns();
+        } else if (global_timer_ns() - t_last > kWaitLimitNs) {
+          record_error(p.status, kDevTimeout);
+          ok = false;
+        }
       }
       tc_commit(bar_done);
       mbar_wait(bar_done, 0, nullptr);
@@ -342,11 +392,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (n_tiles - 1) & 1, p.status));
       tc_fence_after();
     }
-    // every softmax thread must reach this barrier, even after a failed wait
-    if (owner) stat_s[h] = l_run;
+    // every softmax thread must reach these barriers, even after a failed wait
+    if (owner) stat_s[h] = l_run > 0.f ? 1.f / l_run : 0.f;
     softmax_sync();
+    // Normalise O into the (now idle) KV ring as [head][latent dim] fp32 rows, then write
+    // each head's 2 KB row with 16-byte coalesced stores.
+    float* ostage = reinterpret_cast<float*>(smem + kKVOff);
     if (ok) {
-      const size_t row0 = static_cast<size_t>(b) * kH;
 #pragma unroll 1
       for (int db = 0; db < kDc / 128; ++db) {
         const int d = db * 128 + warp * 32 + lane;
@@ -356,13 +408,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tmem + kTmemO + lane_off + db * kH + half * 32, o);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int hh = half * 32 + e;
-            const float l = stat_s[hh];
-            const float v = l > 0.f ? __uint_as_float(o[e]) / l : 0.f;
-            p.o_part[((row0 + hh) * p.n_chunks + c) * kDc + d] = v;
-          }
+          for (int e = 0; e < 32; ++e)
+            ostage[(half * 32 + e) * kDc + d] = __uint_as_float(o[e]) * stat_s[half * 32 + e];
         }
+      }
+    }
+    softmax_sync();
+    if (ok) {
+      const size_t row0 = static_cast<size_t>(b) * kH;
+#pragma unroll 1
+      for (int r = 0; r < 16; ++r) {
+        const int hh = warp * 16 + r;
+        const float4* src = reinterpret_cast<const float4*>(ostage + hh * kDc);
+        float4* dst = reinterpret_cast<float4*>(p.o_part + ((row0 + hh) * p.n_chunks + c) * kDc);
+#pragma unroll
+        for (int k = 0; k < kDc / 4 / 32; ++k) dst[lane + 32 * k] = src[lane + 32 * k];
       }
       if (owner)
         p.lse_part[(row0 + h) * p.n_chunks + c] =
@@ -371,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -384,8 +444,7 @@ int mla_chunk_tokens(int, int, int) { return kChunk; }
 
 cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream) {
   if (p.H != kH || p.Dc != kDc || p.Dr != kDr || p.chunk != kChunk) return cudaErrorInvalidValue;
-  CUtensorMap tqn, tqp, tckv, tkpe;
-  const uint64_t rows = static_cast<uint64_t>(p.num_pages) * p.page_size;
+  CUtensorMap tqn, tqp;
   const uint64_t qrows = static_cast<uint64_t>(p.B) * kH;
   {
     const uint64_t dims[2] = {kDc, qrows};
@@ -403,26 +462,10 @@ cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream) {
                       CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  {
-    const uint64_t dims[2] = {kDc, rows > 0 ? rows : 1};
-    const uint64_t str[1] = {kDc * 2};
-    const uint32_t box[2] = {64, 1};  // gather4 reads four one-row boxes
-    if (!encode_tiled(&tckv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.ckv, dims, str, box,
-                      CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-  }
-  {
-    const uint64_t dims[2] = {kDr, rows > 0 ? rows : 1};
-    const uint64_t str[1] = {kDr * 2};
-    const uint32_t box[2] = {64, 1};
-    if (!encode_tiled(&tkpe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.kpe, dims, str, box,
-                      CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-  }
   cudaError_t e = ensure_smem_limit(mla_kernel, kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_chunks, p.B);
-  mla_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tqn, tqp, tckv, tkpe, p);
+  mla_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tqn, tqp, p);
   return cudaGetLastError();
 }
 
