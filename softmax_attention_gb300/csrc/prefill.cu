@@ -35,11 +35,13 @@ struct Layout {
   static constexpr int kKOff = kQBytes;
   static constexpr int kVOff = kKOff + STAGES * kKVBytes;
   static constexpr int kBarOff = kVOff + STAGES * kKVBytes;
-  // q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full, o_full, mma_done
-  static constexpr int kNumBars = 1 + 3 * STAGES + 2 + 3;
+  // q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full, o_full,
+  // mma_done
+  static constexpr int kNumBars = 1 + 4 * STAGES + 2 + 3;
   static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 bytes
   static_assert(D + 2 * BN <= 512, "tensor memory budget");
+  static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
 template <int D, int BN, int STAGES, bool BF16>
@@ -56,11 +58,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_q = bars;
   auto bar_k = [&](int s) { return bars + 8u * (1 + s); };
   auto bar_v = [&](int s) { return bars + 8u * (1 + STAGES + s); };
-  auto bar_e = [&](int s) { return bars + 8u * (1 + 2 * STAGES + s); };
-  auto bar_s = [&](int b) { return bars + 8u * (1 + 3 * STAGES + b); };
-  const uint32_t bar_p = bars + 8u * (3 + 3 * STAGES);
-  const uint32_t bar_o = bars + 8u * (4 + 3 * STAGES);
-  const uint32_t bar_done = bars + 8u * (5 + 3 * STAGES);
+  auto bar_ke = [&](int s) { return bars + 8u * (1 + 2 * STAGES + s); };
+  auto bar_ve = [&](int s) { return bars + 8u * (1 + 3 * STAGES + s); };
+  auto bar_s = [&](int b) { return bars + 8u * (1 + 4 * STAGES + b); };
+  const uint32_t bar_p = bars + 8u * (3 + 4 * STAGES);
+  const uint32_t bar_o = bars + 8u * (4 + 4 * STAGES);
+  const uint32_t bar_done = bars + 8u * (5 + 4 * STAGES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBarOff + L::kNumBars * 8);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -84,7 +87,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_k(s), 1);
       mbar_init(bar_v(s), 1);
-      mbar_init(bar_e(s), 1);
+      mbar_init(bar_ke(s), 1);
+      mbar_init(bar_ve(s), 1);
     }
     mbar_init(bar_s(0), 1);
     mbar_init(bar_s(1), 1);
@@ -114,15 +118,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < D / 64; ++kb)
         tma_load_4d(sQ + kb * (kRows * 128), &tm_q, bar_q, kb * 64, q0, hk * p.G, b);
       const int kv_row = b * p.Hkv + hk;
-      int issued = 0;
+      int issued = 0, k_only = -1;  // k_only: a K load issued without its V
+      // K and V slots are released separately: K_j once S_j is done, V_j once P_j V_j is.
       for (int jj = 0; jj < n; ++jj) {
         const int stage = jj % STAGES;
-        if (jj >= STAGES && !mbar_wait(bar_e(stage), ((jj / STAGES) - 1) & 1, p.status)) break;
+        if (jj >= STAGES && !mbar_wait(bar_ke(stage), ((jj / STAGES) - 1) & 1, p.status)) break;
         const int key0 = (t_begin + jj) * BN;
         mbar_arrive_expect_tx(bar_k(stage), L::kKVBytes);
         for (int kb = 0; kb < D / 64; ++kb)
           tma_load_3d(sK + stage * L::kKVBytes + kb * (BN * 128), &tm_k, bar_k(stage), kb * 64,
                       key0, kv_row);
+        if (jj >= STAGES && !mbar_wait(bar_ve(stage), ((jj / STAGES) - 1) & 1, p.status)) {
+          k_only = jj;  // K_jj is in flight; let it land below
+          break;
+        }
         mbar_arrive_expect_tx(bar_v(stage), L::kKVBytes);
         for (int kb = 0; kb < D / 64; ++kb)
           tma_load_3d(sV + stage * L::kKVBytes + kb * (BN * 128), &tm_v, bar_v(stage), kb * 64,
@@ -136,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(bar_k(jj % STAGES), (jj / STAGES) & 1, nullptr);
           mbar_wait(bar_v(jj % STAGES), (jj / STAGES) & 1, nullptr);
         }
+        if (k_only >= 0) mbar_wait(bar_k(k_only % STAGES), (k_only / STAGES) & 1, nullptr);
       }
     }
   } else if (warp == 5) {
@@ -154,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(d_s, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
         }
         tc_commit(bar_s(jj & 1));
+        tc_commit(bar_ke(jj % STAGES));
       };
       bool ok = mbar_wait(bar_q, 0, p.status) && mbar_wait(bar_k(0), 0, p.status);
       if (ok) {
@@ -179,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(tm_o, a_p + kk * 8, bd, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(bar_o);
-        tc_commit(bar_e(stage));
+        tc_commit(bar_ve(stage));
       }
       // Every MMA this thread issued must finish before tensor memory is released.
       tc_commit(bar_done);
@@ -215,52 +226,90 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&raw[c * 32]));
       tmem_ld_wait();
       const int key0 = (t_begin + jj) * BN;
-      float s[BN];
-      float row_max = -INFINITY;
-      if (mask_row) {
+      // x[c] is either the raw score (fast path: no mask tensor and scale > 0, so the row
+      // max of the raw scores times scale is the max of the scaled scores) or the finished
+      // log2-domain score (general path).  Masked keys hold -inf either way.  Eight
+      // independent max accumulators keep the reduction's dependency chain short.
+      const bool fast = !mask_row && p.scale_log2 > 0.f;
+      float x[BN];
+      float mx[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+      if (fast) {
+        if (key0 + BN <= key_lim) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) {
+            x[c] = __uint_as_float(raw[c]);
+            mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) {
+            x[c] = (key0 + c < key_lim) ? __uint_as_float(raw[c]) : -INFINITY;
+            mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+          }
+        }
+      } else if (mask_row) {
 #pragma unroll
         for (int c = 0; c < BN; ++c) {
           const int key = key0 + c;
-          float x = -INFINITY;
+          float v = -INFINITY;
           if (key < key_lim) {
             const float mv = p.mask_is_bf16
                                  ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(mask_row)[key])
                                  : reinterpret_cast<const float*>(mask_row)[key];
-            x = fmaf(__uint_as_float(raw[c]), p.scale_log2, mv * kLog2e);
+            v = fmaf(__uint_as_float(raw[c]), p.scale_log2, mv * kLog2e);
           }
-          s[c] = x;
-          row_max = fmaxf(row_max, x);
-        }
-      } else if (key0 + BN <= key_lim) {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          s[c] = __uint_as_float(raw[c]) * p.scale_log2;
-          row_max = fmaxf(row_max, s[c]);
+          x[c] = v;
+          mx[c & 7] = fmaxf(mx[c & 7], v);
         }
       } else {
 #pragma unroll
         for (int c = 0; c < BN; ++c) {
-          s[c] = (key0 + c < key_lim) ? __uint_as_float(raw[c]) * p.scale_log2 : -INFINITY;
-          row_max = fmaxf(row_max, s[c]);
+          x[c] = (key0 + c < key_lim) ? __uint_as_float(raw[c]) * p.scale_log2 : -INFINITY;
+          mx[c & 7] = fmaxf(mx[c & 7], x[c]);
         }
       }
+      float row_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                            fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      if (fast) row_max *= p.scale_log2;
       const float m_new = fmaxf(m_run, row_max);
-      // O must hold every earlier P V product before it is rescaled; waiting on each
-      // phase in turn also keeps this warp at most one tile ahead of the MMA issuer.
+      // Lazy rescale: the running max moves only when it grows by more than 2^8, so O and l
+      // are rescaled rarely; P is computed against the (possibly stale) m_run, which is
+      // exact after the final division by l.
+      const bool need = m_new > m_run + kRescaleLog2;
+      float alpha = 1.f;
+      if (need) {
+        alpha = exp2_approx(m_run - m_new);  // 0 when m_run is -inf
+        m_run = m_new;
+        l_run *= alpha;
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      // p = 2^(x * a - m): one packed fp32x2 FMA per pair, packed adds into four partial
+      // sums.  All of this overlaps the previous tile's P V on the tensor cores.
+      const float a = fast ? p.scale_log2 : 1.f;
+      const float2 a2 = make_float2(a, a), nm2 = make_float2(-m_use, -m_use);
+      float2 sum2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sum2[e] = make_float2(0.f, 0.f);
+      uint32_t pk[BN / 2];
+#pragma unroll
+      for (int c = 0; c < BN / 2; ++c) {
+        const float2 t = __ffma2_rn(make_float2(x[2 * c], x[2 * c + 1]), a2, nm2);
+        const float p0 = exp2_approx(t.x);
+        const float p1 = exp2_approx(t.y);
+        sum2[c & 3] = __fadd2_rn(sum2[c & 3], make_float2(p0, p1));
+        pk[c] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+      }
+      const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
+      l_run += (s01.x + s01.y) + (s23.x + s23.y);
+      // O must hold every earlier P V product before it is rescaled or fed P_j; waiting on
+      // each phase in turn also keeps this warp at most one tile ahead of the MMA issuer.
       if (jj > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (jj - 1) & 1, p.status));
         if (!ok) break;
         tc_fence_after();
-      }
-      const bool need = m_new > m_run + kRescaleLog2;
-      if (__any_sync(0xffffffffu, need)) {
-        float alpha = 1.f;
-        if (need) {
-          alpha = exp2_approx(m_run - m_new);  // 0 when m_run is -inf
-          m_run = m_new;
-          l_run *= alpha;
-        }
-        if (jj > 0) {
+        if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
@@ -270,20 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
             tmem_st32(tm_o + lane_off + c * 32, o);
           }
-          tmem_st_wait();
         }
       }
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      float sum = 0.f;
-      uint32_t pk[BN / 2];
-#pragma unroll
-      for (int c = 0; c < BN / 2; ++c) {
-        const float p0 = exp2_approx(s[2 * c] - m_use);
-        const float p1 = exp2_approx(s[2 * c + 1] - m_use);
-        sum += p0 + p1;
-        pk[c] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
-      }
-      l_run += sum;
 #pragma unroll
       for (int c = 0; c < BN / 2; c += 16)
         tmem_st16(t_s + c, *reinterpret_cast<uint32_t(*)[16]>(&pk[c]));
@@ -387,9 +424,9 @@ cudaError_t launch_prefill(const PrefillParams& p, Dtype operand, cudaStream_t s
   const bool bf16 = operand == Dtype::BF16;
   switch (p.D) {
     case 64:
-      return bf16 ? launch_impl<64, 128, 4, true>(p, stream) : launch_impl<64, 128, 4, false>(p, stream);
+      return bf16 ? launch_impl<64, 128, 5, true>(p, stream) : launch_impl<64, 128, 5, false>(p, stream);
     case 128:
-      return bf16 ? launch_impl<128, 128, 2, true>(p, stream) : launch_impl<128, 128, 2, false>(p, stream);
+      return bf16 ? launch_impl<128, 128, 3, true>(p, stream) : launch_impl<128, 128, 3, false>(p, stream);
     case 256:
       return bf16 ? launch_impl<256, 64, 2, true>(p, stream) : launch_impl<256, 64, 2, false>(p, stream);
     default:
