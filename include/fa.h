@@ -197,7 +197,7 @@ int mla_decode_paged_states(const void* q_nope, const void* q_pe, const void* ck
  *   o_parts [rows, max_splits, D] fp32 (normalised partial outputs), lse_parts
  *   [rows, max_splits] fp32 (natural log; -inf = empty part); n_splits [rows] int32 or NULL
  *   (= max_splits for every row); out [rows, D] in out_dtype; lse [rows] fp32 or NULL.
- *   D a multiple of 4.
+ *   D a multiple of 4, at most 512.
  */
 int fa_merge_states(const float* o_parts, const float* lse_parts, const int32_t* n_splits,
                     void* out, float* lse, int rows, int D, int max_splits, fa_dtype out_dtype,

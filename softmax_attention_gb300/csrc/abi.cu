@@ -648,6 +648,7 @@ int fa_merge_states(const float* o_parts, const float* lse_parts, const int32_t*
                     void* stream) {
   if (rows < 0 || D <= 0 || D % 4 != 0 || max_splits < 0)
     return fail(FA_ERR_INVALID_ARG, "fa_merge_states: need rows >= 0, D > 0 with D %% 4 == 0, max_splits >= 0");
+  if (D > 512) return fail(FA_ERR_UNSUPPORTED, "fa_merge_states: D must be <= 512 (got %d)", D);
   if (out_dtype != FA_BF16 && out_dtype != FA_FP16 && out_dtype != FA_FP32)
     return fail(FA_ERR_INVALID_ARG, "fa_merge_states: unknown out dtype %d", (int)out_dtype);
   if (rows == 0) return FA_OK;

@@ -5,8 +5,6 @@
 // which is the softmax over the union of the ranges.  Parts with lse_s = -inf (no key) get
 // weight 0; a row with no part, or only such parts, gives out = 0 and lse = -inf.  This is
 // the combine step of split-KV decoding and of a prefill whose KV loop is split across CTAs.
-// One warp per row; lanes stride over D in 16-byte vectors so the partial rows are read
-// with full sectors.
 #include <math.h>
 
 #include "internal.h"
@@ -15,9 +13,7 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 256;
 constexpr float kLog2e = 1.44269504088896340736f;
-constexpr float kLn2 = 0.69314718055994530942f;
 
 __device__ __forceinline__ void store4(void* out, Dtype t, size_t idx, float4 v) {
   if (t == Dtype::FP32) {
@@ -31,10 +27,17 @@ __device__ __forceinline__ void store4(void* out, Dtype t, size_t idx, float4 v)
   }
 }
 
-__global__ void __launch_bounds__(kThreads) merge_kernel(const MergeParams p) {
-  const int row = (blockIdx.x * kThreads + threadIdx.x) / 32;
-  const int lane = threadIdx.x % 32;
-  if (row >= p.rows) return;
+// One CTA (4 warps) per row.  Every warp reduces the row's log-sum-exps (cheap, L1-resident),
+// then warp w accumulates the parts s = w, w+4, ... over the whole row (lanes stride D in
+// 16-byte vectors, part loop unrolled so several loads are in flight), and the four partial
+// sums are combined through shared memory.
+constexpr int kMergeWarps = 4;
+constexpr int kMaxD = 512;
+
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p) {
+  __shared__ float4 part[kMergeWarps][kMaxD / 4];
+  const int row = blockIdx.x;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   int n = p.max_splits;
   if (p.n_splits) {
     n = p.n_splits[row];
@@ -55,23 +58,36 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const MergeParams p) {
   for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   const float lse = (m == -INFINITY) ? -INFINITY : m + logf(sum);
   const float* orow = p.o_part + static_cast<size_t>(row) * p.max_splits * p.D;
-  for (int d = lane * 4; d < p.D; d += 128) {
+  const int nv = p.D / 4;  // float4 per row
+  for (int v = lane; v < nv; v += 32) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (m != -INFINITY) {
-      for (int s = 0; s < n; ++s) {
+#pragma unroll 4
+      for (int s = warp; s < n; s += kMergeWarps) {
         const float ls = lrow[s];
-        if (ls == -INFINITY) continue;
-        const float w = exp2_approx((ls - lse) * kLog2e);
-        const float4 v = *reinterpret_cast<const float4*>(orow + static_cast<size_t>(s) * p.D + d);
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+        const float w = (ls == -INFINITY) ? 0.f : exp2_approx((ls - lse) * kLog2e);
+        const float4 x = reinterpret_cast<const float4*>(orow + static_cast<size_t>(s) * p.D)[v];
+        acc.x = fmaf(w, x.x, acc.x);
+        acc.y = fmaf(w, x.y, acc.y);
+        acc.z = fmaf(w, x.z, acc.z);
+        acc.w = fmaf(w, x.w, acc.w);
       }
     }
-    store4(p.out, p.out_dtype, static_cast<size_t>(row) * p.D + d, acc);
+    part[warp][v] = acc;
   }
-  if (lane == 0 && p.lse) p.lse[row] = lse;
+  __syncthreads();
+  for (int v = threadIdx.x; v < nv; v += kMergeWarps * 32) {
+    float4 t = part[0][v];
+#pragma unroll
+    for (int w = 1; w < kMergeWarps; ++w) {
+      t.x += part[w][v].x;
+      t.y += part[w][v].y;
+      t.z += part[w][v].z;
+      t.w += part[w][v].w;
+    }
+    store4(p.out, p.out_dtype, static_cast<size_t>(row) * p.D + 4 * v, t);
+  }
+  if (threadIdx.x == 0 && p.lse) p.lse[row] = lse;
 }
 
 __global__ void f32_to_f16_kernel(const float* __restrict__ src, __half* __restrict__ dst, size_t n) {
@@ -83,9 +99,8 @@ __global__ void f32_to_f16_kernel(const float* __restrict__ src, __half* __restr
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   if (p.rows <= 0) return cudaSuccess;
-  const int rows_per_block = kThreads / 32;
-  const int grid = (p.rows + rows_per_block - 1) / rows_per_block;
-  merge_kernel<<<grid, kThreads, 0, stream>>>(p);
+  if (p.D > kMaxD || p.D % 4 != 0) return cudaErrorInvalidValue;
+  merge_kernel<<<p.rows, kMergeWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

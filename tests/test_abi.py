@@ -122,6 +122,7 @@ def test_merge_rejects_bad_arguments(lib):
     assert lib.fa_merge_states(4096, 4096, None, 4096, None, 4, 6, 2, 0, None) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_merge_states(4096, 4096, None, 4096, None, 4, 8, 2, 9, None) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_merge_states(None, None, None, 4096, None, 0, 8, 2, 0, None) == fa.FA_OK
+    assert lib.fa_merge_states(4096, 4096, None, 4096, None, 4, 516, 2, 0, None) == fa.FA_ERR_UNSUPPORTED
 
 
 def test_size_queries_ignore_pointers(lib):
