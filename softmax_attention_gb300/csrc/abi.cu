@@ -463,8 +463,12 @@ cudaError_t mla_states(const void* q_nope, const void* q_pe, const void* ckv_pag
                        const void* kpe_pages, const int32_t* page_table, const int32_t* seq_lens,
                        float* o_part, float* lse_part, int chunk, int n_chunks, int B, int H,
                        int Dc, int Dr, int page_size, int max_pages_per_seq, int num_pages,
-                       float scale, uint32_t* status, cudaStream_t st) {
+                       float scale, uint32_t* status, cudaStream_t st, void* direct_out = nullptr,
+                       float* direct_lse = nullptr) {
   MlaParams p{};
+  p.direct = direct_out != nullptr;
+  p.out = direct_out;
+  p.lse = direct_lse;
   p.q_nope = q_nope;
   p.q_pe = q_pe;
   p.ckv = ckv_pages;
@@ -606,6 +610,14 @@ int mla_decode_paged(const void* q_nope, const void* q_pe, const void* ckv_pages
   if (!status) return fail(FA_ERR_CUDA, "mla_decode_paged: no usable CUDA device");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float *o_part = nullptr, *lse_part = nullptr;
+  if (n_chunks == 1) {
+    // every sequence fits one chunk: the kernel writes the final output, no merge
+    cudaError_t e = mla_states(q_nope, q_pe, ckv_pages, kpe_pages, page_table, seq_lens, nullptr,
+                               nullptr, chunk, 1, B, H, Dc, Dr, page_size, max_pages_per_seq,
+                               num_pages, scale, status, st, out, lse);
+    if (e != cudaSuccess) return cuda_fail("mla_decode_paged (MLA kernel)", e);
+    return FA_OK;
+  }
   if (n_chunks > 0) {
     carve(workspace, (long)B * H, n_chunks, Dc, &o_part, &lse_part);
     cudaError_t e = mla_states(q_nope, q_pe, ckv_pages, kpe_pages, page_table, seq_lens, o_part,

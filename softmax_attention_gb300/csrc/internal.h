@@ -76,6 +76,9 @@ struct MlaParams {
   float scale_log2;
   float* o_part;          // [B*H, n_chunks, Dc]
   float* lse_part;        // [B*H, n_chunks]
+  int direct;             // n_chunks == 1: write out/lse directly, no partial states
+  void* out;              // [B,H,Dc] bf16 (direct mode)
+  float* lse;             // [B,H] or nullptr (direct mode)
   uint32_t* status;
 };
 cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream);

@@ -45,7 +45,7 @@ constexpr int kThreads = 288;
 constexpr int kProducerThreads = 128;
 constexpr int kMmaWarp = 8;
 
-constexpr int kChunk = 512;                // tokens per CTA (multiple of kTile)
+constexpr int kMaxChunk = 2048;            // tokens per CTA: 512, 1024 or 2048
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -109,7 +109,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const int t_start = c * p.chunk;
-  if (t_start >= len) return;
+  if (t_start >= len) {
+    // an empty sequence still owns its final output when this launch writes it directly
+    if (p.direct && c == 0) {
+      for (int i = threadIdx.x; i < kH * kDc / 8; i += kThreads)
+        reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + static_cast<size_t>(b) * kH * kDc)[i] =
+            make_uint4(0, 0, 0, 0);
+      if (threadIdx.x < kH && p.lse) p.lse[static_cast<size_t>(b) * kH + threadIdx.x] = -INFINITY;
+    }
+    return;
+  }
   const int t_stop = min(len, t_start + p.chunk);
   const int n_tiles = (t_stop - t_start + kTile - 1) / kTile;
   const int n_stages = 2 * n_tiles;  // every tile is two 32-token stages
@@ -152,32 +161,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sQ + kb * (kH * 128), &tm_qn, bar_q, kb * 64, b * kH);
       tma_load_2d(sQ + (kDc / 64) * (kH * 128), &tm_qp, bar_q, 0, b * kH);
     }
-    // Row ids, read once with independent loads: lane l holds the row of token
-    // 32n + 8pw + (l & 7) for the stages n = (l >> 3) + 4m, m < 4.
-    int pages[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const int tok = t_start + 32 * ((lane >> 3) + 4 * m) + 8 * pw + (lane & 7);
-      pages[m] = tok < t_stop ? __ldg(table + tok / p.page_size) : -1;
-    }
+    // Row ids: a group is four 32-token stages; lane l holds the row of token
+    // 32 * (4g + (l >> 3)) + 8pw + (l & 7) of the current group g, and the page id of the
+    // same token of group g + 1 is loaded one group ahead.
     const int first_page = __ldg(table + t_start / p.page_size);
     int fill_row = (first_page >= 0 && first_page < p.num_pages)
                        ? first_page * p.page_size + t_start % p.page_size : 0;
     if (fill_row >= n_rows) fill_row = 0;
-    int rows[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const int tok = t_start + 32 * ((lane >> 3) + 4 * m) + 8 * pw + (lane & 7);
+    auto group_token = [&](int g) { return t_start + 32 * (4 * g + (lane >> 3)) + 8 * pw + (lane & 7); };
+    auto load_page = [&](int g) {
+      const int tok = group_token(g);
+      return tok < t_stop ? __ldg(table + tok / p.page_size) : -1;
+    };
+    auto page_to_row = [&](int page, int g) {
+      const int tok = group_token(g);
       int row = fill_row;  // tokens past the end read a valid row; their scores are masked
       if (tok < t_stop) {
-        if (pages[m] >= 0 && pages[m] < p.num_pages) {
-          row = pages[m] * p.page_size + tok % p.page_size;
+        if (page >= 0 && page < p.num_pages) {
+          row = page * p.page_size + tok % p.page_size;
         } else {
           record_error(p.status, kDevBounds);
         }
       }
-      rows[m] = (row >= 0 && row < n_rows) ? row : fill_row;
-    }
+      return (row >= 0 && row < n_rows) ? row : fill_row;
+    };
+    int row_cur = page_to_row(load_page(0), 0);
+    int page_next = load_page(1);
+    int cur_group = 0;
     const uint8_t* ckv = static_cast<const uint8_t*>(p.ckv);
     const uint8_t* kpe = static_cast<const uint8_t*>(p.kpe);
     // Issue a stage whenever its ring slot is free; otherwise publish the oldest issued
@@ -196,8 +206,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (can_issue) {
         const int n = issued;
         const uint32_t dst = sKV + (n % kStages) * kBlk;
-        // rows[n >> 2] needs a compile-time index: select it
-        const int rsel = (n >> 2) == 0 ? rows[0] : (n >> 2) == 1 ? rows[1] : (n >> 2) == 2 ? rows[2] : rows[3];
+        if ((n >> 2) != cur_group) {
+          cur_group = n >> 2;
+          row_cur = page_to_row(page_next, cur_group);
+          page_next = load_page(cur_group + 1);
+        }
+        const int rsel = row_cur;
 #pragma unroll
         for (int t8 = 0; t8 < 8; ++t8) {
           const int tok = 8 * pw + t8;
@@ -317,8 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_s(j & 1), (j >> 1) & 1, p.status));
       tc_fence_after();
       uint32_t raw[kTile];
-      tmem_ld32(tmem + kTmemS + lane_off + (j & 1) * kTile, *reinterpret_cast<uint32_t(*)[32]>(&raw[0]));
-      tmem_ld32(tmem + kTmemS + lane_off + (j & 1) * kTile + 32, *reinterpret_cast<uint32_t(*)[32]>(&raw[32]));
+      const uint32_t ts = tmem + kTmemS + lane_off + (j & 1) * kTile;
+      tmem_ld32(ts, *reinterpret_cast<uint32_t(*)[32]>(&raw[0]));
+      tmem_ld32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&raw[32]));
       tmem_ld_wait();
       const int tok0 = t_start + j * kTile;
       const int n_valid = min(kTile, t_stop - tok0);
@@ -420,13 +435,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; r < 16; ++r) {
         const int hh = warp * 16 + r;
         const float4* src = reinterpret_cast<const float4*>(ostage + hh * kDc);
-        float4* dst = reinterpret_cast<float4*>(p.o_part + ((row0 + hh) * p.n_chunks + c) * kDc);
+        if (p.direct) {
+          // the whole sequence was this CTA's chunk: write the final bf16 row
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + (row0 + hh) * kDc);
 #pragma unroll
-        for (int k = 0; k < kDc / 4 / 32; ++k) dst[lane + 32 * k] = src[lane + 32 * k];
+          for (int k = 0; k < kDc / 8 / 32; ++k) {
+            const float4 a = src[2 * (lane + 32 * k)], b2 = src[2 * (lane + 32 * k) + 1];
+            dst[lane + 32 * k] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
+                                            pack_bf16x2(b2.x, b2.y), pack_bf16x2(b2.z, b2.w));
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(p.o_part + ((row0 + hh) * p.n_chunks + c) * kDc);
+#pragma unroll
+          for (int k = 0; k < kDc / 4 / 32; ++k) dst[lane + 32 * k] = src[lane + 32 * k];
+        }
       }
-      if (owner)
-        p.lse_part[(row0 + h) * p.n_chunks + c] =
-            l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      if (owner) {
+        const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+        if (!p.direct) p.lse_part[(row0 + h) * p.n_chunks + c] = lse_v;
+        else if (p.lse) p.lse[row0 + h] = lse_v;
+      }
     }
   }
   tc_fence_before();
@@ -440,10 +468,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int mla_chunk_tokens(int, int, int) { return kChunk; }
+// Tokens per CTA: each CTA pays a fixed cost (pipeline start, epilogue) worth a few hundred
+// tokens of streaming, so prefer long chunks, but keep the waves of CTAs balanced.
+int mla_chunk_tokens(int B, int, int max_seq_len) {
+  const int sms = num_sms() > 0 ? num_sms() : 148;
+  const int len = ((max_seq_len + kTile - 1) / kTile) * kTile;
+  int best = 512;
+  long best_cost = -1;
+  for (int c = 512; c <= kMaxChunk; c *= 2) {
+    const long ctas = static_cast<long>(B) * ((max_seq_len + c - 1) / c);
+    const long waves = (ctas + sms - 1) / sms;
+    const long cost = waves * (static_cast<long>(c < len ? c : len) + 384);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = c;
+    }
+  }
+  return best;
+}
 
 cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream) {
-  if (p.H != kH || p.Dc != kDc || p.Dr != kDr || p.chunk != kChunk) return cudaErrorInvalidValue;
+  if (p.H != kH || p.Dc != kDc || p.Dr != kDr || p.chunk % kTile != 0 || p.chunk > kMaxChunk)
+    return cudaErrorInvalidValue;
+  if (p.direct && p.n_chunks != 1) return cudaErrorInvalidValue;
   CUtensorMap tqn, tqp;
   const uint64_t qrows = static_cast<uint64_t>(p.B) * kH;
   {

@@ -39,6 +39,7 @@ def _run(c: workloads.MlaCase, rows=None):
     ([0, 5, 1024], 1),
     ([17, 300, 1030], 16),
     ([200, 64], 64),
+    ([0, 100], 1),          # one chunk per sequence: final output written directly
 ])
 def test_parity_shapes(lens, ps):
     c = workloads.MlaCase(B=len(lens), H=64, seq_len=None, seq_lens=lens, page_size=ps,
