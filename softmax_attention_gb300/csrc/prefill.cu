@@ -16,16 +16,14 @@
 #include <math.h>
 
 #include "internal.h"
+#include "prefill_common.cuh"
 #include "sm103.cuh"
 
 namespace fa {
 namespace {
 
-constexpr int kRows = 128;
+using prefill::kRows;
 constexpr int kThreads = 192;
-constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the running max grows by > 2^8
-constexpr float kLn2 = 0.69314718055994530942f;
-constexpr float kLog2e = 1.44269504088896340736f;
 
 template <int D, int BN, int STAGES>
 struct Layout {
@@ -74,12 +72,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hk = blockIdx.y, b = blockIdx.z;
   const int q0 = qt * p.q_per_tile;
   const int q_last = min(p.Lq, q0 + p.q_per_tile) - 1;
-  int kv_end = p.Lkv;
-  if (p.causal) kv_end = min(p.Lkv, q_last + (p.Lkv - p.Lq) + 1);
-  const int n_kv_tiles = kv_end > 0 ? (kv_end + BN - 1) / BN : 0;
-  const int per_split = (n_kv_tiles + p.n_splits - 1) / p.n_splits;
-  const int t_begin = min(n_kv_tiles, split * per_split);
-  const int t_end = min(n_kv_tiles, t_begin + per_split);
+  int t_begin, t_end;
+  prefill::kv_range(p, q_last, BN, split, t_begin, t_end);
   const int n = t_end - t_begin;
 
   if (threadIdx.x == 0) {
@@ -198,132 +192,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------- softmax + epilogue (row per thread) ----------------------
-    const int r = threadIdx.x;
-    const int g = r / p.q_per_tile, il = r % p.q_per_tile;
-    const int i = q0 + il;
-    const bool row_valid = (g < p.G) && (i < p.Lq);
-    const int h = hk * p.G + g;
-    int key_lim = 0;  // keys j < key_lim are visible before the additive mask
-    if (row_valid) key_lim = p.causal ? min(p.Lkv, i + (p.Lkv - p.Lq) + 1) : p.Lkv;
+    const prefill::Row row = prefill::make_row(p, b, hk, q0, threadIdx.x);
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const char* mask_row = nullptr;
-    if (p.mask && row_valid) {
-      const int mb = p.mask_batches == 1 ? 0 : b;
-      const size_t off = (static_cast<size_t>(mb) * p.Lq + i) * static_cast<size_t>(p.Lkv);
-      mask_row = static_cast<const char*>(p.mask) + off * (p.mask_is_bf16 ? 2 : 4);
-    }
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int jj = 0; jj < n; ++jj) {
-      const int buf = jj & 1;
-      const uint32_t t_s = tm_s0 + lane_off + buf * BN;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_s(buf), (jj >> 1) & 1, p.status));
+      const uint32_t t_s = tm_s0 + lane_off + (jj & 1) * BN;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_s(jj & 1), (jj >> 1) & 1, p.status));
       if (!ok) break;
       tc_fence_after();
       uint32_t raw[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c)
-        tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&raw[c * 32]));
-      tmem_ld_wait();
-      const int key0 = (t_begin + jj) * BN;
-      // x[c] is either the raw score (fast path: no mask tensor and scale > 0, so the row
-      // max of the raw scores times scale is the max of the scaled scores) or the finished
-      // log2-domain score (general path).  Masked keys hold -inf either way.  Eight
-      // independent max accumulators keep the reduction's dependency chain short.
-      const bool fast = !mask_row && p.scale_log2 > 0.f;
-      float x[BN];
-      float mx[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
-      if (fast) {
-        if (key0 + BN <= key_lim) {
-#pragma unroll
-          for (int c = 0; c < BN; ++c) {
-            x[c] = __uint_as_float(raw[c]);
-            mx[c & 7] = fmaxf(mx[c & 7], x[c]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < BN; ++c) {
-            x[c] = (key0 + c < key_lim) ? __uint_as_float(raw[c]) : -INFINITY;
-            mx[c & 7] = fmaxf(mx[c & 7], x[c]);
-          }
-        }
-      } else if (mask_row) {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          const int key = key0 + c;
-          float v = -INFINITY;
-          if (key < key_lim) {
-            const float mv = p.mask_is_bf16
-                                 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(mask_row)[key])
-                                 : reinterpret_cast<const float*>(mask_row)[key];
-            v = fmaf(__uint_as_float(raw[c]), p.scale_log2, mv * kLog2e);
-          }
-          x[c] = v;
-          mx[c & 7] = fmaxf(mx[c & 7], v);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          x[c] = (key0 + c < key_lim) ? __uint_as_float(raw[c]) * p.scale_log2 : -INFINITY;
-          mx[c & 7] = fmaxf(mx[c & 7], x[c]);
-        }
-      }
-      float row_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                            fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      if (fast) row_max *= p.scale_log2;
-      const float m_new = fmaxf(m_run, row_max);
-      // Lazy rescale: the running max moves only when it grows by more than 2^8, so O and l
-      // are rescaled rarely; P is computed against the (possibly stale) m_run, which is
-      // exact after the final division by l.
-      const bool need = m_new > m_run + kRescaleLog2;
-      float alpha = 1.f;
-      if (need) {
-        alpha = exp2_approx(m_run - m_new);  // 0 when m_run is -inf
-        m_run = m_new;
-        l_run *= alpha;
-      }
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      // p = 2^(x * a - m): one packed fp32x2 FMA per pair, packed adds into four partial
-      // sums.  All of this overlaps the previous tile's P V on the tensor cores.
-      const float a = fast ? p.scale_log2 : 1.f;
-      const float2 a2 = make_float2(a, a), nm2 = make_float2(-m_use, -m_use);
-      float2 sum2[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sum2[e] = make_float2(0.f, 0.f);
+      prefill::load_s<BN>(t_s, raw);
+      float alpha;
       uint32_t pk[BN / 2];
-#pragma unroll
-      for (int c = 0; c < BN / 2; ++c) {
-        const float2 t = __ffma2_rn(make_float2(x[2 * c], x[2 * c + 1]), a2, nm2);
-        const float p0 = exp2_approx(t.x);
-        const float p1 = exp2_approx(t.y);
-        sum2[c & 3] = __fadd2_rn(sum2[c & 3], make_float2(p0, p1));
-        pk[c] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
-      }
-      const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
-      l_run += (s01.x + s01.y) + (s23.x + s23.y);
+      // the exponentials overlap the previous tile's P V on the tensor cores
+      const bool need = prefill::softmax_tile<BN, BF16>(p, row, (t_begin + jj) * BN, raw, m_run,
+                                                        l_run, alpha, pk);
       // O must hold every earlier P V product before it is rescaled or fed P_j; waiting on
       // each phase in turn also keeps this warp at most one tile ahead of the MMA issuer.
       if (jj > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (jj - 1) & 1, p.status));
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tm_o + lane_off + c * 32, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tm_o + lane_off + c * 32, o);
-          }
-        }
+        if (__any_sync(0xffffffffu, need)) prefill::rescale_o<D>(tm_o + lane_off, alpha);
       }
-#pragma unroll
-      for (int c = 0; c < BN / 2; c += 16)
-        tmem_st16(t_s + c, *reinterpret_cast<uint32_t(*)[16]>(&pk[c]));
+      prefill::store_p<BN>(t_s, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_p);
@@ -332,51 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (n - 1) & 1, p.status));
       tc_fence_after();
     }
-    if (ok) {
-      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-      const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-      const size_t row_flat = (static_cast<size_t>(b) * p.Hq + h) * p.Lq + i;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        if (n > 0) {
-          tmem_ld32(tm_o + lane_off + c * 32, o);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
-        if (!row_valid) continue;
-        float v[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv_l;
-        if (p.n_splits > 1) {
-          float4* dst = reinterpret_cast<float4*>(
-              p.o_part + (row_flat * p.n_splits + split) * D + c * 32);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-        } else if (p.out_dtype == Dtype::FP32) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + row_flat * D + c * 32);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-        } else {
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = (p.out_dtype == Dtype::BF16) ? pack_bf16x2(v[2 * e], v[2 * e + 1])
-                                                : pack_f16x2(v[2 * e], v[2 * e + 1]);
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row_flat * D + c * 32);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-        }
-      }
-      if (row_valid) {
-        if (p.n_splits > 1) p.lse_part[row_flat * p.n_splits + split] = lse_v;
-        else if (p.lse) p.lse[row_flat] = lse_v;
-      }
-    }
+    if (ok) prefill::epilogue<D>(p, row, tm_o + lane_off, n > 0, m_run, l_run, split);
   }
   tc_fence_before();
   __syncthreads();
