@@ -399,7 +399,7 @@ def run_reference(args, dist: Dist):
     dt, fl = oracle_rate(c, q, k, v, 16)
     per_row = dt / 16
     total_steps = args.steps + args.warmup
-    rows_per_step = int(max(1, min(4096, 120.0 / max(1e-6, per_row) / total_steps)))
+    rows_per_step = int(max(1, min(4096, args.ref_seconds / max(1e-6, per_row) / total_steps)))
     for w in range(args.warmup):
         oracle_rate(c, q, k, v, rows_per_step, offset=w)
     t_sum, f_sum = 0.0, 0.0
@@ -434,6 +434,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="CPU time budget of the --impl reference run (all steps)")
     ap.add_argument("--only", choices=("decode", "mla", "mqa"), default=None,
                     help="run the headline plus only this path (for profiling)")
     args = ap.parse_args()
