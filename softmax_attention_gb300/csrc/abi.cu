@@ -188,11 +188,14 @@ PrefillPlan plan_prefill(const fa_prefill_args* a) {
   } else if (kv_tiles > 0) {
     const long tiles = (long)pl.n_qtiles * a->Hkv * a->B;
     const int sms = num_sms() > 0 ? num_sms() : 148;
-    // One CTA per SM fits; split the KV loop only when the tiles cover less than half
-    // the SMs, keeping at least two KV tiles per split.
+    // One CTA per SM fits.  Split the KV loop only when the tiles cover less than half the
+    // SMs, into as many parts as still fit one wave, keeping at least four KV tiles per
+    // part: each part pays a fixed cost (Q load, pipeline fill) and writes a partial state
+    // as large as its output, so more parts than that cost more than they gain.
     if (tiles > 0 && tiles * 2 <= sms) {
-      s = (int)((sms + tiles - 1) / tiles);
-      s = s < kv_tiles / 2 ? s : (kv_tiles / 2 > 1 ? kv_tiles / 2 : 1);
+      s = (int)(sms / tiles);
+      const int cap = kv_tiles / 4 > 1 ? kv_tiles / 4 : 1;
+      if (s > cap) s = cap;
     }
   }
   if (kv_tiles > 0 && s > kv_tiles) s = kv_tiles;

@@ -27,16 +27,18 @@ __device__ __forceinline__ void store4(void* out, Dtype t, size_t idx, float4 v)
   }
 }
 
-// One CTA (4 warps) per row.  Every warp reduces the row's log-sum-exps (cheap, L1-resident),
-// then warp w accumulates the parts s = w, w+4, ... over the whole row (lanes stride D in
-// 16-byte vectors, part loop unrolled so several loads are in flight), and the four partial
-// sums are combined through shared memory.
+// One CTA (4 warps) per (row, 128-column chunk).  Every warp reduces the row's log-sum-exps
+// (cheap, L1-resident); warp w accumulates the parts s = w, w+4, ... of the chunk (lane l
+// reads the 16-byte vector l, part loop unrolled so several loads are in flight), and the
+// four partial sums are combined through shared memory.  Splitting the row across CTAs keeps
+// few-row, many-part merges (a short query chunk split over the KV loop) parallel.
 constexpr int kMergeWarps = 4;
-constexpr int kMaxD = 512;
+constexpr int kChunkCols = 128;
 
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p) {
-  __shared__ float4 part[kMergeWarps][kMaxD / 4];
+  __shared__ float4 part[kMergeWarps][32];
   const int row = blockIdx.x;
+  const int v = blockIdx.y * 32 + threadIdx.x % 32;  // float4 index in the row
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   int n = p.max_splits;
   if (p.n_splits) {
@@ -58,36 +60,34 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
   for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   const float lse = (m == -INFINITY) ? -INFINITY : m + logf(sum);
   const float* orow = p.o_part + static_cast<size_t>(row) * p.max_splits * p.D;
-  const int nv = p.D / 4;  // float4 per row
-  for (int v = lane; v < nv; v += 32) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (m != -INFINITY) {
+  const bool in_row = v < p.D / 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (in_row && m != -INFINITY) {
 #pragma unroll 4
-      for (int s = warp; s < n; s += kMergeWarps) {
-        const float ls = lrow[s];
-        const float w = (ls == -INFINITY) ? 0.f : exp2_approx((ls - lse) * kLog2e);
-        const float4 x = reinterpret_cast<const float4*>(orow + static_cast<size_t>(s) * p.D)[v];
-        acc.x = fmaf(w, x.x, acc.x);
-        acc.y = fmaf(w, x.y, acc.y);
-        acc.z = fmaf(w, x.z, acc.z);
-        acc.w = fmaf(w, x.w, acc.w);
-      }
+    for (int s = warp; s < n; s += kMergeWarps) {
+      const float ls = lrow[s];
+      const float w = (ls == -INFINITY) ? 0.f : exp2_approx((ls - lse) * kLog2e);
+      const float4 x = reinterpret_cast<const float4*>(orow + static_cast<size_t>(s) * p.D)[v];
+      acc.x = fmaf(w, x.x, acc.x);
+      acc.y = fmaf(w, x.y, acc.y);
+      acc.z = fmaf(w, x.z, acc.z);
+      acc.w = fmaf(w, x.w, acc.w);
     }
-    part[warp][v] = acc;
   }
+  part[warp][lane] = acc;
   __syncthreads();
-  for (int v = threadIdx.x; v < nv; v += kMergeWarps * 32) {
-    float4 t = part[0][v];
+  if (warp == 0 && in_row) {
+    float4 t = part[0][lane];
 #pragma unroll
     for (int w = 1; w < kMergeWarps; ++w) {
-      t.x += part[w][v].x;
-      t.y += part[w][v].y;
-      t.z += part[w][v].z;
-      t.w += part[w][v].w;
+      t.x += part[w][lane].x;
+      t.y += part[w][lane].y;
+      t.z += part[w][lane].z;
+      t.w += part[w][lane].w;
     }
     store4(p.out, p.out_dtype, static_cast<size_t>(row) * p.D + 4 * v, t);
   }
-  if (threadIdx.x == 0 && p.lse) p.lse[row] = lse;
+  if (threadIdx.x == 0 && blockIdx.y == 0 && p.lse) p.lse[row] = lse;
 }
 
 __global__ void f32_to_f16_kernel(const float* __restrict__ src, __half* __restrict__ dst, size_t n) {
@@ -99,8 +99,9 @@ __global__ void f32_to_f16_kernel(const float* __restrict__ src, __half* __restr
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   if (p.rows <= 0) return cudaSuccess;
-  if (p.D > kMaxD || p.D % 4 != 0) return cudaErrorInvalidValue;
-  merge_kernel<<<p.rows, kMergeWarps * 32, 0, stream>>>(p);
+  if (p.D > 512 || p.D % 4 != 0) return cudaErrorInvalidValue;
+  dim3 grid(p.rows, (p.D + kChunkCols - 1) / kChunkCols);
+  merge_kernel<<<grid, kMergeWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
