@@ -319,9 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar_done, 0, nullptr);
     }
   } else {
-    // ---------------------- softmax (thread per head) + epilogue ---------------------------
-    const bool owner = lane < 16;          // lanes 32w..32w+15 hold heads 16w..16w+15
-    const int h = warp * 16 + lane;
+    // ---------------------- softmax (two threads per head) + epilogue ---------------------
+    // Lanes i and 16 + i of warp w both work on head h = 16w + i: the first on the tile's
+    // tokens 0-31, the second on tokens 32-63.  The M=64 score layout puts the head's row in
+    // tensor-memory lane 32w + i, so the second half is handed over with shuffles.  Both
+    // lanes keep the same running max and sum.
+    const int hl = lane & 15, half_t = lane >> 4;
+    const bool lead = half_t == 0;
+    const int h = warp * 16 + hl;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
@@ -335,22 +340,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(ts, *reinterpret_cast<uint32_t(*)[32]>(&raw[0]));
       tmem_ld32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&raw[32]));
       tmem_ld_wait();
-      const int tok0 = t_start + j * kTile;
-      const int n_valid = min(kTile, t_stop - tok0);
-      float s[kTile];
+      const int n_valid = t_stop - (t_start + j * kTile + half_t * (kTile / 2));
+      float s[kTile / 2];
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int e = 0; e < kTile; ++e) {
-        s[e] = (e < n_valid) ? __uint_as_float(raw[e]) * p.scale_log2 : -INFINITY;
+      for (int e = 0; e < kTile / 2; ++e) {
+        const uint32_t hi = __shfl_sync(0xffffffffu, raw[kTile / 2 + e], hl);
+        const float v = __uint_as_float(half_t ? hi : raw[e]);
+        s[e] = (e < n_valid) ? v * p.scale_log2 : -INFINITY;
         mx[e & 3] = fmaxf(mx[e & 3], s[e]);
       }
-      float m_new = fmaxf(m_run, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
-      if (!owner) m_new = m_run;
+      float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 16));
+      const float m_new = fmaxf(m_run, mloc);
       if (j > 0 && ok) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (j - 1) & 1, p.status));
         tc_fence_after();
       }
-      const bool need = owner && (m_new > m_run + kRescaleLog2);
+      const bool need = m_new > m_run + kRescaleLog2;
       if (softmax_any(need)) {
         float alpha = 1.f;
         if (need) {
@@ -358,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run = m_new;
           l_run *= alpha;
         }
-        if (owner) alpha_s[h] = alpha;
+        if (lead) alpha_s[h] = alpha;
         softmax_sync();
         if (j > 0) {
           // O^T column h belongs to head h; every lane holds one latent dim of every head
@@ -382,23 +389,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       float sum[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[kTile / 2];
+      uint32_t pk[kTile / 4];
 #pragma unroll
-      for (int e = 0; e < kTile / 2; ++e) {
+      for (int e = 0; e < kTile / 4; ++e) {
         const float p0 = exp2_approx(s[2 * e] - m_use);
         const float p1 = exp2_approx(s[2 * e + 1] - m_use);
         sum[e & 3] += p0 + p1;
         pk[e] = pack_bf16x2(p0, p1);
       }
-      if (owner) {
-        l_run += (sum[0] + sum[1]) + (sum[2] + sum[3]);
-        // P^T row h: 64 tokens x bf16 = 128 bytes, 16-byte chunks swizzled by h % 8
-        uint8_t* prow = smem + kPOff + h * 128;
+      const float lsum = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+      l_run += lsum + __shfl_xor_sync(0xffffffffu, lsum, 16);  // the same total in both lanes
+      // P^T row h: 64 tokens x bf16 = 128 bytes, 16-byte chunks swizzled by h % 8; this
+      // lane's tokens are chunks 4 * half_t .. 4 * half_t + 3
+      uint8_t* prow = smem + kPOff + h * 128;
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8)
-          *reinterpret_cast<uint4*>(prow + ((c8 ^ (h & 7)) * 16)) =
-              make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
-      }
+      for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<uint4*>(prow + (((4 * half_t + k) ^ (h & 7)) * 16)) =
+            make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_p);
@@ -408,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     // every softmax thread must reach these barriers, even after a failed wait
-    if (owner) stat_s[h] = l_run > 0.f ? 1.f / l_run : 0.f;
+    if (lead) stat_s[h] = l_run > 0.f ? 1.f / l_run : 0.f;
     softmax_sync();
     // Normalise O into the (now idle) KV ring as [head][latent dim] fp32 rows, then write
     // each head's 2 KB row with 16-byte coalesced stores.
@@ -450,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kDc / 4 / 32; ++k) dst[lane + 32 * k] = src[lane + 32 * k];
         }
       }
-      if (owner) {
+      if (lead) {
         const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
         if (!p.direct) p.lse_part[(row0 + h) * p.n_chunks + c] = lse_v;
         else if (p.lse) p.lse[row0 + h] = lse_v;
