@@ -208,6 +208,14 @@ int fa_merge_states(const float* o_parts, const float* lse_parts, const int32_t*
  * clears it. */
 int fa_get_device_status(void* stream);
 
+/* Self-test of the device failure path shared by every kernel above: launches one CTA that
+ * waits, with a limit of timeout_us microseconds (1 .. 2000000, the kernels' own limit being
+ * 2 s), on a barrier that nothing arrives on.  The wait runs out, the kernel records
+ * FA_ERR_TIMEOUT in the sticky status word and ends, so a following fa_get_device_status()
+ * returns FA_ERR_TIMEOUT and the device stays usable.  Returns FA_OK once enqueued,
+ * FA_ERR_INVALID_ARG for a timeout outside the range. */
+int fa_selftest_wait_timeout(unsigned timeout_us, void* stream);
+
 /* Message for the last error returned on the calling thread ("" if none). */
 const char* fa_last_error(void);
 

@@ -36,7 +36,7 @@ EXPORTS = (
     "fa_decode_paged_noalloc",
     "fa_decode_paged_states", "mla_decode_paged", "mla_decode_workspace_size",
     "mla_decode_chunk_tokens", "mla_decode_paged_states", "fa_merge_states",
-    "fa_get_device_status", "fa_last_error", "fa_version",
+    "fa_get_device_status", "fa_selftest_wait_timeout", "fa_last_error", "fa_version",
 )
 
 
@@ -104,6 +104,8 @@ def load_library(path: str | None = None):
         lib.fa_merge_states.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
         lib.fa_get_device_status.restype = _i
         lib.fa_get_device_status.argtypes = [_vp]
+        lib.fa_selftest_wait_timeout.restype = _i
+        lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, _vp]
         lib.fa_last_error.restype = ctypes.c_char_p
         lib.fa_last_error.argtypes = []
         lib.fa_version.restype = _i
@@ -127,6 +129,13 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _need_dtype(dtype, *ts):
+    """The C entry points take raw pointers; element types are checked here."""
+    for t in ts:
+        if t is not None and t.dtype != dtype:
+            raise ValueError(f"expected {dtype}, got {t.dtype}")
+
+
 def _need_cuda(*ts):
     for t in ts:
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
@@ -148,7 +157,9 @@ def fa_prefill(q, k, v, causal: bool = False, scale: float | None = None, out=No
                stream=None):
     """bf16 dense attention through the short-form entry point (no KV split)."""
     lib = load_library()
-    _need_cuda(q, k, v)
+    _need_dtype(torch.bfloat16, q, k, v, out)
+    _need_dtype(torch.float32, lse)
+    _need_cuda(q, k, v, out, lse)
     B, Hq, Lq, D = q.shape
     Hkv, Lkv = k.shape[1], k.shape[2]
     if scale is None:
@@ -193,7 +204,9 @@ def fa_prefill_ex(q, k, v, *, causal=False, scale=None, mask=None, num_splits=0,
     """Dense attention, any supported dtype (bf16/fp16/fp32), optional additive mask
     [1 or B, Lq, Lkv], optional KV split (0 = library's choice)."""
     lib = load_library()
-    _need_cuda(q, k, v, mask)
+    _need_dtype(q.dtype, k, v, out)
+    _need_dtype(torch.float32, lse)
+    _need_cuda(q, k, v, mask, out, lse)
     B, Hq, Lq, D = q.shape
     if out is None:
         out = torch.empty_like(q)
@@ -227,6 +240,8 @@ def fa_decode_paged(q, k_pages, v_pages, page_table, seq_lens, max_seq_len: int,
     """Split-KV paged GQA decode.  q [B,Hq,D] bf16; pages [num_pages,Hkv,page_size,D];
     page_table [B,max_pages] int32; seq_lens [B] int32 (device)."""
     lib = load_library()
+    _need_dtype(torch.bfloat16, q, k_pages, v_pages)
+    _need_dtype(torch.int32, page_table, seq_lens)
     _need_cuda(q, k_pages, v_pages, page_table, seq_lens)
     B, Hq, D = q.shape
     num_pages, Hkv, page_size, _ = k_pages.shape
@@ -236,6 +251,9 @@ def fa_decode_paged(q, k_pages, v_pages, page_table, seq_lens, max_seq_len: int,
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    _need_dtype(torch.bfloat16, out)
+    _need_dtype(torch.float32, lse)
+    _need_cuda(out, lse)
     ws = _workspace(lib.fa_decode_workspace_size(B, Hq, D, max_seq_len), q.device, workspace)
     _check(lib.fa_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
                                _ptr(seq_lens), _ptr(out), _ptr(lse), B, Hq, Hkv, D, page_size,
@@ -250,6 +268,9 @@ def fa_decode_paged_noalloc(q, k_pages, v_pages, page_table, seq_lens, max_seq_l
     fixed device scratch is used instead (problems needing more than it holds are refused).
     Calls that overlap on the GPU share that scratch and race."""
     lib = load_library()
+    _need_dtype(torch.bfloat16, q, k_pages, v_pages, out)
+    _need_dtype(torch.int32, page_table, seq_lens)
+    _need_dtype(torch.float32, lse)
     _need_cuda(q, k_pages, v_pages, page_table, seq_lens, out, lse)
     B, Hq, D = q.shape
     num_pages, Hkv, page_size, _ = k_pages.shape
@@ -275,6 +296,8 @@ def fa_decode_paged_states(q, k_pages, v_pages, page_table, seq_lens, max_seq_le
     """Per-chunk split-KV states of paged decode (no merge).  Returns (o_parts
     [B*Hq, n_chunks, D] fp32, lse_parts [B*Hq, n_chunks] fp32, chunk)."""
     lib = load_library()
+    _need_dtype(torch.bfloat16, q, k_pages, v_pages)
+    _need_dtype(torch.int32, page_table, seq_lens)
     _need_cuda(q, k_pages, v_pages, page_table, seq_lens)
     B, Hq, D = q.shape
     num_pages, Hkv, page_size, _ = k_pages.shape
@@ -302,6 +325,8 @@ def mla_decode_paged_states(q_nope, q_pe, ckv, kpe, page_table, seq_lens, max_se
     """Per-chunk split-KV states of MLA decode (no merge).  Returns (o_parts, lse_parts,
     chunk)."""
     lib = load_library()
+    _need_dtype(torch.bfloat16, q_nope, q_pe, ckv, kpe)
+    _need_dtype(torch.int32, page_table, seq_lens)
     _need_cuda(q_nope, q_pe, ckv, kpe, page_table, seq_lens)
     B, H, Dc = q_nope.shape
     Dr = q_pe.shape[2]
@@ -329,6 +354,8 @@ def mla_decode_paged(q_nope, q_pe, ckv, kpe, page_table, seq_lens, max_seq_len: 
     """MLA paged decode (latent form).  q_nope [B,H,512], q_pe [B,H,64] bf16;
     ckv [P,page_size,512], kpe [P,page_size,64]; page_table [B,max_pages]; seq_lens [B]."""
     lib = load_library()
+    _need_dtype(torch.bfloat16, q_nope, q_pe, ckv, kpe)
+    _need_dtype(torch.int32, page_table, seq_lens)
     _need_cuda(q_nope, q_pe, ckv, kpe, page_table, seq_lens)
     B, H, Dc = q_nope.shape
     Dr = q_pe.shape[2]
@@ -337,6 +364,9 @@ def mla_decode_paged(q_nope, q_pe, ckv, kpe, page_table, seq_lens, max_seq_len: 
         out = torch.empty_like(q_nope)
     if lse is None:
         lse = torch.empty(B, H, dtype=torch.float32, device=q_nope.device)
+    _need_dtype(torch.bfloat16, out)
+    _need_dtype(torch.float32, lse)
+    _need_cuda(out, lse)
     ws = _workspace(lib.mla_decode_workspace_size(B, H, Dc, max_seq_len), q_nope.device, workspace)
     _check(lib.mla_decode_paged(_ptr(q_nope), _ptr(q_pe), _ptr(ckv), _ptr(kpe), _ptr(page_table),
                                 _ptr(seq_lens), _ptr(out), _ptr(lse), B, H, Dc, Dr, page_size,
@@ -349,7 +379,9 @@ def fa_merge_states(o_parts, lse_parts, n_splits=None, out_dtype=torch.bfloat16,
                     lse=None, stream=None):
     """Merge partial states: o_parts [rows,S,D] fp32, lse_parts [rows,S] fp32."""
     lib = load_library()
-    _need_cuda(o_parts, lse_parts, n_splits)
+    _need_dtype(torch.float32, o_parts, lse_parts, lse)
+    _need_dtype(torch.int32, n_splits)
+    _need_cuda(o_parts, lse_parts, n_splits, out, lse)
     rows, S, D = o_parts.shape
     if out is None:
         out = torch.empty(rows, D, dtype=out_dtype, device=o_parts.device)
@@ -363,6 +395,12 @@ def fa_merge_states(o_parts, lse_parts, n_splits=None, out_dtype=torch.bfloat16,
 def fa_get_device_status(stream=None) -> int:
     """Synchronise, return and clear the library's sticky device status (0 = OK)."""
     return load_library().fa_get_device_status(_stream(stream))
+
+
+def fa_selftest_wait_timeout(timeout_us: int, stream=None) -> int:
+    """Enqueue the failure-path self-test (a bounded wait that runs out); returns the call's
+    status.  Read the result with fa_get_device_status(): FA_ERR_TIMEOUT."""
+    return load_library().fa_selftest_wait_timeout(int(timeout_us), _stream(stream))
 
 
 def fa_last_error() -> str:

@@ -703,6 +703,18 @@ int fa_get_device_status(void* stream) {
   return FA_OK;
 }
 
+int fa_selftest_wait_timeout(unsigned timeout_us, void* stream) {
+  if (timeout_us == 0 || timeout_us > kWaitLimitNs / 1000)
+    return fail(FA_ERR_INVALID_ARG, "fa_selftest_wait_timeout: timeout_us must be in [1, %llu]",
+                static_cast<unsigned long long>(kWaitLimitNs / 1000));
+  uint32_t* status = device_status_ptr();
+  if (!status) return fail(FA_ERR_CUDA, "fa_selftest_wait_timeout: no usable CUDA device");
+  cudaError_t e = launch_selftest_wait(static_cast<uint64_t>(timeout_us) * 1000, status,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("fa_selftest_wait_timeout", e);
+  return FA_OK;
+}
+
 const char* fa_last_error(void) { return g_err; }
 
 int fa_version(void) { return 100; }

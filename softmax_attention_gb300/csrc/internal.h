@@ -82,6 +82,9 @@ struct MlaParams {
   uint32_t* status;
 };
 cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream);
+
+// Self-test of the bounded-wait failure path (selftest.cu).
+cudaError_t launch_selftest_wait(uint64_t limit_ns, uint32_t* status, cudaStream_t stream);
 int mla_chunk_tokens(int B, int H, int max_seq_len);
 
 // ---------------------------------------------------------------------------------------

@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import softmax_attention_gb300 as fa
 from softmax_attention_gb300 import build as fa_build
@@ -130,3 +131,25 @@ def test_size_queries_ignore_pointers(lib):
     assert lib.fa_prefill_workspace_size(ctypes.byref(a)) > 0
     a = _args(num_splits=3, Lkv=4096, q=None, out=None)
     assert lib.fa_prefill_num_splits(ctypes.byref(a)) == 3
+
+
+def test_selftest_rejects_bad_timeouts(lib):
+    # validated on the host, before any device is touched
+    for t in (0, 2_000_001, 10**9):
+        assert lib.fa_selftest_wait_timeout(t, None) == fa.FA_ERR_INVALID_ARG
+        assert "timeout_us" in fa.fa_last_error()
+
+
+def test_binding_checks_element_types(lib):
+    # the C entry points take raw pointers, so the binding checks dtypes before anything else
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.float32)
+    with pytest.raises(ValueError, match="bfloat16"):
+        fa.fa_prefill(q, q, q)
+    qb = q.to(torch.bfloat16)
+    with pytest.raises(ValueError, match="bfloat16"):
+        fa.fa_prefill_ex(qb, q, qb)
+    with pytest.raises(ValueError, match="int32"):
+        fa.fa_decode_paged(qb[0], qb, qb, torch.zeros(1, 1, dtype=torch.int64),
+                           torch.zeros(1, dtype=torch.int32), 8)
+    with pytest.raises(ValueError, match="float32"):
+        fa.fa_merge_states(torch.zeros(1, 1, 4, dtype=torch.bfloat16), torch.zeros(1, 1), None)

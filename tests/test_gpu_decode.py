@@ -10,6 +10,7 @@ import oracle
 import softmax_attention_gb300 as fa
 import workloads
 from tests._parity import check
+from tests._guard import Guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -29,8 +30,11 @@ def _run(c: workloads.PagedCase, rows=None):
     q, kp, vp, table, lens = workloads.paged_inputs(c)
     qd, kd, vd, td, ld = _gpu(q, kp, vp, table, lens)
     max_len = int(lens.max()) if c.B else 0
-    out, lse = fa.fa_decode_paged(qd, kd, vd, td, ld, max_len, c.sm_scale)
+    og, lg = Guarded(qd.shape, qd.dtype), Guarded(qd.shape[:-1], torch.float32)
+    out, lse = fa.fa_decode_paged(qd, kd, vd, td, ld, max_len, c.sm_scale, out=og.view, lse=lg.view)
     torch.cuda.synchronize()
+    og.assert_intact("decode out")
+    lg.assert_intact("decode lse")
     ro, rl = oracle.decode_paged(q, kp, vp, table, lens, scale=c.sm_scale, rows=rows)
     if rows is not None:
         idx = torch.as_tensor(rows, device="cuda")

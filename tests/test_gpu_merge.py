@@ -7,6 +7,7 @@ import torch
 import oracle
 import softmax_attention_gb300 as fa
 from tests._parity import check
+from tests._guard import Guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -26,6 +27,10 @@ def test_merge_parity(rows, S, D):
     if rows > 2:
         o2, l2 = oracle.merge(o[2:3, : int(n[2])], lse[2:3, : int(n[2])])
         ro[2], rl[2] = o2[0], l2[0]
-    out, lse_g = fa.fa_merge_states(o.cuda(), lse.cuda(), n.cuda(), out_dtype=torch.float32)
+    og, lg = Guarded((rows, D), torch.float32), Guarded((rows,), torch.float32)
+    out, lse_g = fa.fa_merge_states(o.cuda(), lse.cuda(), n.cuda(), out_dtype=torch.float32,
+                                    out=og.view, lse=lg.view)
     torch.cuda.synchronize()
+    og.assert_intact("merge out")
+    lg.assert_intact("merge lse")
     check(out, lse_g, ro, rl, max_err=1e-5, mean_err=1e-6, lse_err=1e-5, what="merge")

@@ -9,6 +9,7 @@ import oracle
 import softmax_attention_gb300 as fa
 import workloads
 from tests._parity import check
+from tests._guard import Guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -23,8 +24,11 @@ def _lib():
 def _run(c: workloads.MlaCase, rows=None):
     qn, qp, ckv, kpe, table, lens = workloads.mla_inputs(c)
     dev = [t.cuda() for t in (qn, qp, ckv, kpe, table, lens)]
-    out, lse = fa.mla_decode_paged(*dev, c.max_len, c.scale)
+    og, lg = Guarded(dev[0].shape, dev[0].dtype), Guarded(dev[0].shape[:-1], torch.float32)
+    out, lse = fa.mla_decode_paged(*dev, c.max_len, c.scale, out=og.view, lse=lg.view)
     torch.cuda.synchronize()
+    og.assert_intact("mla out")
+    lg.assert_intact("mla lse")
     ro, rl = oracle.mla_decode_paged(qn, qp, ckv, kpe, table, lens, scale=c.scale, rows=rows)
     if rows is not None:
         idx = torch.as_tensor(rows, device="cuda")

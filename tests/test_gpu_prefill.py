@@ -14,6 +14,7 @@ import oracle
 import softmax_attention_gb300 as fa
 import workloads
 from tests._parity import check
+from tests._guard import Guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -30,12 +31,16 @@ def _run(c: workloads.DenseCase, *, mask=None, num_splits=0, short_form=False, r
     dev = torch.device("cuda")
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     md = None if mask is None else mask.to(dev)
+    og, lg = Guarded(qd.shape, qd.dtype), Guarded(qd.shape[:-1], torch.float32)
     if short_form:
-        out, lse = fa.fa_prefill(qd, kd, vd, causal=c.causal, scale=c.sm_scale)
+        out, lse = fa.fa_prefill(qd, kd, vd, causal=c.causal, scale=c.sm_scale, out=og.view,
+                                 lse=lg.view)
     else:
         out, lse = fa.fa_prefill_ex(qd, kd, vd, causal=c.causal, scale=c.sm_scale, mask=md,
-                                    num_splits=num_splits)
+                                    num_splits=num_splits, out=og.view, lse=lg.view)
     torch.cuda.synchronize()
+    og.assert_intact("prefill out")
+    lg.assert_intact("prefill lse")
     ref_o, ref_l = oracle.attention(q, k, v, causal=c.causal, scale=c.sm_scale, mask=mask,
                                     rows=rows)
     if rows is not None:
