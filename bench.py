@@ -323,6 +323,38 @@ def bench_decode(fa, c, steps, warmup, flush, dist, pk):
     return res
 
 
+MLA_GRID = ((128, 2048), (768, 1024), (64, 1024), (64, 2048), (128, 1024), (768, 2048))
+
+
+def bench_prefill_paged(fa, c, steps, warmup, flush, dist, pk):
+    """Chunked prefill against a paged cache: TFLOP/s of the whole call (kernel, plus the
+    merge when the planner splits the KV loop) against the bf16 burst peak."""
+    dev = torch.device("cuda")
+    q, kp, vp, table, lens = workloads.paged_prefill_inputs(c)
+    qd, kd, vd, td, ld = (t.to(dev) for t in (q, kp, vp, table, lens))
+    max_len = int(lens.max())
+    out = torch.empty_like(qd)
+    lse = torch.empty(c.B, c.Hq, c.Lq, dtype=torch.float32, device=dev)
+    nbytes = fa.fa_prefill_paged_workspace_size(c.B, c.Hq, c.Hkv, c.Lq, c.D, max_len)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+
+    def call():
+        fa.fa_prefill_paged(qd, kd, vd, td, ld, max_len, causal=c.causal, scale=c.sm_scale,
+                            out=out, lse=lse, workspace=ws)
+
+    ms, _, mode = time_graph(call, steps, warmup, flush, dist)
+    mean_ms = dist.max(statistics.mean(ms))
+    flops = workloads.paged_prefill_flops(c, lens.tolist())
+    tflops = flops / (mean_ms * 1e-3) / 1e12
+    res = {"value": round(tflops, 2), "unit": "TFLOP/s", "ms": round(mean_ms, 4),
+           "flops": flops, "seq_lens": lens.tolist(), "workspace_bytes": nbytes,
+           "launches_per_step": 1 + (nbytes > 0), "mode": mode,
+           "roofline": roofline("tensor", tflops, pk["bf16"], "TFLOP/s", None, pk)}
+    del qd, kd, vd, td, ld, out, lse, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 def mla_bytes(c: workloads.MlaCase) -> dict:
     T = sum(c.lens())
     kv = T * (c.Dc + c.Dr) * 2
@@ -372,7 +404,7 @@ def bench_mla(fa, c, steps, warmup, flush, dist, pk):
            # reads only
            "roofline": roofline("hbm", b["total" if direct else "kernel"] / (k_ms * 1e-3) / 1e9,
                                 pk["hbm"], "GB/s",
-                                profiled_traffic(f"mla_decode_b{c.B}.md", "mla"), pk),
+                                profiled_traffic(f"mla_decode_b{c.B}_s{c.seq_len}.md", "mla"), pk),
            "kernel_ms": round(k_ms, 4)}
     del qnd, qpd, cd, kd, td, ld, out, lse, ws, op, ol
     torch.cuda.empty_cache()
@@ -458,7 +490,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="CPU time budget of the --impl reference run (all steps)")
-    ap.add_argument("--only", choices=("decode", "mla", "mqa"), default=None,
+    ap.add_argument("--only", choices=("decode", "paged", "mla", "mqa"), default=None,
                     help="run the headline plus only this path (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -488,7 +520,12 @@ def main():
             if want("decode"):
                 pc = workloads.paged_gqa_decode(seed=1 + dist.rank)
                 paths["paged_gqa_decode"] = bench_decode(fa, pc, sub, args.warmup, flush, dist, pk)
-            for batch, seq in (((128, 2048), (768, 1024)) if want("mla") else ()):
+            if want("paged"):
+                ppc = workloads.paged_gqa_prefill(seed=1 + dist.rank)
+                paths["paged_gqa_prefill"] = bench_prefill_paged(fa, ppc, sub, args.warmup, flush,
+                                                                 dist, pk)
+            # the MLA grid of the flashinfer PR's results: batch {64, 128, 768} x {1024, 2048}
+            for batch, seq in (MLA_GRID if want("mla") else ()):
                 mc = workloads.mla_decode(batch, seq, seed=1 + dist.rank)
                 try:
                     paths[f"mla_decode_b{batch}_s{seq}"] = bench_mla(fa, mc, sub, args.warmup,

@@ -192,6 +192,31 @@ int mla_decode_paged_states(const void* q_nope, const void* q_pe, const void* ck
                             void* stream);
 
 /*
+ * Paged prefill (chunked prefill against a paged KV cache): the dense prefill above with
+ * each sequence's keys and values read through a page table, in the layout of the paged
+ * decode path.  Sequence b has kv_len_b = seq_lens[b] cached tokens, the query chunk
+ * included; its Lq queries are its last Lq positions, so with causal = 1 query i sees keys
+ * j <= kv_len_b - Lq + i (a query with no key gets out = 0 and lse = -inf).
+ *   q        [B, Hq, Lq, D] bf16              out [B, Hq, Lq, D] bf16, lse [B, Hq, Lq] fp32 or NULL
+ *   k_pages, v_pages [num_pages, Hkv, page_size, D] bf16
+ *   page_table [B, max_pages] int32, seq_lens [B] int32 (device memory)
+ *   page_size a power of two in [8, 128] (at most 64 when D = 256); Hq % Hkv == 0,
+ *   Hq / Hkv <= 128, D in {64, 128, 256}; max_seq_len >= every seq_lens[b] (it sizes the
+ *   KV split) and <= max_pages * page_size.
+ *   workspace: fa_prefill_paged_workspace_size(B, Hq, Hkv, Lq, D, max_seq_len) bytes,
+ *   256-byte aligned (none when that size is 0).
+ * A sequence length outside [0, max_pages * page_size] or a page id of a key inside the
+ * sequence outside [0, num_pages) sets FA_ERR_BOUNDS in the device status word; the kernel
+ * then reads page 0 instead.  Returns FA_OK or an fa_status code.
+ */
+int fa_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
+                     const int32_t* page_table, const int32_t* seq_lens, void* out, float* lse,
+                     int B, int Hq, int Hkv, int Lq, int D, int page_size, int max_pages,
+                     int num_pages, int max_seq_len, int causal, float scale, void* workspace,
+                     size_t workspace_bytes, void* stream);
+size_t fa_prefill_paged_workspace_size(int B, int Hq, int Hkv, int Lq, int D, int max_seq_len);
+
+/*
  * Merge of attention states over disjoint key sets (the split-KV combine):
  *   lse = ln sum_s e^{lse_s},   out = sum_s e^{lse_s - lse} o_s
  *   o_parts [rows, max_splits, D] fp32 (normalised partial outputs), lse_parts

@@ -13,6 +13,8 @@ silent):
   masked scores.
 * ``decode_paged``: the same with one query per sequence and keys gathered through a page
   table from a [num_pages, Hkv, page_size, D] cache.
+* ``prefill_paged``: ``attention`` per sequence, with the sequence's keys and values gathered
+  in order through its page table and its queries at its last Lq positions.
 * ``mla_decode_paged``: latent-form MLA, where ckv serves as K and V and q_pe . kpe is added
   to each score ("perf: FlashAttention-3 style MLA PageAttention", change list item 4).
 * ``merge``: combination of attention states over disjoint key sets.
@@ -169,6 +171,54 @@ def decode_paged(q, k_pages, v_pages, page_table, seq_lens, *, scale=None, rows=
     if r is None:
         return out.view(B, Hq, D), lse.view(B, Hq)
     return out, lse
+
+
+def prefill_paged(q, k_pages, v_pages, page_table, seq_lens, *, causal=True, scale=None,
+                  rows=None):
+    """Chunked prefill against a paged cache.  q [B,Hq,Lq,D]; k_pages/v_pages
+    [num_pages,Hkv,page_size,D]; page_table [B,max_pages]; seq_lens [B] (the chunk included).
+    For each sequence b the first seq_lens[b] cached tokens are gathered in page order into
+    dense [1,Hkv,seq_lens[b],D] keys and values and ``attention`` runs on them, so the Lq
+    queries sit at the sequence's last Lq positions.  Returns fp64 (out [B,Hq,Lq,D],
+    lse [B,Hq,Lq]) or per-row results for flat ids (b*Hq + h)*Lq + i in ``rows``."""
+    q, kp, vp = _cpu(q), _cpu(k_pages), _cpu(v_pages)
+    pt, sl = _cpu(page_table).to(torch.int64), _cpu(seq_lens).to(torch.int64)
+    B, Hq, Lq, D = q.shape
+    num_pages, Hkv, page_size, _ = kp.shape
+    per_b = Hq * Lq
+    outs, lses, where = [], [], []
+    sel = None if rows is None else torch.as_tensor(rows, dtype=torch.int64).reshape(-1)
+    for b in range(B):
+        n = int(sl[b])
+        n_pages = -(-n // page_size)
+        ids = pt[b, :n_pages]
+        if n_pages and (int(ids.min()) < 0 or int(ids.max()) >= num_pages):
+            raise ValueError("page id out of range")
+        # [n_pages, Hkv, page_size, D] -> [1, Hkv, n_pages * page_size, D], first n tokens
+        kb = kp[ids].permute(1, 0, 2, 3).reshape(1, Hkv, n_pages * page_size, D)[:, :, :n]
+        vb = vp[ids].permute(1, 0, 2, 3).reshape(1, Hkv, n_pages * page_size, D)[:, :, :n]
+        kb, vb = kb.contiguous(), vb.contiguous()
+        if sel is None:
+            o, l = attention(q[b:b + 1], kb, vb, causal=causal, scale=scale)
+            outs.append(o[0])
+            lses.append(l[0])
+        else:
+            pos = torch.nonzero((sel >= b * per_b) & (sel < (b + 1) * per_b)).reshape(-1)
+            if pos.numel():
+                o, l = attention(q[b:b + 1], kb, vb, causal=causal, scale=scale,
+                                 rows=(sel[pos] - b * per_b).tolist())
+                outs.append(o)
+                lses.append(l)
+                where.append(pos)
+    if sel is None:
+        return torch.stack(outs), torch.stack(lses)
+    o = torch.empty(sel.numel(), D, dtype=torch.float64)
+    l = torch.empty(sel.numel(), dtype=torch.float64)
+    if where:
+        idx = torch.cat(where)
+        o[idx] = torch.cat(outs)
+        l[idx] = torch.cat(lses)
+    return o, l
 
 
 def mla_decode_paged(q_nope, q_pe, ckv, kpe, page_table, seq_lens, *, scale, rows=None):

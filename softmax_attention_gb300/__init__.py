@@ -32,6 +32,7 @@ _DT = {torch.bfloat16: FA_BF16, torch.float16: FA_FP16, torch.float32: FA_FP32}
 # Every symbol include/fa.h declares.
 EXPORTS = (
     "fa_prefill", "fa_prefill_ex", "fa_prefill_workspace_size", "fa_prefill_num_splits",
+    "fa_prefill_paged", "fa_prefill_paged_workspace_size",
     "fa_decode_paged", "fa_decode_workspace_size", "fa_decode_chunk_tokens",
     "fa_decode_paged_noalloc",
     "fa_decode_paged_states", "mla_decode_paged", "mla_decode_workspace_size",
@@ -82,6 +83,10 @@ def load_library(path: str | None = None):
         lib.fa_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs)]
         lib.fa_prefill_num_splits.restype = _i
         lib.fa_prefill_num_splits.argtypes = [ctypes.POINTER(PrefillArgs)]
+        lib.fa_prefill_paged.restype = _i
+        lib.fa_prefill_paged.argtypes = [_vp] * 7 + [_i] * 10 + [_f, _vp, _sz, _vp]
+        lib.fa_prefill_paged_workspace_size.restype = _sz
+        lib.fa_prefill_paged_workspace_size.argtypes = [_i] * 6
         lib.fa_decode_paged.restype = _i
         lib.fa_decode_paged.argtypes = [_vp] * 7 + [_i] * 8 + [_f, _vp, _sz, _vp]
         lib.fa_decode_workspace_size.restype = _sz
@@ -229,6 +234,39 @@ def prefill_workspace_size(q, k, v, **kw) -> int:
 
 def prefill_num_splits(q, k, v, **kw) -> int:
     return load_library().fa_prefill_num_splits(ctypes.byref(prefill_args(q, k, v, **kw)))
+
+
+def fa_prefill_paged_workspace_size(B, Hq, Hkv, Lq, D, max_seq_len) -> int:
+    return load_library().fa_prefill_paged_workspace_size(B, Hq, Hkv, Lq, D, max_seq_len)
+
+
+def fa_prefill_paged(q, k_pages, v_pages, page_table, seq_lens, max_seq_len: int,
+                     causal: bool = True, scale: float | None = None, out=None, lse=None,
+                     workspace=None, stream=None):
+    """Chunked prefill against a paged cache.  q [B,Hq,Lq,D] bf16 (each sequence's last Lq
+    positions); pages [num_pages,Hkv,page_size,D] bf16; page_table [B,max_pages] int32;
+    seq_lens [B] int32 (device): each sequence's cached tokens, the chunk included."""
+    lib = load_library()
+    _need_dtype(torch.bfloat16, q, k_pages, v_pages, out)
+    _need_dtype(torch.int32, page_table, seq_lens)
+    _need_dtype(torch.float32, lse)
+    _need_cuda(q, k_pages, v_pages, page_table, seq_lens, out, lse)
+    B, Hq, Lq, D = q.shape
+    num_pages, Hkv, page_size, _ = k_pages.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, Hq, Lq, dtype=torch.float32, device=q.device)
+    ws = _workspace(lib.fa_prefill_paged_workspace_size(B, Hq, Hkv, Lq, D, max_seq_len), q.device,
+                    workspace)
+    _check(lib.fa_prefill_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                _ptr(seq_lens), _ptr(out), _ptr(lse), B, Hq, Hkv, Lq, D, page_size,
+                                page_table.shape[1], num_pages, int(max_seq_len), int(bool(causal)),
+                                float(scale), _ptr(ws), 0 if ws is None else ws.numel(),
+                                _stream(stream)))
+    return out, lse
 
 
 def fa_decode_workspace_size(B, Hq, D, max_seq_len) -> int:

@@ -15,7 +15,8 @@ enum class Dtype : int { BF16 = 0, FP16 = 1, FP32 = 2 };
 // Dense prefill
 // ---------------------------------------------------------------------------------------
 struct PrefillParams {
-  // q [B,Hq,Lq,D], k/v [B,Hkv,Lkv,D] in bf16 or fp16 (the kernel's operand type).
+  // q [B,Hq,Lq,D] in bf16 or fp16 (the kernel's operand type); k/v either dense
+  // [B,Hkv,Lkv,D] or, when page_table is set, pages [num_pages,Hkv,page_size,D].
   const void* q;
   const void* k;
   const void* v;
@@ -34,6 +35,11 @@ struct PrefillParams {
   float* lse_part;      // [rows, n_splits] fp32 (natural log)
   Dtype out_dtype;
   uint32_t* status;
+  // Paged K/V (nullptr: dense).  Sequence b holds kv_lens[b] keys in pages
+  // page_table[b * max_pages + i]; its Lq queries are its last Lq positions.
+  const int32_t* page_table;
+  const int32_t* kv_lens;
+  int page_size, max_pages, num_pages;
 };
 
 // Launch on `stream`; returns a CUDA error code (cudaSuccess on launch success).

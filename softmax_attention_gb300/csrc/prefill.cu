@@ -72,8 +72,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hk = blockIdx.y, b = blockIdx.z;
   const int q0 = qt * p.q_per_tile;
   const int q_last = min(p.Lq, q0 + p.q_per_tile) - 1;
+  // keys of this sequence: dense Lkv, or the sequence's length in the paged cache
+  int Lkv = p.Lkv;
+  if (p.page_table) {
+    Lkv = p.kv_lens[b];
+    if (Lkv < 0 || Lkv > p.max_pages * p.page_size) {
+      if (threadIdx.x == 0) record_error(p.status, kDevBounds);
+      Lkv = 0;
+    }
+  }
   int t_begin, t_end;
-  prefill::kv_range(p, q_last, BN, split, t_begin, t_end);
+  prefill::kv_range(p, q_last, BN, split, Lkv, t_begin, t_end);
   const int n = t_end - t_begin;
 
   if (threadIdx.x == 0) {
@@ -104,35 +113,86 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 4) {
     // ------------------------------- TMA producer ---------------------------------------
-    if (lane == 0 && n > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(bar_q, static_cast<uint32_t>(D * 2 * p.q_per_tile * p.G));
-      for (int kb = 0; kb < D / 64; ++kb)
-        tma_load_4d(sQ + kb * (kRows * 128), &tm_q, bar_q, kb * 64, q0, hk * p.G, b);
-      const int kv_row = b * p.Hkv + hk;
+    if (n > 0) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        mbar_arrive_expect_tx(bar_q, static_cast<uint32_t>(D * 2 * p.q_per_tile * p.G));
+        for (int kb = 0; kb < D / 64; ++kb)
+          tma_load_4d(sQ + kb * (kRows * 128), &tm_q, bar_q, kb * 64, q0, hk * p.G, b);
+      }
       int issued = 0, k_only = -1;  // k_only: a K load issued without its V
       // K and V slots are released separately: K_j once S_j is done, V_j once P_j V_j is.
-      for (int jj = 0; jj < n; ++jj) {
-        const int stage = jj % STAGES;
-        if (jj >= STAGES && !mbar_wait(bar_ke(stage), ((jj / STAGES) - 1) & 1, p.status)) break;
-        const int key0 = (t_begin + jj) * BN;
-        mbar_arrive_expect_tx(bar_k(stage), L::kKVBytes);
-        for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_3d(sK + stage * L::kKVBytes + kb * (BN * 128), &tm_k, bar_k(stage), kb * 64,
-                      key0, kv_row);
-        if (jj >= STAGES && !mbar_wait(bar_ve(stage), ((jj / STAGES) - 1) & 1, p.status)) {
-          k_only = jj;  // K_jj is in flight; let it land below
-          break;
+      if (!p.page_table) {
+        if (lane == 0) {
+          const int kv_row = b * p.Hkv + hk;
+          for (int jj = 0; jj < n; ++jj) {
+            const int stage = jj % STAGES;
+            if (jj >= STAGES && !mbar_wait(bar_ke(stage), ((jj / STAGES) - 1) & 1, p.status)) break;
+            const int key0 = (t_begin + jj) * BN;
+            mbar_arrive_expect_tx(bar_k(stage), L::kKVBytes);
+            for (int kb = 0; kb < D / 64; ++kb)
+              tma_load_3d(sK + stage * L::kKVBytes + kb * (BN * 128), &tm_k, bar_k(stage), kb * 64,
+                          key0, kv_row);
+            if (jj >= STAGES && !mbar_wait(bar_ve(stage), ((jj / STAGES) - 1) & 1, p.status)) {
+              k_only = jj;  // K_jj is in flight; let it land below
+              break;
+            }
+            mbar_arrive_expect_tx(bar_v(stage), L::kKVBytes);
+            for (int kb = 0; kb < D / 64; ++kb)
+              tma_load_3d(sV + stage * L::kKVBytes + kb * (BN * 128), &tm_v, bar_v(stage), kb * 64,
+                          key0, kv_row);
+            issued = jj + 1;
+          }
         }
-        mbar_arrive_expect_tx(bar_v(stage), L::kKVBytes);
-        for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_3d(sV + stage * L::kKVBytes + kb * (BN * 128), &tm_v, bar_v(stage), kb * 64,
-                      key0, kv_row);
-        issued = jj + 1;
+      } else {
+        // Paged: a KV tile is BN / page_size pages, one TMA box (page_size rows x 64 columns,
+        // 1024-byte aligned in shared memory since page_size >= 8) per page and column block.
+        // Lane i holds the page id of page i of a tile, loaded one tile ahead, and issues that
+        // page's boxes itself, so one warp instruction starts the copies of every page.
+        const int ps = p.page_size, tp = BN / ps;
+        const int32_t* table = p.page_table + static_cast<size_t>(b) * p.max_pages;
+        auto tile_page = [&](int jj) {
+          int id = 0;  // pages past the sequence's end read page 0; those keys are masked
+          if (lane < tp) {
+            const int lp = (t_begin + jj) * tp + lane;
+            const int v = lp < p.max_pages ? __ldg(table + lp) : -1;
+            if (v >= 0 && v < p.num_pages) {
+              id = v;
+            } else if (lp * ps < Lkv) {
+              record_error(p.status, kDevBounds);
+            }
+          }
+          return id;
+        };
+        auto load_pages = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar, int id) {
+          if (lane < tp)
+            for (int kb = 0; kb < D / 64; ++kb)
+              tma_load_4d(dst + kb * (BN * 128) + lane * ps * 128, map, bar, kb * 64, 0, hk, id);
+        };
+        int ids_next = tile_page(0);
+        for (int jj = 0; jj < n; ++jj) {
+          const int ids = ids_next;
+          if (jj + 1 < n) ids_next = tile_page(jj + 1);
+          const int stage = jj % STAGES;
+          bool okw = jj < STAGES || mbar_wait(bar_ke(stage), ((jj / STAGES) - 1) & 1, p.status);
+          if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
+          if (lane == 0) mbar_arrive_expect_tx(bar_k(stage), L::kKVBytes);
+          __syncwarp();
+          load_pages(sK + stage * L::kKVBytes, &tm_k, bar_k(stage), ids);
+          okw = jj < STAGES || mbar_wait(bar_ve(stage), ((jj / STAGES) - 1) & 1, p.status);
+          if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) {
+            k_only = jj;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(bar_v(stage), L::kKVBytes);
+          __syncwarp();
+          load_pages(sV + stage * L::kKVBytes, &tm_v, bar_v(stage), ids);
+          issued = jj + 1;
+        }
       }
-      if (issued < n) {
+      if (lane == 0 && issued < n) {
         // A wait ran out: let the copies already in flight land before the CTA exits.
         mbar_wait(bar_q, 0, nullptr);
         for (int jj = max(0, issued - STAGES); jj < issued; ++jj) {
@@ -192,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------- softmax + epilogue (row per thread) ----------------------
-    const prefill::Row row = prefill::make_row(p, b, hk, q0, threadIdx.x);
+    const prefill::Row row = prefill::make_row(p, b, hk, q0, threadIdx.x, Lkv);
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
@@ -218,6 +278,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       prefill::store_p<BN>(t_s, pk);
       tmem_st_wait();
+      const int key0 = (t_begin + jj) * BN;
+      if (p.page_table && key0 + BN > Lkv) {
+        // Rows past the sequence's end hold whatever the pool has there; P is 0 for them,
+        // but 0 times a non-finite V would still poison O, so clear them once V has landed.
+        const int stage = jj % STAGES;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_v(stage), (jj / STAGES) & 1, p.status));
+        if (!ok) break;
+        const int r0 = Lkv - key0;
+        uint8_t* vst = smem + L::kVOff + stage * L::kKVBytes;
+        for (int i = threadIdx.x; i < (BN - r0) * (D / 64) * 8; i += 128) {
+          const int blk = i / ((BN - r0) * 8), rem = i % ((BN - r0) * 8);
+          *reinterpret_cast<uint4*>(vst + blk * (BN * 128) + (r0 + rem / 8) * 128 + (rem % 8) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
       tc_fence_before();
       mbar_arrive(bar_p);
     }
@@ -249,7 +325,17 @@ cudaError_t launch_impl(const PrefillParams& p, cudaStream_t stream) {
     if (!encode_tiled(&tq, dt, 4, p.q, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  {
+  if (p.page_table) {
+    // pages [num_pages, Hkv, page_size, D]; one box = one page's rows of one kv head
+    if (p.page_size < 8 || BN % p.page_size != 0) return cudaErrorInvalidValue;
+    const uint64_t ps = (uint64_t)p.page_size;
+    const uint64_t dims[4] = {(uint64_t)D, ps, (uint64_t)p.Hkv, (uint64_t)p.num_pages};
+    const uint64_t str[3] = {(uint64_t)D * 2, ps * D * 2, (uint64_t)p.Hkv * ps * D * 2};
+    const uint32_t box[4] = {64, (uint32_t)p.page_size, 1, 1};
+    if (!encode_tiled(&tk, dt, 4, p.k, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled(&tv, dt, 4, p.v, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  } else {
     const uint64_t dims[3] = {(uint64_t)D, lkv, (uint64_t)p.Hkv * p.B};
     const uint64_t str[2] = {(uint64_t)D * 2, lkv * D * 2};
     const uint32_t box[3] = {64, (uint32_t)BN, 1};

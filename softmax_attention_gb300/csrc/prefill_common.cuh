@@ -24,14 +24,15 @@ struct Row {
   size_t flat;        // (b * Hq + h) * Lq + i
 };
 
-// Row r (0..127) of the tile whose first query is q0.  Rows are packed head-major:
-// r = g * q_per_tile + (i - q0), query head h = hk * G + g.
-__device__ __forceinline__ Row make_row(const PrefillParams& p, int b, int hk, int q0, int r) {
+// Row r (0..127) of the tile whose first query is q0, for a sequence of Lkv keys.  Rows are
+// packed head-major: r = g * q_per_tile + (i - q0), query head h = hk * G + g.
+__device__ __forceinline__ Row make_row(const PrefillParams& p, int b, int hk, int q0, int r,
+                                        int Lkv) {
   Row row;
   const int g = r / p.q_per_tile, i = q0 + r % p.q_per_tile;
   row.valid = (g < p.G) && (i < p.Lq);
   row.key_lim = 0;
-  if (row.valid) row.key_lim = p.causal ? min(p.Lkv, i + (p.Lkv - p.Lq) + 1) : p.Lkv;
+  if (row.valid) row.key_lim = p.causal ? min(Lkv, i + (Lkv - p.Lq) + 1) : Lkv;
   row.mask = nullptr;
   if (p.mask && row.valid) {
     const int mb = p.mask_batches == 1 ? 0 : b;
@@ -204,11 +205,12 @@ __device__ __forceinline__ void epilogue(const PrefillParams& p, const Row& row,
   }
 }
 
-// KV tiles [t_begin, t_end) of one split for a tile set whose last query is q_last.
+// KV tiles [t_begin, t_end) of one split for a tile set whose last query is q_last, in a
+// sequence of Lkv keys.
 __device__ __forceinline__ void kv_range(const PrefillParams& p, int q_last, int bn, int split,
-                                         int& t_begin, int& t_end) {
-  int kv_end = p.Lkv;
-  if (p.causal) kv_end = min(p.Lkv, q_last + (p.Lkv - p.Lq) + 1);
+                                         int Lkv, int& t_begin, int& t_end) {
+  int kv_end = Lkv;
+  if (p.causal) kv_end = min(Lkv, q_last + (Lkv - p.Lq) + 1);
   const int n_kv_tiles = kv_end > 0 ? (kv_end + bn - 1) / bn : 0;
   const int per_split = (n_kv_tiles + p.n_splits - 1) / p.n_splits;
   t_begin = min(n_kv_tiles, split * per_split);

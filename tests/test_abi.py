@@ -153,3 +153,24 @@ def test_binding_checks_element_types(lib):
                            torch.zeros(1, dtype=torch.int32), 8)
     with pytest.raises(ValueError, match="float32"):
         fa.fa_merge_states(torch.zeros(1, 1, 4, dtype=torch.bfloat16), torch.zeros(1, 1), None)
+
+
+def test_prefill_paged_rejects_bad_arguments(lib):
+    def call(ps=16, max_pages=4, num_pages=4, max_len=64, D=128, Hq=4, Hkv=2):
+        return lib.fa_prefill_paged(None, None, None, None, None, None, None, 1, Hq, Hkv, 8, D,
+                                    ps, max_pages, num_pages, max_len, 1, 0.1, None, 0, None)
+    assert call(ps=4) == fa.FA_ERR_UNSUPPORTED          # below 8 rows per page
+    assert call(ps=24) == fa.FA_ERR_UNSUPPORTED         # not a power of two
+    assert call(ps=256) == fa.FA_ERR_UNSUPPORTED        # wider than a key tile
+    assert call(ps=128, D=256) == fa.FA_ERR_UNSUPPORTED  # D = 256 tiles are 64 keys
+    assert call(max_len=65) == fa.FA_ERR_INVALID_ARG    # more than max_pages * page_size
+    assert call(Hq=3) == fa.FA_ERR_INVALID_ARG
+    assert call() == fa.FA_ERR_INVALID_ARG              # null pointers
+    assert "fa_prefill_paged" in fa.fa_last_error()
+
+
+def test_prefill_paged_workspace_follows_the_dense_plan(lib):
+    # one 128-row tile per kv head and long keys: the planner splits, so a workspace exists
+    assert lib.fa_prefill_paged_workspace_size(1, 8, 1, 16, 128, 16384) > 0
+    assert lib.fa_prefill_paged_workspace_size(0, 8, 1, 16, 128, 16384) == 0
+    assert lib.fa_prefill_paged_workspace_size(1, 8, 1, 16, 128, 0) == 0

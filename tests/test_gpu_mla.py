@@ -52,8 +52,10 @@ def test_parity_shapes(lens, ps):
     check(out, lse, ro, rl, what=f"mla {lens} ps={ps}")
 
 
-@pytest.mark.parametrize("batch,seq", [(128, 2048), (768, 1024)])
+@pytest.mark.parametrize("batch,seq", [(128, 2048), (768, 1024), (64, 1024), (64, 2048),
+                                       (128, 1024), (768, 2048)])
 def test_mla_full_size_sampled(batch, seq):
+    """The MLA grid of the flashinfer PR's results section, on sampled (sequence, head) rows."""
     c = workloads.mla_decode(batch, seq)
     rows = list(range(0, c.B * c.H, 97 if batch == 768 else 41))
     out, lse, ro, rl = _run(c, rows=rows)

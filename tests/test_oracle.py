@@ -330,3 +330,58 @@ def test_merge_of_partition_equals_whole():
     o, l = oracle.merge(torch.stack(parts_o, 1), torch.stack(parts_l, 1))
     torch.testing.assert_close(o, whole_o.reshape(-1, 8), rtol=0, atol=1e-12)
     torch.testing.assert_close(l, whole_l.reshape(-1), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------------------
+# Paged prefill: each sequence's chunk attends to its gathered cache
+# ---------------------------------------------------------------------------------------
+def _paged_prefill_case(**kw):
+    args = dict(B=4, Hq=6, Hkv=2, Lq=5, D=16, page_size=4, num_pages=40, min_len=0, max_len=23,
+                dtype=torch.float64, seed=21, seq_lens=[23, 5, 3, 0])
+    args.update(kw)
+    c = workloads.PagedPrefillCase(**args)
+    return c, workloads.paged_prefill_inputs(c)
+
+
+def test_prefill_paged_equals_dense_attention_on_the_gathered_cache():
+    c, (q, kp, vp, table, lens) = _paged_prefill_case()
+    for causal in (True, False):
+        out, lse = oracle.prefill_paged(q, kp, vp, table, lens, causal=causal, scale=0.4)
+        for b in range(c.B):
+            n = int(lens[b])
+            kd = _dense_from_pages(kp, table, n, b).unsqueeze(0)
+            vd = _dense_from_pages(vp, table, n, b).unsqueeze(0)
+            o2, l2 = oracle.attention(q[b:b + 1], kd, vd, causal=causal, scale=0.4)
+            torch.testing.assert_close(out[b], o2[0], rtol=0, atol=1e-12)
+            torch.testing.assert_close(lse[b], l2[0], rtol=0, atol=1e-12)
+
+
+def test_prefill_paged_single_query_equals_paged_decode():
+    # one query per sequence sits at the sequence's last position: the decode definition,
+    # computed by the oracle's separate C routine that walks the page table itself
+    c, (q, kp, vp, table, lens) = _paged_prefill_case(Lq=1, seq_lens=[23, 5, 3, 1])
+    out, lse = oracle.prefill_paged(q, kp, vp, table, lens, causal=True, scale=0.4)
+    o2, l2 = oracle.decode_paged(q[:, :, 0], kp, vp, table, lens, scale=0.4)
+    torch.testing.assert_close(out[:, :, 0], o2, rtol=0, atol=1e-12)
+    torch.testing.assert_close(lse[:, :, 0], l2, rtol=0, atol=1e-12)
+
+
+def test_prefill_paged_is_invariant_to_page_placement():
+    c, (q, kp, vp, table, lens) = _paged_prefill_case()
+    out, lse = oracle.prefill_paged(q, kp, vp, table, lens, causal=True)
+    perm = torch.randperm(c.num_pages, generator=torch.Generator().manual_seed(5))
+    inv = torch.argsort(perm)
+    kp2, vp2 = kp[perm], vp[perm]          # page p of the new pool is old page perm[p]
+    t2 = torch.where(table >= 0, inv[table.clamp(min=0).long()].to(torch.int32), table)
+    out2, lse2 = oracle.prefill_paged(q, kp2, vp2, t2, lens, causal=True)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def test_prefill_paged_rows_without_keys_are_empty():
+    # sequence lengths 3 and 0 with Lq = 5: causally the first 2 (resp. all 5) queries of
+    # those sequences have no key
+    c, (q, kp, vp, table, lens) = _paged_prefill_case()
+    out, lse = oracle.prefill_paged(q, kp, vp, table, lens, causal=True)
+    assert torch.all(lse[2, :, :2] == -math.inf) and torch.all(out[2, :, :2] == 0)
+    assert torch.isfinite(lse[2, :, 2:]).all()
+    assert torch.all(lse[3] == -math.inf) and torch.all(out[3] == 0)

@@ -147,6 +147,58 @@ def paged_inputs(c: PagedCase):
 
 
 # ----------------------------------------------------------------------------------------
+# Paged prefill inputs (a query chunk at the end of each sequence's cached context)
+# ----------------------------------------------------------------------------------------
+@dataclass
+class PagedPrefillCase:
+    B: int
+    Hq: int
+    Hkv: int
+    Lq: int
+    D: int
+    page_size: int
+    num_pages: int
+    min_len: int
+    max_len: int
+    causal: bool = True
+    dtype: torch.dtype = torch.bfloat16
+    sigma: float = 0.5
+    seed: int = 1
+    seq_lens: list | None = None  # explicit lengths (chunk included) override min/max
+
+    @property
+    def max_pages(self) -> int:
+        return max(1, -(-self.max_len // self.page_size))
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+
+def paged_prefill_inputs(c: PagedPrefillCase):
+    """q [B,Hq,Lq,D]; k_pages, v_pages [num_pages,Hkv,page_size,D]; page_table
+    [B,max_pages] int32 (unused slots = -1); seq_lens [B] int32 (the chunk included).
+    Pages come from one seeded permutation of the pool, as in paged_inputs."""
+    dc = PagedCase(B=c.B, Hq=c.Hq, Hkv=c.Hkv, D=c.D, page_size=c.page_size,
+                   num_pages=c.num_pages, min_len=c.min_len, max_len=c.max_len, dtype=c.dtype,
+                   sigma=c.sigma, seed=c.seed, seq_lens=c.seq_lens)
+    _, kp, vp, table, lens = paged_inputs(dc)
+    g = _gen(c.seed + 7919)
+    q = normal((c.B, c.Hq, c.Lq, c.D), c.sigma, c.dtype, g)
+    return q, kp, vp, table, lens
+
+
+def paged_prefill_flops(c: PagedPrefillCase, lens) -> float:
+    """Algorithmic FLOPs (4 * D per visible (query, key) pair per query head)."""
+    total = 0
+    for n in (int(x) for x in lens):
+        for i in range(c.Lq):
+            pos = n - c.Lq + i
+            total += max(0, min(n, pos + 1)) if c.causal else n
+    return 4.0 * c.D * c.Hq * total
+
+
+# ----------------------------------------------------------------------------------------
 # MLA paged decode inputs
 # ----------------------------------------------------------------------------------------
 @dataclass
@@ -226,6 +278,14 @@ def mla_decode(batch: int = 128, seq_len: int = 2048, seed: int = 1) -> MlaCase:
 
 
 MQA_SWEEP_LQ = (16, 64, 256, 1024, 4096, 16384)
+
+
+def paged_gqa_prefill(seed: int = 1) -> PagedPrefillCase:
+    """Chunked prefill against a paged cache, Llama-8B-like heads: 8 sequences, Hq=32,
+    Hkv=8, D=128, a 512-query chunk at the end of each sequence's context of U{2048..8192}
+    tokens (chunk included), page_size 16, causal, bf16 N(0,1)*0.5, scale 1/sqrt(128)."""
+    return PagedPrefillCase(B=8, Hq=32, Hkv=8, Lq=512, D=128, page_size=16, num_pages=6000,
+                            min_len=2048, max_len=8192, seed=seed)
 
 
 def mqa_prefill(Lq: int, seed: int = 1) -> DenseCase:
