@@ -80,6 +80,15 @@ typedef struct fa_prefill_args {
   int num_splits;        /* 0: the library picks; >= 1: split the KV loop this many ways */
   void* workspace;       /* device scratch, >= fa_prefill_workspace_size(args) bytes */
   size_t workspace_bytes;
+  /* Paged K/V (page_size = 0: dense k and v as above).  With page_size > 0, k and v are
+     pages [num_pages, Hkv, page_size, D]; key t of sequence b is slot t % page_size of page
+     page_table[b, t / page_size]; sequence b holds seq_lens[b] keys (device memory) and its
+     Lq queries are its last Lq positions.  Lkv is then the largest seq_lens[b]: it sizes the
+     KV split and is the last dimension of the mask.  dtype FA_BF16 or FA_FP16; page_size a
+     power of two in [8, 128] (at most 64 when D = 256); Lkv <= max_pages * page_size. */
+  const int32_t* page_table; /* [B, max_pages] int32 */
+  const int32_t* seq_lens;   /* [B] int32 */
+  int page_size, max_pages, num_pages;
 } fa_prefill_args;
 
 int fa_prefill_ex(const fa_prefill_args* args, void* stream);
@@ -192,11 +201,12 @@ int mla_decode_paged_states(const void* q_nope, const void* q_pe, const void* ck
                             void* stream);
 
 /*
- * Paged prefill (chunked prefill against a paged KV cache): the dense prefill above with
- * each sequence's keys and values read through a page table, in the layout of the paged
- * decode path.  Sequence b has kv_len_b = seq_lens[b] cached tokens, the query chunk
- * included; its Lq queries are its last Lq positions, so with causal = 1 query i sees keys
- * j <= kv_len_b - Lq + i (a query with no key gets out = 0 and lse = -inf).
+ * Paged prefill (chunked prefill against a paged KV cache), bf16 short form of
+ * fa_prefill_ex with page_size > 0: each sequence's keys and values are read through a page
+ * table, in the layout of the paged decode path.  Sequence b has kv_len_b = seq_lens[b]
+ * cached tokens, the query chunk included; its Lq queries are its last Lq positions, so
+ * with causal = 1 query i sees keys j <= kv_len_b - Lq + i (a query with no key gets
+ * out = 0 and lse = -inf).
  *   q        [B, Hq, Lq, D] bf16              out [B, Hq, Lq, D] bf16, lse [B, Hq, Lq] fp32 or NULL
  *   k_pages, v_pages [num_pages, Hkv, page_size, D] bf16
  *   page_table [B, max_pages] int32, seq_lens [B] int32 (device memory)

@@ -174,18 +174,23 @@ def decode_paged(q, k_pages, v_pages, page_table, seq_lens, *, scale=None, rows=
 
 
 def prefill_paged(q, k_pages, v_pages, page_table, seq_lens, *, causal=True, scale=None,
-                  rows=None):
+                  mask=None, rows=None):
     """Chunked prefill against a paged cache.  q [B,Hq,Lq,D]; k_pages/v_pages
-    [num_pages,Hkv,page_size,D]; page_table [B,max_pages]; seq_lens [B] (the chunk included).
-    For each sequence b the first seq_lens[b] cached tokens are gathered in page order into
-    dense [1,Hkv,seq_lens[b],D] keys and values and ``attention`` runs on them, so the Lq
-    queries sit at the sequence's last Lq positions.  Returns fp64 (out [B,Hq,Lq,D],
+    [num_pages,Hkv,page_size,D]; page_table [B,max_pages]; seq_lens [B] (the chunk included);
+    optional additive mask [1 or B, Lq, >= max seq_lens].  For each sequence b the first
+    seq_lens[b] cached tokens are gathered in page order into dense [1,Hkv,seq_lens[b],D]
+    keys and values and ``attention`` runs on them (with the mask's first seq_lens[b]
+    columns), so the Lq queries sit at the sequence's last Lq positions.  Returns fp64 (out [B,Hq,Lq,D],
     lse [B,Hq,Lq]) or per-row results for flat ids (b*Hq + h)*Lq + i in ``rows``."""
     q, kp, vp = _cpu(q), _cpu(k_pages), _cpu(v_pages)
     pt, sl = _cpu(page_table).to(torch.int64), _cpu(seq_lens).to(torch.int64)
     B, Hq, Lq, D = q.shape
     num_pages, Hkv, page_size, _ = kp.shape
     per_b = Hq * Lq
+    if mask is not None:
+        mask = _cpu(mask)
+        if mask.dim() == 2:
+            mask = mask.unsqueeze(0)
     outs, lses, where = [], [], []
     sel = None if rows is None else torch.as_tensor(rows, dtype=torch.int64).reshape(-1)
     for b in range(B):
@@ -198,14 +203,17 @@ def prefill_paged(q, k_pages, v_pages, page_table, seq_lens, *, causal=True, sca
         kb = kp[ids].permute(1, 0, 2, 3).reshape(1, Hkv, n_pages * page_size, D)[:, :, :n]
         vb = vp[ids].permute(1, 0, 2, 3).reshape(1, Hkv, n_pages * page_size, D)[:, :, :n]
         kb, vb = kb.contiguous(), vb.contiguous()
+        mb = None
+        if mask is not None:
+            mb = mask[0 if mask.shape[0] == 1 else b, :, :n].unsqueeze(0).contiguous()
         if sel is None:
-            o, l = attention(q[b:b + 1], kb, vb, causal=causal, scale=scale)
+            o, l = attention(q[b:b + 1], kb, vb, causal=causal, scale=scale, mask=mb)
             outs.append(o[0])
             lses.append(l[0])
         else:
             pos = torch.nonzero((sel >= b * per_b) & (sel < (b + 1) * per_b)).reshape(-1)
             if pos.numel():
-                o, l = attention(q[b:b + 1], kb, vb, causal=causal, scale=scale,
+                o, l = attention(q[b:b + 1], kb, vb, causal=causal, scale=scale, mask=mb,
                                  rows=(sel[pos] - b * per_b).tolist())
                 outs.append(o)
                 lses.append(l)

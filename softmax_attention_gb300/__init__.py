@@ -57,6 +57,8 @@ class PrefillArgs(ctypes.Structure):
         ("mask_dtype", ctypes.c_int), ("mask_batches", ctypes.c_int),
         ("num_splits", ctypes.c_int), ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
+        ("page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+        ("page_size", ctypes.c_int), ("max_pages", ctypes.c_int), ("num_pages", ctypes.c_int),
     ]
 
 
@@ -179,10 +181,21 @@ def fa_prefill(q, k, v, causal: bool = False, scale: float | None = None, out=No
 
 
 def prefill_args(q, k, v, *, causal=False, scale=None, out=None, lse=None, mask=None,
-                 num_splits=0, workspace=None) -> PrefillArgs:
+                 num_splits=0, workspace=None, page_table=None, seq_lens=None,
+                 max_seq_len=None) -> PrefillArgs:
+    """Argument struct of fa_prefill_ex.  Dense: k, v [B,Hkv,Lkv,D].  Paged (page_table
+    given): k, v are pages [num_pages,Hkv,page_size,D] and Lkv = max_seq_len."""
     B, Hq, Lq, D = q.shape
-    Hkv, Lkv = k.shape[1], k.shape[2]
+    if page_table is None:
+        Hkv, Lkv = k.shape[1], k.shape[2]
+    else:
+        Hkv, Lkv = k.shape[1], int(max_seq_len)
     a = PrefillArgs()
+    if page_table is not None:
+        a.page_table = page_table.data_ptr()
+        a.seq_lens = seq_lens.data_ptr()
+        a.num_pages, a.page_size = k.shape[0], k.shape[2]
+        a.max_pages = page_table.shape[1]
     a.q, a.k, a.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
     a.out = out.data_ptr() if out is not None else None
     a.lse = lse.data_ptr() if lse is not None else None
@@ -241,31 +254,33 @@ def fa_prefill_paged_workspace_size(B, Hq, Hkv, Lq, D, max_seq_len) -> int:
 
 
 def fa_prefill_paged(q, k_pages, v_pages, page_table, seq_lens, max_seq_len: int,
-                     causal: bool = True, scale: float | None = None, out=None, lse=None,
-                     workspace=None, stream=None):
-    """Chunked prefill against a paged cache.  q [B,Hq,Lq,D] bf16 (each sequence's last Lq
-    positions); pages [num_pages,Hkv,page_size,D] bf16; page_table [B,max_pages] int32;
-    seq_lens [B] int32 (device): each sequence's cached tokens, the chunk included."""
+                     causal: bool = True, scale: float | None = None, mask=None, num_splits=0,
+                     out=None, lse=None, workspace=None, stream=None):
+    """Chunked prefill against a paged cache (fa_prefill_ex with a page table).
+    q [B,Hq,Lq,D] bf16 or fp16 (each sequence's last Lq positions); pages
+    [num_pages,Hkv,page_size,D] in q's dtype; page_table [B,max_pages] int32; seq_lens [B]
+    int32 (device): each sequence's cached tokens, the chunk included; optional additive
+    mask [1 or B, Lq, max_seq_len]."""
     lib = load_library()
-    _need_dtype(torch.bfloat16, q, k_pages, v_pages, out)
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError(f"expected bfloat16 or float16, got {q.dtype}")
+    _need_dtype(q.dtype, k_pages, v_pages, out)
     _need_dtype(torch.int32, page_table, seq_lens)
     _need_dtype(torch.float32, lse)
-    _need_cuda(q, k_pages, v_pages, page_table, seq_lens, out, lse)
+    _need_cuda(q, k_pages, v_pages, page_table, seq_lens, mask, out, lse)
     B, Hq, Lq, D = q.shape
-    num_pages, Hkv, page_size, _ = k_pages.shape
-    if scale is None:
-        scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty(B, Hq, Lq, dtype=torch.float32, device=q.device)
-    ws = _workspace(lib.fa_prefill_paged_workspace_size(B, Hq, Hkv, Lq, D, max_seq_len), q.device,
-                    workspace)
-    _check(lib.fa_prefill_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
-                                _ptr(seq_lens), _ptr(out), _ptr(lse), B, Hq, Hkv, Lq, D, page_size,
-                                page_table.shape[1], num_pages, int(max_seq_len), int(bool(causal)),
-                                float(scale), _ptr(ws), 0 if ws is None else ws.numel(),
-                                _stream(stream)))
+    a = prefill_args(q, k_pages, v_pages, causal=causal, scale=scale, out=out, lse=lse,
+                     mask=mask, num_splits=num_splits, page_table=page_table,
+                     seq_lens=seq_lens, max_seq_len=max_seq_len)
+    ws = _workspace(lib.fa_prefill_workspace_size(ctypes.byref(a)), q.device, workspace)
+    if ws is not None:
+        a.workspace = ws.data_ptr()
+        a.workspace_bytes = ws.numel() * ws.element_size()
+    _check(lib.fa_prefill_ex(ctypes.byref(a), _stream(stream)))
     return out, lse
 
 

@@ -166,8 +166,25 @@ int validate_prefill(const fa_prefill_args* a, bool check_pointers = true) {
   }
   if (work && a->num_splits < 0)
     return fail(FA_ERR_INVALID_ARG, "fa_prefill: num_splits must be >= 0");
+  if (a->page_size < 0) return fail(FA_ERR_INVALID_ARG, "fa_prefill: page_size must be >= 0");
+  if (a->page_size > 0) {
+    const int bn = prefill_block_n(a->D);
+    if (a->page_size < 8 || a->page_size > bn || (a->page_size & (a->page_size - 1)) != 0)
+      return fail(FA_ERR_UNSUPPORTED,
+                  "fa_prefill: page_size must be a power of two in [8, %d] (got %d)", bn,
+                  a->page_size);
+    if (a->dtype == FA_FP32)
+      return fail(FA_ERR_UNSUPPORTED, "fa_prefill: paged K/V must be bf16 or fp16");
+    if (work && (a->max_pages <= 0 || a->num_pages <= 0))
+      return fail(FA_ERR_INVALID_ARG, "fa_prefill: max_pages and num_pages must be > 0");
+    if ((long)a->Lkv > (long)a->max_pages * a->page_size)
+      return fail(FA_ERR_INVALID_ARG, "fa_prefill: Lkv %d exceeds max_pages * page_size",
+                  a->Lkv);
+    if (work && check_pointers && (!a->page_table || !a->seq_lens))
+      return fail(FA_ERR_INVALID_ARG, "fa_prefill: null page_table or seq_lens");
+  }
   if (work && check_pointers) {
-    if (!a->q || !a->out || (a->Lkv > 0 && (!a->k || !a->v)))
+    if (!a->q || !a->out || ((a->Lkv > 0 || a->page_size > 0) && (!a->k || !a->v)))
       return fail(FA_ERR_INVALID_ARG, "fa_prefill: null q/k/v/out pointer");
     if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->out))
       return fail(FA_ERR_INVALID_ARG, "fa_prefill: q, k, v and out must be 16-byte aligned");
@@ -255,9 +272,16 @@ int run_prefill(const fa_prefill_args* a, cudaStream_t stream) {
     p.v = ws + pl.off_v;
     operand = Dtype::FP16;
   }
-  if (a->Lkv == 0) {  // keep the tensor maps valid; the kernel reads no key
+  if (a->Lkv == 0 && a->page_size == 0) {  // keep the tensor maps valid; no key is read
     p.k = p.q;
     p.v = p.q;
+  }
+  if (a->page_size > 0) {
+    p.page_table = a->page_table;
+    p.kv_lens = a->seq_lens;
+    p.page_size = a->page_size;
+    p.max_pages = a->max_pages;
+    p.num_pages = a->num_pages;
   }
   p.out = a->out;
   p.lse = a->lse;
@@ -324,139 +348,6 @@ size_t split_ws_bytes(long rows, int n_chunks, int D) {
 
 using namespace fa;
 
-// ---------------------------------------------------------------------------------------
-// Paged prefill: the dense prefill kernel with K/V read through a page table
-// ---------------------------------------------------------------------------------------
-namespace {
-
-struct PagedPrefill {
-  const void* q;
-  const void* k_pages;
-  const void* v_pages;
-  const int32_t* page_table;
-  const int32_t* seq_lens;
-  void* out;
-  float* lse;
-  int B, Hq, Hkv, Lq, D, page_size, max_pages, num_pages, max_seq_len, causal;
-  float scale;
-  void* workspace;
-  size_t workspace_bytes;
-};
-
-// The dense plan with max_seq_len keys: tiles, split count and partial-state workspace.
-fa_prefill_args paged_plan_args(const PagedPrefill& a) {
-  fa_prefill_args d;
-  memset(&d, 0, sizeof d);
-  d.B = a.B;
-  d.Hq = a.Hq;
-  d.Hkv = a.Hkv;
-  d.Lq = a.Lq;
-  d.Lkv = a.max_seq_len;
-  d.D = a.D;
-  d.causal = a.causal;
-  d.scale = a.scale;
-  d.dtype = FA_BF16;
-  return d;
-}
-
-int validate_prefill_paged(const PagedPrefill& a, bool check_pointers) {
-  if (a.B < 0 || a.Lq < 0 || a.max_seq_len < 0)
-    return fail(FA_ERR_INVALID_ARG, "fa_prefill_paged: B, Lq, max_seq_len must be >= 0");
-  if (a.Hq <= 0 || a.Hkv <= 0 || a.Hq % a.Hkv != 0)
-    return fail(FA_ERR_INVALID_ARG, "fa_prefill_paged: need Hq, Hkv > 0 and Hq %% Hkv == 0");
-  if (a.Hq / a.Hkv > 128)
-    return fail(FA_ERR_UNSUPPORTED, "fa_prefill_paged: query heads per kv head must be <= 128");
-  if (a.D != 64 && a.D != 128 && a.D != 256)
-    return fail(FA_ERR_UNSUPPORTED, "fa_prefill_paged: D must be 64, 128 or 256 (got %d)", a.D);
-  if (a.Hkv > 65535 || a.B > 65535)
-    return fail(FA_ERR_UNSUPPORTED, "fa_prefill_paged: B and Hkv must be <= 65535");
-  if (!(a.scale == a.scale) || isinf(a.scale))
-    return fail(FA_ERR_INVALID_ARG, "fa_prefill_paged: scale must be finite");
-  const int bn = prefill_block_n(a.D);
-  if (a.page_size < 8 || a.page_size > bn || (a.page_size & (a.page_size - 1)) != 0)
-    return fail(FA_ERR_UNSUPPORTED,
-                "fa_prefill_paged: page_size must be a power of two in [8, %d] (got %d)", bn,
-                a.page_size);
-  const bool work = a.B > 0 && a.Lq > 0;
-  if (!work) return FA_OK;
-  if (a.max_pages <= 0 || a.num_pages <= 0)
-    return fail(FA_ERR_INVALID_ARG, "fa_prefill_paged: max_pages and num_pages must be > 0");
-  if ((long)a.max_seq_len > (long)a.max_pages * a.page_size)
-    return fail(FA_ERR_INVALID_ARG,
-                "fa_prefill_paged: max_seq_len %d exceeds max_pages * page_size", a.max_seq_len);
-  if (check_pointers) {
-    if (!a.q || !a.k_pages || !a.v_pages || !a.page_table || !a.seq_lens || !a.out)
-      return fail(FA_ERR_INVALID_ARG, "fa_prefill_paged: null pointer argument");
-    if (!aligned16(a.q) || !aligned16(a.k_pages) || !aligned16(a.v_pages) || !aligned16(a.out))
-      return fail(FA_ERR_INVALID_ARG,
-                  "fa_prefill_paged: q, k_pages, v_pages and out must be 16-byte aligned");
-  }
-  return FA_OK;
-}
-
-int run_prefill_paged(const PagedPrefill& a, cudaStream_t stream) {
-  int rc = validate_prefill_paged(a, true);
-  if (rc != FA_OK) return rc;
-  if (a.B == 0 || a.Lq == 0) return FA_OK;
-  const fa_prefill_args d = paged_plan_args(a);
-  const PrefillPlan pl = plan_prefill(&d);
-  if (pl.total_bytes > 0) {
-    if (!a.workspace || a.workspace_bytes < pl.total_bytes)
-      return fail(FA_ERR_WORKSPACE, "fa_prefill_paged: workspace of %zu bytes needed (got %zu)",
-                  pl.total_bytes, a.workspace ? a.workspace_bytes : (size_t)0);
-    if ((reinterpret_cast<uintptr_t>(a.workspace) & 255u) != 0)
-      return fail(FA_ERR_INVALID_ARG, "fa_prefill_paged: workspace must be 256-byte aligned");
-  }
-  uint32_t* status = device_status_ptr();
-  if (!status) return fail(FA_ERR_CUDA, "fa_prefill_paged: no usable CUDA device");
-  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  PrefillParams p{};
-  p.q = a.q;
-  p.k = a.k_pages;
-  p.v = a.v_pages;
-  p.out = a.out;
-  p.lse = a.lse;
-  p.B = a.B;
-  p.Hq = a.Hq;
-  p.Hkv = a.Hkv;
-  p.G = pl.G;
-  p.Lq = a.Lq;
-  p.Lkv = a.max_seq_len;
-  p.D = a.D;
-  p.causal = a.causal ? 1 : 0;
-  p.scale_log2 = a.scale * 1.44269504088896340736f;
-  p.q_per_tile = pl.q_per_tile;
-  p.n_qtiles = pl.n_qtiles;
-  p.n_splits = pl.n_splits;
-  p.o_part = pl.n_splits > 1 ? reinterpret_cast<float*>(ws + pl.off_o) : nullptr;
-  p.lse_part = pl.n_splits > 1 ? reinterpret_cast<float*>(ws + pl.off_lse) : nullptr;
-  p.out_dtype = Dtype::BF16;
-  p.status = status;
-  p.page_table = a.page_table;
-  p.kv_lens = a.seq_lens;
-  p.page_size = a.page_size;
-  p.max_pages = a.max_pages;
-  p.num_pages = a.num_pages;
-  cudaError_t e = launch_prefill(p, Dtype::BF16, stream);
-  if (e != cudaSuccess) return cuda_fail("fa_prefill_paged (attention kernel)", e);
-  if (pl.n_splits > 1) {
-    MergeParams m{};
-    m.o_part = p.o_part;
-    m.lse_part = p.lse_part;
-    m.out = a.out;
-    m.lse = a.lse;
-    m.rows = a.B * a.Hq * a.Lq;
-    m.D = a.D;
-    m.max_splits = pl.n_splits;
-    m.out_dtype = Dtype::BF16;
-    e = launch_merge(m, stream);
-    if (e != cudaSuccess) return cuda_fail("fa_prefill_paged (merge kernel)", e);
-  }
-  return FA_OK;
-}
-
-}  // namespace
-
 extern "C" {
 
 int fa_prefill(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
@@ -502,28 +393,44 @@ int fa_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
                      int B, int Hq, int Hkv, int Lq, int D, int page_size, int max_pages,
                      int num_pages, int max_seq_len, int causal, float scale, void* workspace,
                      size_t workspace_bytes, void* stream) {
-  const PagedPrefill a{q, k_pages, v_pages, page_table, seq_lens, out, lse, B, Hq, Hkv, Lq, D,
-                       page_size, max_pages, num_pages, max_seq_len, causal, scale, workspace,
-                       workspace_bytes};
-  return run_prefill_paged(a, static_cast<cudaStream_t>(stream));
-}
-
-size_t fa_prefill_paged_workspace_size(int B, int Hq, int Hkv, int Lq, int D, int max_seq_len) {
-  PagedPrefill a{};
+  fa_prefill_args a;
+  memset(&a, 0, sizeof a);
+  a.q = q;
+  a.k = k_pages;
+  a.v = v_pages;
+  a.out = out;
+  a.lse = lse;
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.Lq = Lq;
+  a.Lkv = max_seq_len;
   a.D = D;
-  a.max_seq_len = max_seq_len;
-  a.page_size = 8;  // the plan does not depend on the page size
-  a.max_pages = max_seq_len > 0 ? (max_seq_len + 7) / 8 : 1;
-  a.num_pages = 1;
+  a.causal = causal;
+  a.scale = scale;
+  a.dtype = FA_BF16;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.page_table = page_table;
+  a.seq_lens = seq_lens;
+  a.page_size = page_size;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  return run_prefill(&a, static_cast<cudaStream_t>(stream));
+}
+
+size_t fa_prefill_paged_workspace_size(int B, int Hq, int Hkv, int Lq, int D, int max_seq_len) {
+  fa_prefill_args a;
+  memset(&a, 0, sizeof a);
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Lq = Lq;
+  a.Lkv = max_seq_len;
+  a.D = D;
   a.scale = 1.f;
-  if (validate_prefill_paged(a, false) != FA_OK) return 0;
-  if (a.B == 0 || a.Lq == 0) return 0;
-  const fa_prefill_args d = paged_plan_args(a);
-  return plan_prefill(&d).total_bytes;
+  a.dtype = FA_BF16;  // the plan depends on neither the page geometry nor the pointers
+  return fa_prefill_workspace_size(&a);
 }
 
 size_t fa_decode_workspace_size(int B, int Hq, int D, int max_seq_len) {
@@ -879,6 +786,6 @@ int fa_selftest_wait_timeout(unsigned timeout_us, void* stream) {
 
 const char* fa_last_error(void) { return g_err; }
 
-int fa_version(void) { return 100; }
+int fa_version(void) { return 200; }
 
 }  // extern "C"

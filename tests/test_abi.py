@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version(lib):
-    assert lib.fa_version() >= 100
+    assert lib.fa_version() == 200  # 0.2.0: fa_prefill_args gained the paging fields
 
 
 def _args(**kw):
@@ -166,7 +166,20 @@ def test_prefill_paged_rejects_bad_arguments(lib):
     assert call(max_len=65) == fa.FA_ERR_INVALID_ARG    # more than max_pages * page_size
     assert call(Hq=3) == fa.FA_ERR_INVALID_ARG
     assert call() == fa.FA_ERR_INVALID_ARG              # null pointers
-    assert "fa_prefill_paged" in fa.fa_last_error()
+    assert "null" in fa.fa_last_error()
+
+
+def test_prefill_ex_paged_mode_validation(lib):
+    # page_size > 0 switches fa_prefill_ex to paged K/V
+    a = _args(page_size=16, max_pages=4, num_pages=4, Lkv=64)
+    a.dtype = fa.FA_FP32
+    assert lib.fa_prefill_ex(ctypes.byref(a), None) == fa.FA_ERR_UNSUPPORTED
+    a = _args(page_size=16, max_pages=4, num_pages=4, Lkv=64)
+    assert lib.fa_prefill_ex(ctypes.byref(a), None) == fa.FA_ERR_INVALID_ARG  # no page table
+    a = _args(page_size=16, max_pages=4, num_pages=4, Lkv=65)
+    assert lib.fa_prefill_workspace_size(ctypes.byref(a)) == 0  # invalid: Lkv > 64 slots
+    a = _args(page_size=-1)
+    assert lib.fa_prefill_ex(ctypes.byref(a), None) == fa.FA_ERR_INVALID_ARG
 
 
 def test_prefill_paged_workspace_follows_the_dense_plan(lib):

@@ -103,3 +103,71 @@ def test_out_of_range_page_is_reported():
     fa.fa_prefill_paged(*(t.cuda() for t in (q, kp, vp, table, long)), 100, scale=c.sm_scale)
     assert fa.fa_get_device_status() == fa.FA_ERR_BOUNDS
     assert fa.fa_get_device_status() == fa.FA_OK
+
+
+def _inputs_on_gpu(c):
+    q, kp, vp, table, lens = workloads.paged_prefill_inputs(c)
+    return (q, kp, vp, table, lens), [t.cuda() for t in (q, kp, vp, table, lens)]
+
+
+def test_fp16():
+    c = workloads.PagedPrefillCase(B=2, Hq=8, Hkv=2, Lq=70, D=128, page_size=16, num_pages=120,
+                                   min_len=0, max_len=900, seq_lens=[900, 60],
+                                   dtype=torch.float16, seed=6)
+    (q, kp, vp, table, lens), dev = _inputs_on_gpu(c)
+    out, lse = fa.fa_prefill_paged(*dev, 900, scale=c.sm_scale)
+    torch.cuda.synchronize()
+    assert out.dtype == torch.float16
+    ro, rl = oracle.prefill_paged(q, kp, vp, table, lens, scale=c.sm_scale)
+    check(out, lse, ro, rl, what="paged prefill fp16")
+
+
+@pytest.mark.parametrize("mask_dtype,per_seq", [(torch.bfloat16, True), (torch.float32, False)])
+def test_additive_mask(mask_dtype, per_seq):
+    """A llama.cpp-style explicit mask [1 or B, Lq, max_len] (here non-causal with -inf
+    holes and finite biases), the paged counterpart of small-batch decode with a KQ mask."""
+    c = workloads.PagedPrefillCase(B=3, Hq=8, Hkv=4, Lq=6, D=64, page_size=8, num_pages=100,
+                                   min_len=0, max_len=500, seq_lens=[500, 37, 6], causal=False,
+                                   seed=8)
+    (q, kp, vp, table, lens), dev = _inputs_on_gpu(c)
+    g = torch.Generator().manual_seed(11)
+    mb = c.B if per_seq else 1
+    mask = (torch.randn(mb, c.Lq, c.max_len, generator=g) * 0.5).to(mask_dtype)
+    mask[:, :, 5::7] = -float("inf")
+    out, lse = fa.fa_prefill_paged(*dev, c.max_len, causal=False, scale=c.sm_scale,
+                                   mask=mask.cuda())
+    torch.cuda.synchronize()
+    ro, rl = oracle.prefill_paged(q, kp, vp, table, lens, causal=False, scale=c.sm_scale,
+                                  mask=mask)
+    check(out, lse, ro, rl, what=f"paged prefill mask {mask_dtype} per_seq={per_seq}")
+
+
+@pytest.mark.parametrize("splits", [2, 5])
+def test_forced_splits(splits):
+    c = workloads.PagedPrefillCase(B=2, Hq=8, Hkv=2, Lq=40, D=128, page_size=32, num_pages=90,
+                                   min_len=0, max_len=1200, seq_lens=[1200, 300], seed=9)
+    (q, kp, vp, table, lens), dev = _inputs_on_gpu(c)
+    out, lse = fa.fa_prefill_paged(*dev, 1200, scale=c.sm_scale, num_splits=splits)
+    torch.cuda.synchronize()
+    ro, rl = oracle.prefill_paged(q, kp, vp, table, lens, scale=c.sm_scale)
+    check(out, lse, ro, rl, what=f"paged prefill splits={splits}")
+
+
+def test_positional_entry_point_matches_the_struct_one():
+    c = workloads.PagedPrefillCase(B=2, Hq=8, Hkv=2, Lq=50, D=128, page_size=16, num_pages=90,
+                                   min_len=0, max_len=1000, seq_lens=[1000, 200], seed=10)
+    _, (qd, kd, vd, td, ld) = _inputs_on_gpu(c)
+    lib = fa.load_library()
+    o1, l1 = fa.fa_prefill_paged(qd, kd, vd, td, ld, 1000, scale=c.sm_scale)
+    o2 = torch.empty_like(qd)
+    l2 = torch.empty(c.B, c.Hq, c.Lq, dtype=torch.float32, device="cuda")
+    n = lib.fa_prefill_paged_workspace_size(c.B, c.Hq, c.Hkv, c.Lq, c.D, 1000)
+    ws = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
+    rc = lib.fa_prefill_paged(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), td.data_ptr(),
+                              ld.data_ptr(), o2.data_ptr(), l2.data_ptr(), c.B, c.Hq, c.Hkv,
+                              c.Lq, c.D, c.page_size, td.shape[1], c.num_pages, 1000, 1,
+                              c.sm_scale, ws.data_ptr(), n,
+                              torch.cuda.current_stream().cuda_stream)
+    assert rc == fa.FA_OK, fa.fa_last_error()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)

@@ -385,3 +385,18 @@ def test_prefill_paged_rows_without_keys_are_empty():
     assert torch.all(lse[2, :, :2] == -math.inf) and torch.all(out[2, :, :2] == 0)
     assert torch.isfinite(lse[2, :, 2:]).all()
     assert torch.all(lse[3] == -math.inf) and torch.all(out[3] == 0)
+
+
+def test_prefill_paged_mask_equals_dense_with_the_mask_columns():
+    c, (q, kp, vp, table, lens) = _paged_prefill_case()
+    g = torch.Generator().manual_seed(9)
+    mask = torch.randn(c.B, c.Lq, c.max_len, generator=g, dtype=torch.float64)
+    mask[:, :, 3] = -math.inf
+    out, lse = oracle.prefill_paged(q, kp, vp, table, lens, causal=False, mask=mask)
+    for b in range(c.B):
+        n = int(lens[b])
+        kd = _dense_from_pages(kp, table, n, b).unsqueeze(0)
+        vd = _dense_from_pages(vp, table, n, b).unsqueeze(0)
+        o2, l2 = oracle.attention(q[b:b + 1], kd, vd, mask=mask[b:b + 1, :, :n])
+        torch.testing.assert_close(out[b], o2[0], rtol=0, atol=1e-12)
+        torch.testing.assert_close(lse[b], l2[0], rtol=0, atol=1e-12)
