@@ -124,6 +124,25 @@ int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
 
 size_t fa_decode_workspace_size(int B, int Hq, int D, int max_seq_len);
 
+/* fa_decode_paged with the element type as an argument: the same fields, plus dtype
+ * FA_BF16 or FA_FP16 for q, the pages and out (the split states and lse stay fp32). */
+typedef struct fa_decode_args {
+  const void* q;
+  const void* k_pages;
+  const void* v_pages;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  void* out;
+  float* lse;
+  int B, Hq, Hkv, D, page_size, max_pages_per_seq, num_pages, max_seq_len;
+  float scale;
+  fa_dtype dtype;
+  void* workspace;
+  size_t workspace_bytes;
+} fa_decode_args;
+
+int fa_decode_paged_ex(const fa_decode_args* args, void* stream);
+
 /*
  * fa_decode_paged for callers that cannot allocate device memory (the pages describe no
  * such entry point; it has no counterpart there).  Same arguments and results as
@@ -186,6 +205,26 @@ int mla_decode_paged(const void* q_nope, const void* q_pe, const void* ckv_pages
                      void* workspace, size_t workspace_bytes, void* stream);
 
 size_t mla_decode_workspace_size(int B, int H, int Dc, int max_seq_len);
+
+/* mla_decode_paged with the element type as an argument: the same fields, plus dtype
+ * FA_BF16 or FA_FP16 for q_nope, q_pe, the pages and out. */
+typedef struct mla_decode_args {
+  const void* q_nope;
+  const void* q_pe;
+  const void* ckv_pages;
+  const void* kpe_pages;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  void* out;
+  float* lse;
+  int B, H, Dc, Dr, page_size, max_pages_per_seq, num_pages, max_seq_len;
+  float scale;
+  fa_dtype dtype;
+  void* workspace;
+  size_t workspace_bytes;
+} mla_decode_args;
+
+int mla_decode_paged_ex(const mla_decode_args* args, void* stream);
 
 /* Tokens per split-KV chunk that mla_decode_paged uses (a multiple of the kernel's tile). */
 int mla_decode_chunk_tokens(int B, int H, int max_seq_len);

@@ -33,10 +33,10 @@ _DT = {torch.bfloat16: FA_BF16, torch.float16: FA_FP16, torch.float32: FA_FP32}
 EXPORTS = (
     "fa_prefill", "fa_prefill_ex", "fa_prefill_workspace_size", "fa_prefill_num_splits",
     "fa_prefill_paged", "fa_prefill_paged_workspace_size",
-    "fa_decode_paged", "fa_decode_workspace_size", "fa_decode_chunk_tokens",
+    "fa_decode_paged", "fa_decode_paged_ex", "fa_decode_workspace_size", "fa_decode_chunk_tokens",
     "fa_decode_paged_noalloc",
     "fa_decode_paged_states", "mla_decode_paged", "mla_decode_workspace_size",
-    "mla_decode_chunk_tokens", "mla_decode_paged_states", "fa_merge_states",
+    "mla_decode_chunk_tokens", "mla_decode_paged_states", "mla_decode_paged_ex", "fa_merge_states",
     "fa_get_device_status", "fa_selftest_wait_timeout", "fa_last_error", "fa_version",
 )
 
@@ -59,6 +59,33 @@ class PrefillArgs(ctypes.Structure):
         ("workspace_bytes", ctypes.c_size_t),
         ("page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
         ("page_size", ctypes.c_int), ("max_pages", ctypes.c_int), ("num_pages", ctypes.c_int),
+    ]
+
+
+class DecodeArgs(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k_pages", ctypes.c_void_p), ("v_pages", ctypes.c_void_p),
+        ("page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("D", ctypes.c_int),
+        ("page_size", ctypes.c_int), ("max_pages_per_seq", ctypes.c_int),
+        ("num_pages", ctypes.c_int), ("max_seq_len", ctypes.c_int),
+        ("scale", ctypes.c_float), ("dtype", ctypes.c_int), ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+class MlaArgs(ctypes.Structure):
+    _fields_ = [
+        ("q_nope", ctypes.c_void_p), ("q_pe", ctypes.c_void_p),
+        ("ckv_pages", ctypes.c_void_p), ("kpe_pages", ctypes.c_void_p),
+        ("page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("H", ctypes.c_int), ("Dc", ctypes.c_int), ("Dr", ctypes.c_int),
+        ("page_size", ctypes.c_int), ("max_pages_per_seq", ctypes.c_int),
+        ("num_pages", ctypes.c_int), ("max_seq_len", ctypes.c_int),
+        ("scale", ctypes.c_float), ("dtype", ctypes.c_int), ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
     ]
 
 
@@ -91,6 +118,10 @@ def load_library(path: str | None = None):
         lib.fa_prefill_paged_workspace_size.argtypes = [_i] * 6
         lib.fa_decode_paged.restype = _i
         lib.fa_decode_paged.argtypes = [_vp] * 7 + [_i] * 8 + [_f, _vp, _sz, _vp]
+        lib.fa_decode_paged_ex.restype = _i
+        lib.fa_decode_paged_ex.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
+        lib.mla_decode_paged_ex.restype = _i
+        lib.mla_decode_paged_ex.argtypes = [ctypes.POINTER(MlaArgs), _vp]
         lib.fa_decode_workspace_size.restype = _sz
         lib.fa_decode_workspace_size.argtypes = [_i] * 4
         lib.fa_decode_paged_noalloc.restype = _i
@@ -290,10 +321,12 @@ def fa_decode_workspace_size(B, Hq, D, max_seq_len) -> int:
 
 def fa_decode_paged(q, k_pages, v_pages, page_table, seq_lens, max_seq_len: int,
                     scale: float | None = None, out=None, lse=None, workspace=None, stream=None):
-    """Split-KV paged GQA decode.  q [B,Hq,D] bf16; pages [num_pages,Hkv,page_size,D];
-    page_table [B,max_pages] int32; seq_lens [B] int32 (device)."""
+    """Split-KV paged GQA decode.  q [B,Hq,D] bf16 or fp16; pages [num_pages,Hkv,page_size,D]
+    in q's dtype; page_table [B,max_pages] int32; seq_lens [B] int32 (device)."""
     lib = load_library()
-    _need_dtype(torch.bfloat16, q, k_pages, v_pages)
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError(f"expected bfloat16 or float16, got {q.dtype}")
+    _need_dtype(q.dtype, k_pages, v_pages)
     _need_dtype(torch.int32, page_table, seq_lens)
     _need_cuda(q, k_pages, v_pages, page_table, seq_lens)
     B, Hq, D = q.shape
@@ -304,14 +337,15 @@ def fa_decode_paged(q, k_pages, v_pages, page_table, seq_lens, max_seq_len: int,
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
-    _need_dtype(torch.bfloat16, out)
+    _need_dtype(q.dtype, out)
     _need_dtype(torch.float32, lse)
     _need_cuda(out, lse)
     ws = _workspace(lib.fa_decode_workspace_size(B, Hq, D, max_seq_len), q.device, workspace)
-    _check(lib.fa_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
-                               _ptr(seq_lens), _ptr(out), _ptr(lse), B, Hq, Hkv, D, page_size,
-                               page_table.shape[1], num_pages, int(max_seq_len), float(scale),
-                               _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+    a = DecodeArgs(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(seq_lens),
+                   _ptr(out), _ptr(lse), B, Hq, Hkv, D, page_size, page_table.shape[1], num_pages,
+                   int(max_seq_len), float(scale), _DT[q.dtype], _ptr(ws),
+                   0 if ws is None else ws.numel())
+    _check(lib.fa_decode_paged_ex(ctypes.byref(a), _stream(stream)))
     return out, lse
 
 
@@ -404,10 +438,13 @@ def mla_decode_workspace_size(B, H, Dc, max_seq_len) -> int:
 
 def mla_decode_paged(q_nope, q_pe, ckv, kpe, page_table, seq_lens, max_seq_len: int,
                      scale: float, out=None, lse=None, workspace=None, stream=None):
-    """MLA paged decode (latent form).  q_nope [B,H,512], q_pe [B,H,64] bf16;
-    ckv [P,page_size,512], kpe [P,page_size,64]; page_table [B,max_pages]; seq_lens [B]."""
+    """MLA paged decode (latent form).  q_nope [B,H,512], q_pe [B,H,64] bf16 or fp16;
+    ckv [P,page_size,512], kpe [P,page_size,64] in that dtype; page_table [B,max_pages];
+    seq_lens [B]."""
     lib = load_library()
-    _need_dtype(torch.bfloat16, q_nope, q_pe, ckv, kpe)
+    if q_nope.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError(f"expected bfloat16 or float16, got {q_nope.dtype}")
+    _need_dtype(q_nope.dtype, q_pe, ckv, kpe)
     _need_dtype(torch.int32, page_table, seq_lens)
     _need_cuda(q_nope, q_pe, ckv, kpe, page_table, seq_lens)
     B, H, Dc = q_nope.shape
@@ -417,14 +454,15 @@ def mla_decode_paged(q_nope, q_pe, ckv, kpe, page_table, seq_lens, max_seq_len: 
         out = torch.empty_like(q_nope)
     if lse is None:
         lse = torch.empty(B, H, dtype=torch.float32, device=q_nope.device)
-    _need_dtype(torch.bfloat16, out)
+    _need_dtype(q_nope.dtype, out)
     _need_dtype(torch.float32, lse)
     _need_cuda(out, lse)
     ws = _workspace(lib.mla_decode_workspace_size(B, H, Dc, max_seq_len), q_nope.device, workspace)
-    _check(lib.mla_decode_paged(_ptr(q_nope), _ptr(q_pe), _ptr(ckv), _ptr(kpe), _ptr(page_table),
-                                _ptr(seq_lens), _ptr(out), _ptr(lse), B, H, Dc, Dr, page_size,
-                                page_table.shape[1], num_pages, int(max_seq_len), float(scale),
-                                _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+    a = MlaArgs(_ptr(q_nope), _ptr(q_pe), _ptr(ckv), _ptr(kpe), _ptr(page_table), _ptr(seq_lens),
+                _ptr(out), _ptr(lse), B, H, Dc, Dr, page_size, page_table.shape[1], num_pages,
+                int(max_seq_len), float(scale), _DT[q_nope.dtype], _ptr(ws),
+                0 if ws is None else ws.numel())
+    _check(lib.mla_decode_paged_ex(ctypes.byref(a), _stream(stream)))
     return out, lse
 
 

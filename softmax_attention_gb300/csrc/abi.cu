@@ -483,8 +483,9 @@ cudaError_t decode_states(const void* q, const void* k_pages, const void* v_page
                           const int32_t* page_table, const int32_t* seq_lens, float* o_part,
                           float* lse_part, int chunk, int n_chunks, int B, int Hq, int Hkv, int D,
                           int page_size, int max_pages_per_seq, int num_pages, float scale,
-                          uint32_t* status, cudaStream_t st) {
+                          uint32_t* status, cudaStream_t st, bool f16 = false) {
   DecodeParams p{};
+  p.f16 = f16 ? 1 : 0;
   p.q = q;
   p.k_pages = k_pages;
   p.v_pages = v_pages;
@@ -536,8 +537,9 @@ cudaError_t mla_states(const void* q_nope, const void* q_pe, const void* ckv_pag
                        float* o_part, float* lse_part, int chunk, int n_chunks, int B, int H,
                        int Dc, int Dr, int page_size, int max_pages_per_seq, int num_pages,
                        float scale, uint32_t* status, cudaStream_t st, void* direct_out = nullptr,
-                       float* direct_lse = nullptr) {
+                       float* direct_lse = nullptr, bool f16 = false) {
   MlaParams p{};
+  p.f16 = f16 ? 1 : 0;
   p.direct = direct_out != nullptr;
   p.out = direct_out;
   p.lse = direct_lse;
@@ -572,7 +574,7 @@ void carve(void* ws, long rows, int n_chunks, int D, float** o, float** l) {
 
 int merge_chunks(float* o_part, float* lse_part, const int32_t* seq_lens, int rows_per_seq,
                  int chunk, int n_chunks, void* out, float* lse, int rows, int D, cudaStream_t st,
-                 const char* who) {
+                 const char* who, Dtype out_dtype = Dtype::BF16) {
   MergeParams m{};
   m.o_part = o_part;
   m.lse_part = lse_part;
@@ -584,7 +586,7 @@ int merge_chunks(float* o_part, float* lse_part, const int32_t* seq_lens, int ro
   m.rows = rows;
   m.D = D;
   m.max_splits = n_chunks;
-  m.out_dtype = Dtype::BF16;
+  m.out_dtype = out_dtype;
   cudaError_t e = launch_merge(m, st);
   if (e != cudaSuccess) return cuda_fail(who, e);
   return FA_OK;
@@ -595,36 +597,50 @@ int merge_chunks(float* o_part, float* lse_part, const int32_t* seq_lens, int ro
 
 extern "C" {
 
+int fa_decode_paged_ex(const fa_decode_args* a, void* stream) {
+  if (!a) return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: null argument struct");
+  if (a->dtype != FA_BF16 && a->dtype != FA_FP16)
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: dtype must be FA_BF16 or FA_FP16");
+  const int B = a->B, Hq = a->Hq, D = a->D, max_seq_len = a->max_seq_len;
+  int rc = check_decode(a->q, a->k_pages, a->v_pages, a->page_table, a->seq_lens, B, Hq, a->Hkv,
+                        D, a->page_size, a->max_pages_per_seq, a->num_pages, max_seq_len, a->scale);
+  if (rc != FA_OK || B == 0) return rc;
+  if (!a->out || !aligned16(a->out))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: out must be a 16-byte aligned pointer");
+  const int chunk = decode_chunk(B, Hq, max_seq_len > 0 ? max_seq_len : 1);
+  const int n_chunks = max_seq_len > 0 ? (max_seq_len + chunk - 1) / chunk : 0;
+  const size_t need = n_chunks > 0 ? split_ws_bytes((long)B * Hq, n_chunks, D) : 0;
+  if (need > 0 && (!a->workspace || a->workspace_bytes < need))
+    return fail(FA_ERR_WORKSPACE, "fa_decode_paged: workspace of %zu bytes needed (got %zu)", need,
+                a->workspace ? a->workspace_bytes : (size_t)0);
+  if (need > 0 && (reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: workspace must be 256-byte aligned");
+  uint32_t* status = device_status_ptr();
+  if (!status) return fail(FA_ERR_CUDA, "fa_decode_paged: no usable CUDA device");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool f16 = a->dtype == FA_FP16;
+  float *o_part = nullptr, *lse_part = nullptr;
+  if (n_chunks > 0) {
+    carve(a->workspace, (long)B * Hq, n_chunks, D, &o_part, &lse_part);
+    cudaError_t e = decode_states(a->q, a->k_pages, a->v_pages, a->page_table, a->seq_lens,
+                                  o_part, lse_part, chunk, n_chunks, B, Hq, a->Hkv, D,
+                                  a->page_size, a->max_pages_per_seq, a->num_pages, a->scale,
+                                  status, st, f16);
+    if (e != cudaSuccess) return cuda_fail("fa_decode_paged (decode kernel)", e);
+  }
+  return merge_chunks(o_part, lse_part, a->seq_lens, Hq, chunk, n_chunks, a->out, a->lse, B * Hq,
+                      D, st, "fa_decode_paged (merge kernel)", f16 ? Dtype::FP16 : Dtype::BF16);
+}
+
 int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                     const int32_t* page_table, const int32_t* seq_lens, void* out, float* lse,
                     int B, int Hq, int Hkv, int D, int page_size, int max_pages_per_seq,
                     int num_pages, int max_seq_len, float scale, void* workspace,
                     size_t workspace_bytes, void* stream) {
-  int rc = check_decode(q, k_pages, v_pages, page_table, seq_lens, B, Hq, Hkv, D, page_size,
-                        max_pages_per_seq, num_pages, max_seq_len, scale);
-  if (rc != FA_OK || B == 0) return rc;
-  if (!out || !aligned16(out)) return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: out must be a 16-byte aligned pointer");
-  const int chunk = decode_chunk(B, Hq, max_seq_len > 0 ? max_seq_len : 1);
-  const int n_chunks = max_seq_len > 0 ? (max_seq_len + chunk - 1) / chunk : 0;
-  const size_t need = n_chunks > 0 ? split_ws_bytes((long)B * Hq, n_chunks, D) : 0;
-  if (need > 0 && (!workspace || workspace_bytes < need))
-    return fail(FA_ERR_WORKSPACE, "fa_decode_paged: workspace of %zu bytes needed (got %zu)", need,
-                workspace ? workspace_bytes : (size_t)0);
-  if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: workspace must be 256-byte aligned");
-  uint32_t* status = device_status_ptr();
-  if (!status) return fail(FA_ERR_CUDA, "fa_decode_paged: no usable CUDA device");
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  float *o_part = nullptr, *lse_part = nullptr;
-  if (n_chunks > 0) {
-    carve(workspace, (long)B * Hq, n_chunks, D, &o_part, &lse_part);
-    cudaError_t e = decode_states(q, k_pages, v_pages, page_table, seq_lens, o_part, lse_part,
-                                  chunk, n_chunks, B, Hq, Hkv, D, page_size, max_pages_per_seq,
-                                  num_pages, scale, status, st);
-    if (e != cudaSuccess) return cuda_fail("fa_decode_paged (decode kernel)", e);
-  }
-  return merge_chunks(o_part, lse_part, seq_lens, Hq, chunk, n_chunks, out, lse, B * Hq, D, st,
-                      "fa_decode_paged (merge kernel)");
+  const fa_decode_args a = {q, k_pages, v_pages, page_table, seq_lens, out, lse, B, Hq, Hkv, D,
+                            page_size, max_pages_per_seq, num_pages, max_seq_len, scale, FA_BF16,
+                            workspace, workspace_bytes};
+  return fa_decode_paged_ex(&a, stream);
 }
 
 int fa_decode_paged_states(const void* q, const void* k_pages, const void* v_pages,
@@ -661,44 +677,60 @@ int mla_decode_chunk_tokens(int B, int H, int max_seq_len) {
   return mla_chunk_tokens(B > 0 ? B : 1, H > 0 ? H : 1, max_seq_len > 0 ? max_seq_len : 1);
 }
 
+int mla_decode_paged_ex(const mla_decode_args* a, void* stream) {
+  if (!a) return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: null argument struct");
+  if (a->dtype != FA_BF16 && a->dtype != FA_FP16)
+    return fail(FA_ERR_UNSUPPORTED, "mla_decode_paged: dtype must be FA_BF16 or FA_FP16");
+  const int B = a->B, H = a->H, Dc = a->Dc, max_seq_len = a->max_seq_len;
+  int rc = check_mla(a->q_nope, a->q_pe, a->ckv_pages, a->kpe_pages, a->page_table, a->seq_lens,
+                     B, H, Dc, a->Dr, a->page_size, a->max_pages_per_seq, a->num_pages,
+                     max_seq_len, a->scale);
+  if (rc != FA_OK || B == 0) return rc;
+  if (!a->out || !aligned16(a->out))
+    return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: out must be a 16-byte aligned pointer");
+  const int chunk = mla_chunk_tokens(B, H, max_seq_len > 0 ? max_seq_len : 1);
+  const int n_chunks = max_seq_len > 0 ? (max_seq_len + chunk - 1) / chunk : 0;
+  const size_t need = n_chunks > 0 ? split_ws_bytes((long)B * H, n_chunks, Dc) : 0;
+  if (need > 0 && (!a->workspace || a->workspace_bytes < need))
+    return fail(FA_ERR_WORKSPACE, "mla_decode_paged: workspace of %zu bytes needed (got %zu)", need,
+                a->workspace ? a->workspace_bytes : (size_t)0);
+  if (need > 0 && (reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0)
+    return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: workspace must be 256-byte aligned");
+  uint32_t* status = device_status_ptr();
+  if (!status) return fail(FA_ERR_CUDA, "mla_decode_paged: no usable CUDA device");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool f16 = a->dtype == FA_FP16;
+  float *o_part = nullptr, *lse_part = nullptr;
+  if (n_chunks == 1) {
+    // every sequence fits one chunk: the kernel writes the final output, no merge
+    cudaError_t e = mla_states(a->q_nope, a->q_pe, a->ckv_pages, a->kpe_pages, a->page_table,
+                               a->seq_lens, nullptr, nullptr, chunk, 1, B, H, Dc, a->Dr,
+                               a->page_size, a->max_pages_per_seq, a->num_pages, a->scale,
+                               status, st, a->out, a->lse, f16);
+    if (e != cudaSuccess) return cuda_fail("mla_decode_paged (MLA kernel)", e);
+    return FA_OK;
+  }
+  if (n_chunks > 0) {
+    carve(a->workspace, (long)B * H, n_chunks, Dc, &o_part, &lse_part);
+    cudaError_t e = mla_states(a->q_nope, a->q_pe, a->ckv_pages, a->kpe_pages, a->page_table,
+                               a->seq_lens, o_part, lse_part, chunk, n_chunks, B, H, Dc, a->Dr,
+                               a->page_size, a->max_pages_per_seq, a->num_pages, a->scale,
+                               status, st, nullptr, nullptr, f16);
+    if (e != cudaSuccess) return cuda_fail("mla_decode_paged (MLA kernel)", e);
+  }
+  return merge_chunks(o_part, lse_part, a->seq_lens, H, chunk, n_chunks, a->out, a->lse, B * H, Dc,
+                      st, "mla_decode_paged (merge kernel)", f16 ? Dtype::FP16 : Dtype::BF16);
+}
+
 int mla_decode_paged(const void* q_nope, const void* q_pe, const void* ckv_pages,
                      const void* kpe_pages, const int32_t* page_table, const int32_t* seq_lens,
                      void* out, float* lse, int B, int H, int Dc, int Dr, int page_size,
                      int max_pages_per_seq, int num_pages, int max_seq_len, float scale,
                      void* workspace, size_t workspace_bytes, void* stream) {
-  int rc = check_mla(q_nope, q_pe, ckv_pages, kpe_pages, page_table, seq_lens, B, H, Dc, Dr,
-                     page_size, max_pages_per_seq, num_pages, max_seq_len, scale);
-  if (rc != FA_OK || B == 0) return rc;
-  if (!out || !aligned16(out)) return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: out must be a 16-byte aligned pointer");
-  const int chunk = mla_chunk_tokens(B, H, max_seq_len > 0 ? max_seq_len : 1);
-  const int n_chunks = max_seq_len > 0 ? (max_seq_len + chunk - 1) / chunk : 0;
-  const size_t need = n_chunks > 0 ? split_ws_bytes((long)B * H, n_chunks, Dc) : 0;
-  if (need > 0 && (!workspace || workspace_bytes < need))
-    return fail(FA_ERR_WORKSPACE, "mla_decode_paged: workspace of %zu bytes needed (got %zu)", need,
-                workspace ? workspace_bytes : (size_t)0);
-  if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: workspace must be 256-byte aligned");
-  uint32_t* status = device_status_ptr();
-  if (!status) return fail(FA_ERR_CUDA, "mla_decode_paged: no usable CUDA device");
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  float *o_part = nullptr, *lse_part = nullptr;
-  if (n_chunks == 1) {
-    // every sequence fits one chunk: the kernel writes the final output, no merge
-    cudaError_t e = mla_states(q_nope, q_pe, ckv_pages, kpe_pages, page_table, seq_lens, nullptr,
-                               nullptr, chunk, 1, B, H, Dc, Dr, page_size, max_pages_per_seq,
-                               num_pages, scale, status, st, out, lse);
-    if (e != cudaSuccess) return cuda_fail("mla_decode_paged (MLA kernel)", e);
-    return FA_OK;
-  }
-  if (n_chunks > 0) {
-    carve(workspace, (long)B * H, n_chunks, Dc, &o_part, &lse_part);
-    cudaError_t e = mla_states(q_nope, q_pe, ckv_pages, kpe_pages, page_table, seq_lens, o_part,
-                               lse_part, chunk, n_chunks, B, H, Dc, Dr, page_size,
-                               max_pages_per_seq, num_pages, scale, status, st);
-    if (e != cudaSuccess) return cuda_fail("mla_decode_paged (MLA kernel)", e);
-  }
-  return merge_chunks(o_part, lse_part, seq_lens, H, chunk, n_chunks, out, lse, B * H, Dc, st,
-                      "mla_decode_paged (merge kernel)");
+  const mla_decode_args a = {q_nope, q_pe, ckv_pages, kpe_pages, page_table, seq_lens, out, lse,
+                             B, H, Dc, Dr, page_size, max_pages_per_seq, num_pages, max_seq_len,
+                             scale, FA_BF16, workspace, workspace_bytes};
+  return mla_decode_paged_ex(&a, stream);
 }
 
 int mla_decode_paged_states(const void* q_nope, const void* q_pe, const void* ckv_pages,
@@ -786,6 +818,6 @@ int fa_selftest_wait_timeout(unsigned timeout_us, void* stream) {
 
 const char* fa_last_error(void) { return g_err; }
 
-int fa_version(void) { return 200; }
+int fa_version(void) { return 300; }
 
 }  // extern "C"

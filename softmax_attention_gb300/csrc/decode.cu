@@ -32,31 +32,38 @@ struct DecLayout {
   static constexpr int kRing = kWarps * kStages * kSlot;
 };
 
-// bf16 pairs -> fp32
-__device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) {
-  lo = __uint_as_float(w << 16);
-  hi = __uint_as_float(w & 0xffff0000u);
-}
-
-template <int DPL>
-__device__ __forceinline__ void load_row_slice(const uint8_t* row, int lane, float (&f)[DPL]) {
-  if constexpr (DPL == 2) {
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(row + lane * 4);
-    bf16x2_to_f32(w, f[0], f[1]);
-  } else if constexpr (DPL == 4) {
-    const uint2 w = *reinterpret_cast<const uint2*>(row + lane * 8);
-    bf16x2_to_f32(w.x, f[0], f[1]);
-    bf16x2_to_f32(w.y, f[2], f[3]);
+// 16-bit pairs (bf16, or fp16 when F16) -> fp32
+template <bool F16>
+__device__ __forceinline__ void x2_to_f32(uint32_t w, float& lo, float& hi) {
+  if constexpr (F16) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+    lo = f.x;
+    hi = f.y;
   } else {
-    const uint4 w = *reinterpret_cast<const uint4*>(row + lane * 16);
-    bf16x2_to_f32(w.x, f[0], f[1]);
-    bf16x2_to_f32(w.y, f[2], f[3]);
-    bf16x2_to_f32(w.z, f[4], f[5]);
-    bf16x2_to_f32(w.w, f[6], f[7]);
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
   }
 }
 
-template <int D, int G>
+template <int DPL, bool F16>
+__device__ __forceinline__ void load_row_slice(const uint8_t* row, int lane, float (&f)[DPL]) {
+  if constexpr (DPL == 2) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(row + lane * 4);
+    x2_to_f32<F16>(w, f[0], f[1]);
+  } else if constexpr (DPL == 4) {
+    const uint2 w = *reinterpret_cast<const uint2*>(row + lane * 8);
+    x2_to_f32<F16>(w.x, f[0], f[1]);
+    x2_to_f32<F16>(w.y, f[2], f[3]);
+  } else {
+    const uint4 w = *reinterpret_cast<const uint4*>(row + lane * 16);
+    x2_to_f32<F16>(w.x, f[0], f[1]);
+    x2_to_f32<F16>(w.y, f[2], f[3]);
+    x2_to_f32<F16>(w.z, f[4], f[5]);
+    x2_to_f32<F16>(w.w, f[6], f[7]);
+  }
+}
+
+template <int D, int G, bool F16>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) {
   constexpr int DPL = D / 32;         // dims per lane
   constexpr int V = kBT * G;          // partial dot products per lane per block
@@ -95,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
                           (static_cast<size_t>(b) * p.Hq + hk * G) * D * 2;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      load_row_slice<DPL>(qrow + g * D * 2, lane, q[g]);
+      load_row_slice<DPL, F16>(qrow + g * D * 2, lane, q[g]);
 #pragma unroll
       for (int d = 0; d < DPL; ++d) q[g][d] *= p.scale_log2;
     }
@@ -189,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
 #pragma unroll
     for (int t = 0; t < kBT; ++t) {
       float kf[DPL];
-      load_row_slice<DPL>(Ks + t * D * 2, lane, kf);
+      load_row_slice<DPL, F16>(Ks + t * D * 2, lane, kf);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float a = 0.f;
@@ -247,7 +254,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
 #pragma unroll
     for (int t = 0; t < kBT; ++t) {
       float vf[DPL];
-      load_row_slice<DPL>(Vs + t * D * 2, lane, vf);
+      load_row_slice<DPL, F16>(Vs + t * D * 2, lane, vf);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const float pg = pbuf[warp][t][g];
@@ -308,7 +315,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
 template <int D, int G>
 cudaError_t launch_impl(const DecodeParams& p, cudaStream_t stream) {
   using L = DecLayout<D>;
-  auto kern = decode_kernel<D, G>;
+  auto kern = p.f16 ? decode_kernel<D, G, true> : decode_kernel<D, G, false>;
   const int smem = L::kRing;
   cudaError_t e = ensure_smem_limit(kern, smem);
   if (e != cudaSuccess) return e;

@@ -64,6 +64,7 @@ struct DecodeParams {
   float* o_part;          // [B*Hq, n_chunks, D]
   float* lse_part;        // [B*Hq, n_chunks]
   uint32_t* status;
+  int f16;                // q and pages are fp16 (else bf16)
 };
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 
@@ -83,9 +84,10 @@ struct MlaParams {
   float* o_part;          // [B*H, n_chunks, Dc]
   float* lse_part;        // [B*H, n_chunks]
   int direct;             // n_chunks == 1: write out/lse directly, no partial states
-  void* out;              // [B,H,Dc] bf16 (direct mode)
+  void* out;              // [B,H,Dc] in the inputs' type (direct mode)
   float* lse;             // [B,H] or nullptr (direct mode)
   uint32_t* status;
+  int f16;                // q, ckv and kpe are fp16 (else bf16)
 };
 cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream);
 

@@ -81,6 +81,7 @@ __device__ __forceinline__ bool softmax_any(bool v) {
 }
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_kernel(const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qp,
                const MlaParams p) {
@@ -249,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ----------------------------------- MMA issuer --------------------------------------
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16(true, 64, kTile, false, false);
-      constexpr uint32_t idesc_o = idesc_f16(true, 128, kH, true, false);
+      constexpr uint32_t idesc_s = idesc_f16(BF16, 64, kTile, false, false);
+      constexpr uint32_t idesc_o = idesc_f16(BF16, 128, kH, true, false);
       // S of tile j: two N=32 halves, one per stage, into S buffer j & 1
       // (the two halves' accumulation chains are interleaved so the tensor core always
       // has an independent MMA to start)
@@ -395,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float p0 = exp2_approx(s[2 * e] - m_use);
         const float p1 = exp2_approx(s[2 * e + 1] - m_use);
         sum[e & 3] += p0 + p1;
-        pk[e] = pack_bf16x2(p0, p1);
+        pk[e] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
       }
       const float lsum = (sum[0] + sum[1]) + (sum[2] + sum[3]);
       l_run += lsum + __shfl_xor_sync(0xffffffffu, lsum, 16);  // the same total in both lanes
@@ -448,8 +449,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kDc / 8 / 32; ++k) {
             const float4 a = src[2 * (lane + 32 * k)], b2 = src[2 * (lane + 32 * k) + 1];
-            dst[lane + 32 * k] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
-                                            pack_bf16x2(b2.x, b2.y), pack_bf16x2(b2.z, b2.w));
+            dst[lane + 32 * k] =
+                BF16 ? make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
+                                  pack_bf16x2(b2.x, b2.y), pack_bf16x2(b2.z, b2.w))
+                     : make_uint4(pack_f16x2(a.x, a.y), pack_f16x2(a.z, a.w),
+                                  pack_f16x2(b2.x, b2.y), pack_f16x2(b2.z, b2.w));
           }
         } else {
           float4* dst = reinterpret_cast<float4*>(p.o_part + ((row0 + hh) * p.n_chunks + c) * kDc);
@@ -500,11 +504,12 @@ cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream) {
   if (p.direct && p.n_chunks != 1) return cudaErrorInvalidValue;
   CUtensorMap tqn, tqp;
   const uint64_t qrows = static_cast<uint64_t>(p.B) * kH;
+  const CUtensorMapDataType dt = p.f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   {
     const uint64_t dims[2] = {kDc, qrows};
     const uint64_t str[1] = {kDc * 2};
     const uint32_t box[2] = {64, kH};
-    if (!encode_tiled(&tqn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.q_nope, dims, str, box,
+    if (!encode_tiled(&tqn, dt, 2, p.q_nope, dims, str, box,
                       CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
@@ -512,14 +517,15 @@ cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream) {
     const uint64_t dims[2] = {kDr, qrows};
     const uint64_t str[1] = {kDr * 2};
     const uint32_t box[2] = {64, kH};
-    if (!encode_tiled(&tqp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.q_pe, dims, str, box,
+    if (!encode_tiled(&tqp, dt, 2, p.q_pe, dims, str, box,
                       CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = ensure_smem_limit(mla_kernel, kSmemBytes);
+  auto kern = p.f16 ? mla_kernel<false> : mla_kernel<true>;
+  cudaError_t e = ensure_smem_limit(kern, kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_chunks, p.B);
-  mla_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tqn, tqp, p);
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(tqn, tqp, p);
   return cudaGetLastError();
 }
 

@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version(lib):
-    assert lib.fa_version() == 200  # 0.2.0: fa_prefill_args gained the paging fields
+    assert lib.fa_version() == 300  # 0.3.0: decode and MLA argument structs with a dtype
 
 
 def _args(**kw):

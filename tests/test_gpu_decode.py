@@ -119,3 +119,12 @@ def test_states_then_merge_equals_full_call():
     out2, lse2 = fa.fa_merge_states(op, ol, n.cuda(), out_dtype=torch.bfloat16)
     torch.cuda.synchronize()
     assert torch.equal(out.reshape(-1, c.D), out2) and torch.equal(lse.reshape(-1), lse2)
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,ps", [(128, 32, 8, 16), (64, 8, 1, 32)])
+def test_fp16(D, Hq, Hkv, ps):
+    c = workloads.PagedCase(B=5, Hq=Hq, Hkv=Hkv, D=D, page_size=ps, num_pages=400, min_len=0,
+                            max_len=1500, dtype=torch.float16, seed=D + Hq)
+    out, lse, ro, rl = _run(c)
+    assert out.dtype == torch.float16
+    check(out, lse, ro, rl, what=f"decode fp16 D={D}")

@@ -100,3 +100,14 @@ def test_out_of_range_page_is_reported():
     fa.mla_decode_paged(*[t.cuda() for t in (qn, qp, ckv, kpe, table, lens)], c.max_len, c.scale)
     assert fa.fa_get_device_status() == fa.FA_ERR_BOUNDS
     assert fa.fa_get_device_status() == fa.FA_OK
+
+
+@pytest.mark.parametrize("lens", [[300, 1, 2048], [100, 0]])
+def test_fp16(lens):
+    """fp16 operands (the tensor cores' f16 kind with fp16 on both sides); the first case
+    splits sequences into chunks and merges, the second writes the output directly."""
+    c = workloads.MlaCase(B=len(lens), H=64, seq_len=None, seq_lens=lens, page_size=1,
+                          dtype=torch.float16, seed=len(lens) + 17)
+    out, lse, ro, rl = _run(c)
+    assert out.dtype == torch.float16
+    check(out, lse, ro, rl, what=f"mla fp16 {lens}")
