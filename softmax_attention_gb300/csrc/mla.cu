@@ -422,17 +422,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // each head's 2 KB row with 16-byte coalesced stores.
     float* ostage = reinterpret_cast<float*>(smem + kKVOff);
     if (ok) {
+      // the 64 per-head scales go to registers first: read from shared memory between the
+      // staging stores, each would wait for the stores before it (the compiler cannot tell
+      // the two arrays apart)
+      float inv[kH];
+#pragma unroll
+      for (int e = 0; e < kH; ++e) inv[e] = stat_s[e];
 #pragma unroll 1
       for (int db = 0; db < kDc / 128; ++db) {
         const int d = db * 128 + warp * 32 + lane;
-#pragma unroll 1
+#pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t o[32];
           tmem_ld32(tmem + kTmemO + lane_off + db * kH + half * 32, o);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            ostage[(half * 32 + e) * kDc + d] = __uint_as_float(o[e]) * stat_s[half * 32 + e];
+            ostage[(half * 32 + e) * kDc + d] = __uint_as_float(o[e]) * inv[half * 32 + e];
         }
       }
     }
