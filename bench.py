@@ -349,7 +349,8 @@ def bench_prefill_paged(fa, c, steps, warmup, flush, dist, pk):
     res = {"value": round(tflops, 2), "unit": "TFLOP/s", "ms": round(mean_ms, 4),
            "flops": flops, "seq_lens": lens.tolist(), "workspace_bytes": nbytes,
            "launches_per_step": 1 + (nbytes > 0), "mode": mode,
-           "roofline": roofline("tensor", tflops, pk["bf16"], "TFLOP/s", None, pk)}
+           "roofline": roofline("tensor", tflops, pk["bf16"], "TFLOP/s",
+                                profiled_traffic("prefill_paged_gqa.md", "prefill"), pk)}
     del qd, kd, vd, td, ld, out, lse, ws
     torch.cuda.empty_cache()
     return res
