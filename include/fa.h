@@ -85,7 +85,8 @@ typedef struct fa_prefill_args {
      page_table[b, t / page_size]; sequence b holds seq_lens[b] keys (device memory) and its
      Lq queries are its last Lq positions.  Lkv is then the largest seq_lens[b]: it sizes the
      KV split and is the last dimension of the mask.  dtype FA_BF16 or FA_FP16; page_size a
-     power of two in [8, 128] (at most 64 when D = 256); Lkv <= max_pages * page_size. */
+     power of two in [8, 128] (at most 64 when D = 256); Lkv <= max_pages * page_size;
+     num_pages * Hkv < 2^31 (FA_ERR_UNSUPPORTED otherwise). */
   const int32_t* page_table; /* [B, max_pages] int32 */
   const int32_t* seq_lens;   /* [B] int32 */
   int page_size, max_pages, num_pages;

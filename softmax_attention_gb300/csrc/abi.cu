@@ -177,6 +177,8 @@ int validate_prefill(const fa_prefill_args* a, bool check_pointers = true) {
       return fail(FA_ERR_UNSUPPORTED, "fa_prefill: paged K/V must be bf16 or fp16");
     if (work && (a->max_pages <= 0 || a->num_pages <= 0))
       return fail(FA_ERR_INVALID_ARG, "fa_prefill: max_pages and num_pages must be > 0");
+    if ((long)a->num_pages * a->Hkv > 2147483647L)
+      return fail(FA_ERR_UNSUPPORTED, "fa_prefill: num_pages * Hkv must fit in int32");
     if ((long)a->Lkv > (long)a->max_pages * a->page_size)
       return fail(FA_ERR_INVALID_ARG, "fa_prefill: Lkv %d exceeds max_pages * page_size",
                   a->Lkv);

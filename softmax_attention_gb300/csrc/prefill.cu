@@ -25,6 +25,18 @@ namespace {
 using prefill::kRows;
 constexpr int kThreads = 192;
 
+// 5-D tiled TMA load (the paged K/V boxes below).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t c0, int32_t c1, int32_t c2, int32_t c3,
+                                            int32_t c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "r"(bar)
+      : "memory");
+}
+
 template <int D, int BN, int STAGES>
 struct Layout {
   static constexpr int kQBytes = kRows * D * 2;
@@ -42,7 +54,8 @@ struct Layout {
   static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
-template <int D, int BN, int STAGES, bool BF16>
+// One CTA per (query tile, split) x kv head x batch.  PAGED: K/V through a page table.
+template <int D, int BN, int STAGES, bool BF16, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -65,6 +78,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBarOff + L::kNumBars * 8);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // A K or V stage holds BN rows x D columns as 1024-byte SW128 atoms (8 rows x 64 columns).
+  // Dense: the atoms of one 64-column block follow each other down the rows, block after
+  // block, so a column block of a tile is one TMA box.  Paged: the D/64 atoms of one 8-row
+  // group sit side by side, group after group, so a page (whole 8-row groups) is one box.
+  constexpr uint32_t kCB = PAGED ? 1024u : BN * 128u;             // column-block stride
+  constexpr uint32_t kRG = PAGED ? (D / 64) * 1024u : 1024u;      // 8-row-group stride
 
   // ---- work item: (query tile, split) x kv head x batch; heavier (later) tiles first ----
   const int split = blockIdx.x % p.n_splits;
@@ -74,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q_last = min(p.Lq, q0 + p.q_per_tile) - 1;
   // keys of this sequence: dense Lkv, or the sequence's length in the paged cache
   int Lkv = p.Lkv;
-  if (p.page_table) {
+  if constexpr (PAGED) {
     Lkv = p.kv_lens[b];
     if (Lkv < 0 || Lkv > p.max_pages * p.page_size) {
       if (threadIdx.x == 0) record_error(p.status, kDevBounds);
@@ -124,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int issued = 0, k_only = -1;  // k_only: a K load issued without its V
       // K and V slots are released separately: K_j once S_j is done, V_j once P_j V_j is.
-      if (!p.page_table) {
+      if constexpr (!PAGED) {
         if (lane == 0) {
           const int kv_row = b * p.Hkv + hk;
           for (int jj = 0; jj < n; ++jj) {
@@ -147,10 +166,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        // Paged: a KV tile is BN / page_size pages, one TMA box (page_size rows x 64 columns,
-        // 1024-byte aligned in shared memory since page_size >= 8) per page and column block.
+        // Paged: a KV tile is BN / page_size pages and each page is one TMA box of page_size
+        // rows x D columns (page_size / 8 whole row groups).  The 5-D map walks a page as
+        // (64 columns, 8 rows, D/64 column blocks, page_size/8 row groups) so the box lands
+        // in the row-group-major atom order above; its last coordinate is page * Hkv + head.
         // Lane i holds the page id of page i of a tile, loaded one tile ahead, and issues that
-        // page's boxes itself, so one warp instruction starts the copies of every page.
+        // page's box itself, so one warp instruction starts the copies of every page.
         const int ps = p.page_size, tp = BN / ps;
         const int32_t* table = p.page_table + static_cast<size_t>(b) * p.max_pages;
         auto tile_page = [&](int jj) {
@@ -168,8 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         auto load_pages = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar, int id) {
           if (lane < tp)
-            for (int kb = 0; kb < D / 64; ++kb)
-              tma_load_4d(dst + kb * (BN * 128) + lane * ps * 128, map, bar, kb * 64, 0, hk, id);
+            tma_load_5d(dst + lane * (ps / 8) * kRG, map, bar, 0, 0, 0, 0, id * p.Hkv + hk);
         };
         int ids_next = tile_page(0);
         for (int jj = 0; jj < n; ++jj) {
@@ -214,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk % 4) * 32;
           const uint64_t ad = sdesc_sw128(sQ + (kk / 4) * (kRows * 128) + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(kbase + (kk / 4) * (BN * 128) + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(kbase + (kk / 4) * kCB + off, 16, kRG);
           mma_ss(d_s, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
         }
         tc_commit(bar_s(jj & 1));
@@ -240,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_p = tm_s0 + (jj & 1) * BN;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(vbase + kk * (16 * 128), BN * 128, 1024);
+          const uint64_t bd = sdesc_sw128(vbase + kk * (2 * kRG), kCB, kRG);
           mma_ts(tm_o, a_p + kk * 8, bd, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(bar_o);
@@ -279,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefill::store_p<BN>(t_s, pk);
       tmem_st_wait();
       const int key0 = (t_begin + jj) * BN;
-      if (p.page_table && key0 + BN > Lkv) {
+      if (PAGED && key0 + BN > Lkv) {
         // Rows past the sequence's end hold whatever the pool has there; P is 0 for them,
         // but 0 times a non-finite V would still poison O, so clear them once V has landed.
         const int stage = jj % STAGES;
@@ -289,7 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* vst = smem + L::kVOff + stage * L::kKVBytes;
         for (int i = threadIdx.x; i < (BN - r0) * (D / 64) * 8; i += 128) {
           const int blk = i / ((BN - r0) * 8), rem = i % ((BN - r0) * 8);
-          *reinterpret_cast<uint4*>(vst + blk * (BN * 128) + (r0 + rem / 8) * 128 + (rem % 8) * 16) =
+          const int r = r0 + rem / 8;
+          *reinterpret_cast<uint4*>(vst + (r / 8) * kRG + blk * kCB + (r % 8) * 128 + (rem % 8) * 16) =
               make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
@@ -301,7 +322,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (n - 1) & 1, p.status));
       tc_fence_after();
     }
-    if (ok) prefill::epilogue<D>(p, row, tm_o + lane_off, n > 0, m_run, l_run, split);
+    if (ok) {
+      float* part_o = nullptr;
+      float* part_lse = nullptr;
+      if (p.n_splits > 1 && row.valid) {
+        const size_t r = row.flat * p.n_splits + split;
+        part_o = p.o_part + r * D;
+        part_lse = p.lse_part + r;
+      }
+      prefill::epilogue<D>(p, row, tm_o + lane_off, n > 0, m_run, l_run, part_o, part_lse);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -312,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int BN, int STAGES, bool BF16>
+template <int D, int BN, int STAGES, bool BF16, bool PAGED>
 cudaError_t launch_impl(const PrefillParams& p, cudaStream_t stream) {
   using L = Layout<D, BN, STAGES>;
   const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -325,15 +355,16 @@ cudaError_t launch_impl(const PrefillParams& p, cudaStream_t stream) {
     if (!encode_tiled(&tq, dt, 4, p.q, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  if (p.page_table) {
-    // pages [num_pages, Hkv, page_size, D]; one box = one page's rows of one kv head
+  if constexpr (PAGED) {
+    // pages [num_pages, Hkv, page_size, D] seen as (column, row in group, column block, row
+    // group, page * Hkv + head); one box = one page of one kv head, every column
     if (p.page_size < 8 || BN % p.page_size != 0) return cudaErrorInvalidValue;
-    const uint64_t ps = (uint64_t)p.page_size;
-    const uint64_t dims[4] = {(uint64_t)D, ps, (uint64_t)p.Hkv, (uint64_t)p.num_pages};
-    const uint64_t str[3] = {(uint64_t)D * 2, ps * D * 2, (uint64_t)p.Hkv * ps * D * 2};
-    const uint32_t box[4] = {64, (uint32_t)p.page_size, 1, 1};
-    if (!encode_tiled(&tk, dt, 4, p.k, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tiled(&tv, dt, 4, p.v, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint64_t ps = (uint64_t)p.page_size, row = (uint64_t)D * 2;
+    const uint64_t dims[5] = {64, 8, (uint64_t)D / 64, ps / 8, (uint64_t)p.num_pages * p.Hkv};
+    const uint64_t str[4] = {row, 128, 8 * row, ps * row};
+    const uint32_t box[5] = {64, 8, (uint32_t)D / 64, (uint32_t)p.page_size / 8, 1};
+    if (!encode_tiled(&tk, dt, 5, p.k, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled(&tv, dt, 5, p.v, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   } else {
     const uint64_t dims[3] = {(uint64_t)D, lkv, (uint64_t)p.Hkv * p.B};
@@ -343,12 +374,23 @@ cudaError_t launch_impl(const PrefillParams& p, cudaStream_t stream) {
         !encode_tiled(&tv, dt, 3, p.v, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  auto kern = prefill_kernel<D, BN, STAGES, BF16>;
+  auto kern = prefill_kernel<D, BN, STAGES, BF16, PAGED>;
   cudaError_t e = ensure_smem_limit(kern, L::kAlloc);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_qtiles * p.n_splits, p.Hkv, p.B);
+  const dim3 grid(p.n_qtiles * p.n_splits, p.Hkv, p.B);
   kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
+}
+
+// The dense and paged kernels are separate instantiations, so the dense one carries none of
+// the page-table reads, the per-sequence length or the V-tail clearing.
+template <int D, int BN, int STAGES>
+cudaError_t launch_d(const PrefillParams& p, bool bf16, cudaStream_t stream) {
+  if (p.page_table)
+    return bf16 ? launch_impl<D, BN, STAGES, true, true>(p, stream)
+                : launch_impl<D, BN, STAGES, false, true>(p, stream);
+  return bf16 ? launch_impl<D, BN, STAGES, true, false>(p, stream)
+              : launch_impl<D, BN, STAGES, false, false>(p, stream);
 }
 
 }  // namespace
@@ -359,11 +401,11 @@ cudaError_t launch_prefill(const PrefillParams& p, Dtype operand, cudaStream_t s
   const bool bf16 = operand == Dtype::BF16;
   switch (p.D) {
     case 64:
-      return bf16 ? launch_impl<64, 128, 5, true>(p, stream) : launch_impl<64, 128, 5, false>(p, stream);
+      return launch_d<64, 128, 5>(p, bf16, stream);
     case 128:
-      return bf16 ? launch_impl<128, 128, 3, true>(p, stream) : launch_impl<128, 128, 3, false>(p, stream);
+      return launch_d<128, 128, 3>(p, bf16, stream);
     case 256:
-      return bf16 ? launch_impl<256, 64, 2, true>(p, stream) : launch_impl<256, 64, 2, false>(p, stream);
+      return launch_d<256, 64, 2>(p, bf16, stream);
     default:
       return cudaErrorInvalidValue;
   }

@@ -158,12 +158,14 @@ __device__ __forceinline__ void store_p(uint32_t t_s, const uint32_t (&pk)[BN / 
     tmem_st16(t_s + c, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c]));
 }
 
-// Epilogue of one row: O / l to the output (or the split state), lse.  Warp-collective:
-// every lane reads its TMEM lane; rows that are not valid store nothing.  have_o is false
-// when no P V product was issued (no KV tile in this split): the row is then empty.
+// Epilogue of one row: O / l to the output, or to a partial state (part_o [D] fp32 and
+// part_lse, natural log) when part_o is set; lse to p.lse.  Warp-collective: every lane reads
+// its TMEM lane; rows that are not valid store nothing.  have_o is false when no P V product
+// was issued (no KV tile in this part): the row is then empty.
 template <int D>
 __device__ __forceinline__ void epilogue(const PrefillParams& p, const Row& row, uint32_t t_o,
-                                         bool have_o, float m, float l, int split) {
+                                         bool have_o, float m, float l, float* part_o,
+                                         float* part_lse) {
   const float inv_l = l > 0.f ? 1.f / l : 0.f;
   const float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 #pragma unroll 1
@@ -180,8 +182,8 @@ __device__ __forceinline__ void epilogue(const PrefillParams& p, const Row& row,
     float v[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv_l;
-    if (p.n_splits > 1) {
-      float4* dst = reinterpret_cast<float4*>(p.o_part + (row.flat * p.n_splits + split) * D + c * 32);
+    if (part_o) {
+      float4* dst = reinterpret_cast<float4*>(part_o + c * 32);
 #pragma unroll
       for (int e = 0; e < 8; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
     } else if (p.out_dtype == Dtype::FP32) {
@@ -200,7 +202,7 @@ __device__ __forceinline__ void epilogue(const PrefillParams& p, const Row& row,
     }
   }
   if (row.valid) {
-    if (p.n_splits > 1) p.lse_part[row.flat * p.n_splits + split] = lse_v;
+    if (part_o) *part_lse = lse_v;
     else if (p.lse) p.lse[row.flat] = lse_v;
   }
 }

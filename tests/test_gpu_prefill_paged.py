@@ -51,6 +51,9 @@ CASES = [
     (2, 32, 8, 33, [2049, 0], 128, 128, False),        # non-causal, an empty sequence
     (4, 12, 4, 50, [129, 128, 127, 1], 64, 32, True),  # G = 3, lengths around a tile
     (1, 16, 1, 7, [4000], 128, 16, True),              # G = 16
+    (2, 8, 2, 30, [515, 90], 256, 8, True),            # D = 256, eight pages a tile
+    (1, 4, 1, 20, [300], 128, 8, False),               # 8-key pages, one row group each
+    (2, 8, 4, 10, [260, 129], 64, 128, True),          # D = 64, a page per tile
 ]
 
 
@@ -72,8 +75,8 @@ def test_full_size_sampled():
 
 
 def test_paged_equals_dense_on_gathered_cache_bit_exact():
-    """One sequence: the paged call and the dense call on the same keys in order run the
-    same plan and arithmetic, so they agree bit for bit."""
+    """One sequence: the paged call and the dense call on the same keys in order, with the
+    same split count, run the same arithmetic, so they agree bit for bit."""
     c = workloads.PagedPrefillCase(B=1, Hq=8, Hkv=2, Lq=200, D=128, page_size=16,
                                    num_pages=200, min_len=0, max_len=1500, seq_lens=[1500],
                                    seed=3)
@@ -83,8 +86,9 @@ def test_paged_equals_dense_on_gathered_cache_bit_exact():
     kd = kp[pages].permute(1, 0, 2, 3).reshape(1, c.Hkv, -1, c.D)[:, :, :n].contiguous()
     vd = vp[pages].permute(1, 0, 2, 3).reshape(1, c.Hkv, -1, c.D)[:, :, :n].contiguous()
     o1, l1 = fa.fa_prefill_paged(*(t.cuda() for t in (q, kp, vp, table, lens)), n, causal=True,
-                                 scale=c.sm_scale)
-    o2, l2 = fa.fa_prefill_ex(q.cuda(), kd.cuda(), vd.cuda(), causal=True, scale=c.sm_scale)
+                                 scale=c.sm_scale, num_splits=3)
+    o2, l2 = fa.fa_prefill_ex(q.cuda(), kd.cuda(), vd.cuda(), causal=True, scale=c.sm_scale,
+                              num_splits=3)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
