@@ -27,67 +27,92 @@ __device__ __forceinline__ void store4(void* out, Dtype t, size_t idx, float4 v)
   }
 }
 
-// One CTA (4 warps) per (row, 128-column chunk).  Every warp reduces the row's log-sum-exps
-// (cheap, L1-resident); warp w accumulates the parts s = w, w+4, ... of the chunk (lane l
-// reads the 16-byte vector l, part loop unrolled so several loads are in flight), and the
-// four partial sums are combined through shared memory.  Splitting the row across CTAs keeps
-// few-row, many-part merges (a short query chunk split over the KV loop) parallel.
-constexpr int kMergeWarps = 4;
-constexpr int kChunkCols = 128;
+// kMergeWarps warps per CTA; W of them (1, 2, 4 or 8, from the largest part count) share one
+// row, so a CTA merges kMergeWarps / W rows.  Every warp of a row reduces the row's
+// log-sum-exps (a few loads, L1-resident), then accumulates the parts s = k, k + W, ... of
+// the row over all D columns: lane l holds the 16-byte vectors l, l + 32, ... (VPL of them),
+// and the part loop is unrolled so that several parts' loads are in flight at once.  With
+// W > 1 the warps' sums are combined through shared memory.  Few parts: one warp per row
+// and eight rows per CTA; many parts: eight warps on one row.
+constexpr int kMergeWarps = 8;
 
-__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p) {
-  __shared__ float4 part[kMergeWarps][32];
-  const int row = blockIdx.x;
-  const int v = blockIdx.y * 32 + threadIdx.x % 32;  // float4 index in the row
+template <int VPL>
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p, int W) {
+  extern __shared__ float4 part[];  // [kMergeWarps][VPL * 32] when W > 1
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  int n = p.max_splits;
-  if (p.n_splits) {
-    n = p.n_splits[row];
-  } else if (p.seq_lens) {
-    const int len = p.seq_lens[row / p.rows_per_seq];
-    n = len > 0 ? (len + p.chunk - 1) / p.chunk : 0;
-  }
-  n = max(0, min(n, p.max_splits));
-  const float* lrow = p.lse_part + static_cast<size_t>(row) * p.max_splits;
-  float m = -INFINITY;
-  for (int s = lane; s < n; s += 32) m = fmaxf(m, lrow[s]);
+  const int rows_per_cta = kMergeWarps / W;
+  const int row = blockIdx.x * rows_per_cta + warp / W;
+  const int k = warp % W;  // this warp's share of the row's parts
+  const bool live = row < p.rows;
+  const int nv = p.D / 4;  // float4 per row
+  float4 acc[VPL];
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float sum = 0.f;
-  if (m != -INFINITY)
-    for (int s = lane; s < n; s += 32) sum += exp2_approx((lrow[s] - m) * kLog2e);
+  for (int j = 0; j < VPL; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lse = -INFINITY;
+  if (live) {
+    int n = p.max_splits;
+    if (p.n_splits) {
+      n = p.n_splits[row];
+    } else if (p.seq_lens) {
+      const int len = p.seq_lens[row / p.rows_per_seq];
+      n = len > 0 ? (len + p.chunk - 1) / p.chunk : 0;
+    }
+    n = max(0, min(n, p.max_splits));
+    const float* lrow = p.lse_part + static_cast<size_t>(row) * p.max_splits;
+    float m = -INFINITY;
+    for (int s = lane; s < n; s += 32) m = fmaxf(m, lrow[s]);
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  const float lse = (m == -INFINITY) ? -INFINITY : m + logf(sum);
-  const float* orow = p.o_part + static_cast<size_t>(row) * p.max_splits * p.D;
-  const bool in_row = v < p.D / 4;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (in_row && m != -INFINITY) {
+    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float sum = 0.f;
+    if (m != -INFINITY)
+      for (int s = lane; s < n; s += 32) sum += exp2_approx((lrow[s] - m) * kLog2e);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    lse = (m == -INFINITY) ? -INFINITY : m + logf(sum);
+    if (m != -INFINITY) {
+      const float4* orow = reinterpret_cast<const float4*>(p.o_part + static_cast<size_t>(row) * p.max_splits * p.D);
 #pragma unroll 4
-    for (int s = warp; s < n; s += kMergeWarps) {
-      const float ls = lrow[s];
-      const float w = (ls == -INFINITY) ? 0.f : exp2_approx((ls - lse) * kLog2e);
-      const float4 x = reinterpret_cast<const float4*>(orow + static_cast<size_t>(s) * p.D)[v];
-      acc.x = fmaf(w, x.x, acc.x);
-      acc.y = fmaf(w, x.y, acc.y);
-      acc.z = fmaf(w, x.z, acc.z);
-      acc.w = fmaf(w, x.w, acc.w);
-    }
-  }
-  part[warp][lane] = acc;
-  __syncthreads();
-  if (warp == 0 && in_row) {
-    float4 t = part[0][lane];
+      for (int s = k; s < n; s += W) {
+        const float ls = lrow[s];
+        const float w = (ls == -INFINITY) ? 0.f : exp2_approx((ls - lse) * kLog2e);
+        const float4* src = orow + static_cast<size_t>(s) * nv;
 #pragma unroll
-    for (int w = 1; w < kMergeWarps; ++w) {
-      t.x += part[w][lane].x;
-      t.y += part[w][lane].y;
-      t.z += part[w][lane].z;
-      t.w += part[w][lane].w;
+        for (int j = 0; j < VPL; ++j) {
+          const int v = lane + 32 * j;
+          if (v < nv) {
+            const float4 x = src[v];
+            acc[j].x = fmaf(w, x.x, acc[j].x);
+            acc[j].y = fmaf(w, x.y, acc[j].y);
+            acc[j].z = fmaf(w, x.z, acc[j].z);
+            acc[j].w = fmaf(w, x.w, acc[j].w);
+          }
+        }
+      }
     }
-    store4(p.out, p.out_dtype, static_cast<size_t>(row) * p.D + 4 * v, t);
   }
-  if (threadIdx.x == 0 && blockIdx.y == 0 && p.lse) p.lse[row] = lse;
+  if (W > 1) {
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) part[warp * (VPL * 32) + j * 32 + lane] = acc[j];
+    __syncthreads();
+    if (k != 0) return;
+    for (int w2 = 1; w2 < W; ++w2) {
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) {
+        const float4 t = part[(warp + w2) * (VPL * 32) + j * 32 + lane];
+        acc[j].x += t.x;
+        acc[j].y += t.y;
+        acc[j].z += t.z;
+        acc[j].w += t.w;
+      }
+    }
+  }
+  if (!live) return;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int v = lane + 32 * j;
+    if (v < nv) store4(p.out, p.out_dtype, static_cast<size_t>(row) * p.D + 4 * v, acc[j]);
+  }
+  if (lane == 0 && p.lse) p.lse[row] = lse;
 }
 
 __global__ void f32_to_f16_kernel(const float* __restrict__ src, __half* __restrict__ dst, size_t n) {
@@ -100,8 +125,17 @@ __global__ void f32_to_f16_kernel(const float* __restrict__ src, __half* __restr
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   if (p.rows <= 0) return cudaSuccess;
   if (p.D > 512 || p.D % 4 != 0) return cudaErrorInvalidValue;
-  dim3 grid(p.rows, (p.D + kChunkCols - 1) / kChunkCols);
-  merge_kernel<<<grid, kMergeWarps * 32, 0, stream>>>(p);
+  const int W = p.max_splits <= 8 ? 1 : p.max_splits <= 16 ? 2 : p.max_splits <= 32 ? 4 : 8;
+  const int rows_per_cta = kMergeWarps / W;
+  const unsigned grid = static_cast<unsigned>((p.rows + rows_per_cta - 1) / rows_per_cta);
+  const int vpl = (p.D / 4 + 31) / 32;
+  const size_t smem = W > 1 ? static_cast<size_t>(kMergeWarps) * vpl * 32 * sizeof(float4) : 0;
+  switch (vpl) {
+    case 1: merge_kernel<1><<<grid, kMergeWarps * 32, smem, stream>>>(p, W); break;
+    case 2: merge_kernel<2><<<grid, kMergeWarps * 32, smem, stream>>>(p, W); break;
+    case 3: merge_kernel<3><<<grid, kMergeWarps * 32, smem, stream>>>(p, W); break;
+    default: merge_kernel<4><<<grid, kMergeWarps * 32, smem, stream>>>(p, W); break;
+  }
   return cudaGetLastError();
 }
 

@@ -12,7 +12,10 @@ from tests._guard import Guarded
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("rows,S,D", [(37, 5, 128), (8, 40, 512), (3, 1, 64)])
+# (rows, parts, D): one to eight warps per row (parts <= 8, 16, 32, more), one to four 16-byte
+# vectors per lane, D not a multiple of 128, row counts that leave a CTA partly empty.
+@pytest.mark.parametrize("rows,S,D", [(37, 5, 128), (8, 40, 512), (3, 1, 64), (21, 12, 256),
+                                      (9, 30, 384), (5, 150, 100), (50, 16, 200), (17, 8, 4)])
 def test_merge_parity(rows, S, D):
     g = torch.Generator().manual_seed(rows * S)
     o = torch.randn(rows, S, D, generator=g)
@@ -34,3 +37,19 @@ def test_merge_parity(rows, S, D):
     og.assert_intact("merge out")
     lg.assert_intact("merge lse")
     check(out, lse_g, ro, rl, max_err=1e-5, mean_err=1e-6, lse_err=1e-5, what="merge")
+
+
+def test_merge_bf16_output():
+    rows, S, D = 33, 9, 128
+    g = torch.Generator().manual_seed(5)
+    o = torch.randn(rows, S, D, generator=g)
+    lse = torch.randn(rows, S, generator=g) * 3
+    ro, rl = oracle.merge(o, lse)
+    og, lg = Guarded((rows, D), torch.bfloat16), Guarded((rows,), torch.float32)
+    out, lse_g = fa.fa_merge_states(o.cuda(), lse.cuda(), None, out_dtype=torch.bfloat16,
+                                    out=og.view, lse=lg.view)
+    torch.cuda.synchronize()
+    og.assert_intact("merge out")
+    lg.assert_intact("merge lse")
+    assert out.dtype == torch.bfloat16
+    check(out, lse_g, ro, rl, what="merge bf16")
