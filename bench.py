@@ -428,9 +428,13 @@ def bench_mla(fa, c, steps, warmup, flush, dist, pk):
                                    lse_parts=ol)
 
     b = mla_bytes(c)
-    # One chunk per sequence: the call is the MLA kernel alone, writing the final output;
-    # otherwise the kernel (timed on its own through the states entry point) plus a merge.
+    # One chunk per sequence: the MLA kernel writes the final output.  When that leaves a
+    # short last wave, the call also cuts that wave's sequences into chunks and merges them
+    # (a second, small launch); the roofline then takes the whole call's time, merge
+    # included.  Otherwise: the kernel (timed on its own through the states entry point)
+    # plus a merge.
     direct = n_chunks == 1
+    tail_split = direct and ws.numel() > 0
     ms_f, _, mode = time_graph(full, steps, warmup, flush, dist)
     f_ms = dist.max(statistics.mean(ms_f))
     if direct:
@@ -440,7 +444,8 @@ def bench_mla(fa, c, steps, warmup, flush, dist, pk):
         k_ms = dist.max(statistics.mean(ms_k))
     res = {"value": round(b["total"] / (f_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
            "ms": round(f_ms, 4), "bytes": b["total"], "chunk": chunk, "mode": mode,
-           "launches_per_step": 1 if direct else 2,
+           "launches_per_step": 1 if direct and not tail_split else 2,
+           "last_wave_split": tail_split,
            # the direct launch also writes the output; the states launch is counted by its
            # reads only
            "roofline": roofline("hbm", b["total" if direct else "kernel"] / (k_ms * 1e-3) / 1e9,

@@ -536,15 +536,16 @@ int check_mla(const void* q_nope, const void* q_pe, const void* ckv_pages, const
 
 cudaError_t mla_states(const void* q_nope, const void* q_pe, const void* ckv_pages,
                        const void* kpe_pages, const int32_t* page_table, const int32_t* seq_lens,
-                       float* o_part, float* lse_part, int chunk, int n_chunks, int B, int H,
+                       float* o_part, float* lse_part, const MlaPlan& pl, int B, int H,
                        int Dc, int Dr, int page_size, int max_pages_per_seq, int num_pages,
-                       float scale, uint32_t* status, cudaStream_t st, void* direct_out = nullptr,
-                       float* direct_lse = nullptr, bool f16 = false) {
+                       float scale, uint32_t* status, cudaStream_t st, void* out = nullptr,
+                       float* lse = nullptr, bool f16 = false) {
   MlaParams p{};
   p.f16 = f16 ? 1 : 0;
-  p.direct = direct_out != nullptr;
-  p.out = direct_out;
-  p.lse = direct_lse;
+  p.n_whole = pl.n_whole;
+  p.whole_chunk = pl.whole_chunk;
+  p.out = out;
+  p.lse = lse;
   p.q_nope = q_nope;
   p.q_pe = q_pe;
   p.ckv = ckv_pages;
@@ -558,8 +559,8 @@ cudaError_t mla_states(const void* q_nope, const void* q_pe, const void* ckv_pag
   p.page_size = page_size;
   p.max_pages = max_pages_per_seq;
   p.num_pages = num_pages;
-  p.chunk = chunk;
-  p.n_chunks = n_chunks;
+  p.chunk = pl.chunk;
+  p.n_chunks = pl.n_chunks;
   p.scale_log2 = scale * 1.44269504088896340736f;
   p.o_part = o_part;
   p.lse_part = lse_part;
@@ -671,8 +672,9 @@ int fa_decode_paged_states(const void* q, const void* k_pages, const void* v_pag
 
 size_t mla_decode_workspace_size(int B, int H, int Dc, int max_seq_len) {
   if (B <= 0 || H <= 0 || Dc <= 0 || max_seq_len <= 0) return 0;
-  const int chunk = mla_chunk_tokens(B, H, max_seq_len);
-  return split_ws_bytes((long)B * H, (max_seq_len + chunk - 1) / chunk, Dc);
+  const MlaPlan pl = mla_plan(B, H, max_seq_len);
+  if (pl.n_whole >= B) return 0;
+  return split_ws_bytes((long)(B - pl.n_whole) * H, pl.n_chunks, Dc);
 }
 
 int mla_decode_chunk_tokens(int B, int H, int max_seq_len) {
@@ -690,9 +692,15 @@ int mla_decode_paged_ex(const mla_decode_args* a, void* stream) {
   if (rc != FA_OK || B == 0) return rc;
   if (!a->out || !aligned16(a->out))
     return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: out must be a 16-byte aligned pointer");
-  const int chunk = mla_chunk_tokens(B, H, max_seq_len > 0 ? max_seq_len : 1);
-  const int n_chunks = max_seq_len > 0 ? (max_seq_len + chunk - 1) / chunk : 0;
-  const size_t need = n_chunks > 0 ? split_ws_bytes((long)B * H, n_chunks, Dc) : 0;
+  if (max_seq_len == 0) {
+    // no sequence holds a key: every row is empty (out 0, lse -inf)
+    return merge_chunks(nullptr, nullptr, a->seq_lens, H, 1, 0, a->out, a->lse, B * H, Dc,
+                        static_cast<cudaStream_t>(stream), "mla_decode_paged (merge kernel)",
+                        a->dtype == FA_FP16 ? Dtype::FP16 : Dtype::BF16);
+  }
+  const MlaPlan pl = mla_plan(B, H, max_seq_len);
+  const int n_split = B - pl.n_whole;  // sequences cut into chunks
+  const size_t need = n_split > 0 ? split_ws_bytes((long)n_split * H, pl.n_chunks, Dc) : 0;
   if (need > 0 && (!a->workspace || a->workspace_bytes < need))
     return fail(FA_ERR_WORKSPACE, "mla_decode_paged: workspace of %zu bytes needed (got %zu)", need,
                 a->workspace ? a->workspace_bytes : (size_t)0);
@@ -703,25 +711,21 @@ int mla_decode_paged_ex(const mla_decode_args* a, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool f16 = a->dtype == FA_FP16;
   float *o_part = nullptr, *lse_part = nullptr;
-  if (n_chunks == 1) {
-    // every sequence fits one chunk: the kernel writes the final output, no merge
-    cudaError_t e = mla_states(a->q_nope, a->q_pe, a->ckv_pages, a->kpe_pages, a->page_table,
-                               a->seq_lens, nullptr, nullptr, chunk, 1, B, H, Dc, a->Dr,
-                               a->page_size, a->max_pages_per_seq, a->num_pages, a->scale,
-                               status, st, a->out, a->lse, f16);
-    if (e != cudaSuccess) return cuda_fail("mla_decode_paged (MLA kernel)", e);
-    return FA_OK;
-  }
-  if (n_chunks > 0) {
-    carve(a->workspace, (long)B * H, n_chunks, Dc, &o_part, &lse_part);
-    cudaError_t e = mla_states(a->q_nope, a->q_pe, a->ckv_pages, a->kpe_pages, a->page_table,
-                               a->seq_lens, o_part, lse_part, chunk, n_chunks, B, H, Dc, a->Dr,
-                               a->page_size, a->max_pages_per_seq, a->num_pages, a->scale,
-                               status, st, nullptr, nullptr, f16);
-    if (e != cudaSuccess) return cuda_fail("mla_decode_paged (MLA kernel)", e);
-  }
-  return merge_chunks(o_part, lse_part, a->seq_lens, H, chunk, n_chunks, a->out, a->lse, B * H, Dc,
-                      st, "mla_decode_paged (merge kernel)", f16 ? Dtype::FP16 : Dtype::BF16);
+  if (n_split > 0) carve(a->workspace, (long)n_split * H, pl.n_chunks, Dc, &o_part, &lse_part);
+  // one launch: whole sequences write their final rows, the others their chunks' states
+  cudaError_t e = mla_states(a->q_nope, a->q_pe, a->ckv_pages, a->kpe_pages, a->page_table,
+                             a->seq_lens, o_part, lse_part, pl, B, H, Dc, a->Dr, a->page_size,
+                             a->max_pages_per_seq, a->num_pages, a->scale, status, st, a->out,
+                             a->lse, f16);
+  if (e != cudaSuccess) return cuda_fail("mla_decode_paged (MLA kernel)", e);
+  if (n_split == 0) return FA_OK;
+  // merge the split sequences' rows, which follow the whole ones in out, lse and seq_lens
+  const size_t row0 = (size_t)pl.n_whole * H;
+  void* out_split = static_cast<uint8_t*>(a->out) + row0 * Dc * 2;
+  float* lse_split = a->lse ? a->lse + row0 : nullptr;
+  return merge_chunks(o_part, lse_part, a->seq_lens + pl.n_whole, H, pl.chunk, pl.n_chunks,
+                      out_split, lse_split, n_split * H, Dc, st, "mla_decode_paged (merge kernel)",
+                      f16 ? Dtype::FP16 : Dtype::BF16);
 }
 
 int mla_decode_paged(const void* q_nope, const void* q_pe, const void* ckv_pages,
@@ -753,10 +757,13 @@ int mla_decode_paged_states(const void* q_nope, const void* q_pe, const void* ck
     return fail(FA_ERR_INVALID_ARG, "mla_decode_paged_states: o_parts/lse_parts missing or misaligned");
   uint32_t* status = device_status_ptr();
   if (!status) return fail(FA_ERR_CUDA, "mla_decode_paged_states: no usable CUDA device");
+  MlaPlan pl{};
+  pl.n_whole = 0;
+  pl.chunk = chunk;
+  pl.n_chunks = n_chunks;
   cudaError_t e = mla_states(q_nope, q_pe, ckv_pages, kpe_pages, page_table, seq_lens, o_parts,
-                             lse_parts, chunk, n_chunks, B, H, Dc, Dr, page_size,
-                             max_pages_per_seq, num_pages, scale, status,
-                             static_cast<cudaStream_t>(stream));
+                             lse_parts, pl, B, H, Dc, Dr, page_size, max_pages_per_seq, num_pages,
+                             scale, status, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail("mla_decode_paged_states", e);
   return FA_OK;
 }

@@ -79,13 +79,17 @@ struct MlaParams {
   const int32_t* page_table;
   const int32_t* seq_lens;
   int B, H, Dc, Dr, page_size, max_pages, num_pages;
+  // Sequences [0, n_whole) take one CTA each (up to whole_chunk tokens) and write the final
+  // out/lse directly.  Sequences [n_whole, B) are cut into n_chunks chunks of `chunk` tokens
+  // whose partial states go to o_part/lse_part, rows counted from sequence n_whole.  The grid
+  // is one-dimensional: n_whole + (B - n_whole) * n_chunks CTAs, the whole sequences first.
+  int n_whole, whole_chunk;
   int chunk, n_chunks;
   float scale_log2;
-  float* o_part;          // [B*H, n_chunks, Dc]
-  float* lse_part;        // [B*H, n_chunks]
-  int direct;             // n_chunks == 1: write out/lse directly, no partial states
-  void* out;              // [B,H,Dc] in the inputs' type (direct mode)
-  float* lse;             // [B,H] or nullptr (direct mode)
+  float* o_part;          // [(B - n_whole)*H, n_chunks, Dc]
+  float* lse_part;        // [(B - n_whole)*H, n_chunks]
+  void* out;              // [B,H,Dc] in the inputs' type (whole sequences)
+  float* lse;             // [B,H] or nullptr (whole sequences)
   uint32_t* status;
   int f16;                // q, ckv and kpe are fp16 (else bf16)
 };
@@ -94,6 +98,12 @@ cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream);
 // Self-test of the bounded-wait failure path (selftest.cu).
 cudaError_t launch_selftest_wait(uint64_t limit_ns, uint32_t* status, cudaStream_t stream);
 int mla_chunk_tokens(int B, int H, int max_seq_len);
+// Plan of a full MLA call (see MlaParams): n_whole whole sequences of up to whole_chunk
+// tokens, the rest in n_chunks chunks of `chunk` tokens.
+struct MlaPlan {
+  int n_whole, whole_chunk, chunk, n_chunks;
+};
+MlaPlan mla_plan(int B, int H, int max_seq_len);
 
 // ---------------------------------------------------------------------------------------
 // Merge of split states

@@ -103,16 +103,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* stat_s = alpha_s + 64;  // [0..63]: l per head (epilogue)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int c = blockIdx.x, b = blockIdx.y;
+  // whole sequences first, then the chunks of the split ones
+  const int bx = blockIdx.x;
+  const bool direct = bx < p.n_whole;
+  const int b = direct ? bx : p.n_whole + (bx - p.n_whole) / p.n_chunks;
+  const int c = direct ? 0 : (bx - p.n_whole) % p.n_chunks;
+  const int chunk = direct ? p.whole_chunk : p.chunk;
   const int len = p.seq_lens[b];
   if (len < 0 || len > p.max_pages * p.page_size) {
     if (threadIdx.x == 0) record_error(p.status, kDevBounds);
     return;
   }
-  const int t_start = c * p.chunk;
+  const int t_start = c * chunk;
   if (t_start >= len) {
     // an empty sequence still owns its final output when this launch writes it directly
-    if (p.direct && c == 0) {
+    if (direct) {
       for (int i = threadIdx.x; i < kH * kDc / 8; i += kThreads)
         reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + static_cast<size_t>(b) * kH * kDc)[i] =
             make_uint4(0, 0, 0, 0);
@@ -120,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     return;
   }
-  const int t_stop = min(len, t_start + p.chunk);
+  const int t_stop = min(len, t_start + chunk);
   const int n_tiles = (t_stop - t_start + kTile - 1) / kTile;
   const int n_stages = 2 * n_tiles;  // every tile is two 32-token stages
 
@@ -444,12 +449,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     softmax_sync();
     if (ok) {
-      const size_t row0 = static_cast<size_t>(b) * kH;
+      const size_t row0 = static_cast<size_t>(b) * kH;                 // output rows
+      const size_t prow0 = static_cast<size_t>(b - p.n_whole) * kH;    // partial-state rows
 #pragma unroll 1
       for (int r = 0; r < 16; ++r) {
         const int hh = warp * 16 + r;
         const float4* src = reinterpret_cast<const float4*>(ostage + hh * kDc);
-        if (p.direct) {
+        if (direct) {
           // the whole sequence was this CTA's chunk: write the final bf16 row
           uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + (row0 + hh) * kDc);
 #pragma unroll
@@ -462,14 +468,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   pack_f16x2(b2.x, b2.y), pack_f16x2(b2.z, b2.w));
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(p.o_part + ((row0 + hh) * p.n_chunks + c) * kDc);
+          float4* dst = reinterpret_cast<float4*>(p.o_part + ((prow0 + hh) * p.n_chunks + c) * kDc);
 #pragma unroll
           for (int k = 0; k < kDc / 4 / 32; ++k) dst[lane + 32 * k] = src[lane + 32 * k];
         }
       }
       if (lead) {
         const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-        if (!p.direct) p.lse_part[(row0 + h) * p.n_chunks + c] = lse_v;
+        if (!direct) p.lse_part[(prow0 + h) * p.n_chunks + c] = lse_v;
         else if (p.lse) p.lse[row0 + h] = lse_v;
       }
     }
@@ -504,10 +510,49 @@ int mla_chunk_tokens(int B, int, int max_seq_len) {
   return best;
 }
 
+// The plan of a full MLA call.  With several chunks per sequence every sequence is split.
+// With one, every sequence is one CTA writing its final output, unless the last wave of
+// CTAs would be at most half full: then the sequences of that wave are cut into chunks that
+// together fill it (whole sequences are dispatched first), so the call ends after a short
+// wave instead of a full-length one, and only those sequences' rows are merged.
+MlaPlan mla_plan(int B, int H, int max_seq_len) {
+  MlaPlan pl{};
+  const int chunk = mla_chunk_tokens(B, H, max_seq_len);
+  const int n_chunks = max_seq_len > 0 ? (max_seq_len + chunk - 1) / chunk : 0;
+  if (n_chunks != 1) {
+    pl.n_whole = 0;
+    pl.chunk = chunk;
+    pl.n_chunks = n_chunks;
+    return pl;
+  }
+  pl.n_whole = B;
+  pl.whole_chunk = chunk;
+  pl.chunk = chunk;
+  pl.n_chunks = 1;
+  const int sms = num_sms() > 0 ? num_sms() : 148;
+  const int waves = (B + sms - 1) / sms;
+  const int tail = B - (waves - 1) * sms;  // sequences in the last wave
+  if (waves >= 2 && 2 * tail <= sms) {
+    const int k = sms / tail;
+    const int ct = ((max_seq_len + k - 1) / k + kTile - 1) / kTile * kTile;
+    const int kc = (max_seq_len + ct - 1) / ct;
+    if (kc >= 2) {
+      pl.n_whole = B - tail;
+      pl.chunk = ct;
+      pl.n_chunks = kc;
+    }
+  }
+  return pl;
+}
+
 cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream) {
-  if (p.H != kH || p.Dc != kDc || p.Dr != kDr || p.chunk % kTile != 0 || p.chunk > kMaxChunk)
+  if (p.H != kH || p.Dc != kDc || p.Dr != kDr || p.n_whole < 0 || p.n_whole > p.B)
     return cudaErrorInvalidValue;
-  if (p.direct && p.n_chunks != 1) return cudaErrorInvalidValue;
+  if (p.n_whole > 0 && (p.whole_chunk % kTile != 0 || p.whole_chunk > kMaxChunk))
+    return cudaErrorInvalidValue;
+  if (p.n_whole < p.B &&
+      (p.n_chunks < 1 || p.chunk % kTile != 0 || p.chunk > kMaxChunk || !p.o_part || !p.lse_part))
+    return cudaErrorInvalidValue;
   CUtensorMap tqn, tqp;
   const uint64_t qrows = static_cast<uint64_t>(p.B) * kH;
   const CUtensorMapDataType dt = p.f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -530,7 +575,10 @@ cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream) {
   auto kern = p.f16 ? mla_kernel<false> : mla_kernel<true>;
   cudaError_t e = ensure_smem_limit(kern, kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_chunks, p.B);
+  const long ctas = p.n_whole + static_cast<long>(p.B - p.n_whole) * (p.n_whole < p.B ? p.n_chunks : 0);
+  if (ctas <= 0) return cudaSuccess;
+  if (ctas > 0x7fffffffL) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(ctas));
   kern<<<grid, kThreads, kSmemBytes, stream>>>(tqn, tqp, p);
   return cudaGetLastError();
 }

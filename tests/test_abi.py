@@ -91,7 +91,12 @@ def test_workspace_sizes_are_consistent(lib):
     assert lib.fa_prefill_workspace_size(ctypes.byref(a)) >= 1 * 4 * 8 * 4 * (128 + 1) * 4
     assert lib.fa_decode_workspace_size(128, 32, 128, 4096) >= 128 * 32 * (128 + 1) * 4
     assert lib.fa_decode_workspace_size(0, 32, 128, 4096) == 0
-    assert lib.mla_decode_workspace_size(128, 64, 512, 2048) >= 128 * 64 * (512 + 1) * 4
+    # MLA: one chunk per sequence writes the output directly (no workspace); sequences split
+    # into chunks need partial states for their rows only
+    assert lib.mla_decode_workspace_size(128, 64, 512, 2048) == 0
+    assert lib.mla_decode_workspace_size(64, 64, 512, 2048) >= 64 * 64 * 2 * (512 + 1) * 4
+    tail = lib.mla_decode_workspace_size(768, 64, 512, 1024)  # a short last wave is split
+    assert 0 < tail < 768 * 64 * (512 + 1) * 4
 
 
 @pytest.mark.parametrize("args,code", [

@@ -52,6 +52,20 @@ def test_parity_shapes(lens, ps):
     check(out, lse, ro, rl, what=f"mla {lens} ps={ps}")
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_short_last_wave_is_split(dtype):
+    """More sequences than SMs, one chunk each: the sequences of the short last wave are cut
+    into chunks and merged, the others written directly.  The cut ones include an empty
+    sequence and lengths around the 64-token tile and the chunk."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tail = [0, 1, 63, 64, 65, 129, 130, 100]
+    lens = [130 - (i % 7) for i in range(sms)] + tail
+    c = workloads.MlaCase(B=len(lens), H=64, seq_len=None, seq_lens=lens, dtype=dtype, seed=3)
+    assert fa.load_library().mla_decode_workspace_size(c.B, c.H, c.Dc, c.max_len) > 0
+    out, lse, ro, rl = _run(c)
+    check(out, lse, ro, rl, what=f"mla short last wave {dtype}")
+
+
 @pytest.mark.parametrize("batch,seq", [(128, 2048), (768, 1024), (64, 1024), (64, 2048),
                                        (128, 1024), (768, 2048)])
 def test_mla_full_size_sampled(batch, seq):
