@@ -205,6 +205,10 @@ int mla_decode_paged(const void* q_nope, const void* q_pe, const void* ckv_pages
                      int max_pages_per_seq, int num_pages, int max_seq_len, float scale,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* Workspace bytes mla_decode_paged needs on the current device: partial states for the
+ * sequences it cuts into chunks.  0 when every sequence is one chunk written directly; when
+ * there are more sequences than SMs and the last wave of CTAs would be at most half full,
+ * only that wave's sequences are cut (and merged), the others written directly. */
 size_t mla_decode_workspace_size(int B, int H, int Dc, int max_seq_len);
 
 /* mla_decode_paged with the element type as an argument: the same fields, plus dtype
@@ -227,7 +231,8 @@ typedef struct mla_decode_args {
 
 int mla_decode_paged_ex(const mla_decode_args* args, void* stream);
 
-/* Tokens per split-KV chunk that mla_decode_paged uses (a multiple of the kernel's tile). */
+/* Tokens per split-KV chunk of mla_decode_paged_states (a multiple of the kernel's tile);
+ * mla_decode_paged uses it too, except for the sequences of a split last wave. */
 int mla_decode_chunk_tokens(int B, int H, int max_seq_len);
 
 /* mla_decode_paged without the final merge (same contract as fa_decode_paged_states):

@@ -14,15 +14,18 @@
 // 64-column blocks, written at their swizzled addresses by the copying threads.  Like the flashinfer design the ring is shared by the
 // K and V roles (one pipeline, small tiles, several stages in flight), but the MMAs are
 // Blackwell's:
-//   S  = Q [64 heads x 576] . KV^T         tcgen05 M=64 (heads), N=32 tokens, S in TMEM
+//   S  = Q [64 heads x 576] . KV^T         tcgen05 M=64 (heads), N=64 tokens (the two
+//                                           32-token stages of a tile), S in TMEM
 //   O^T += ckv^T [512 x tokens] . P^T       tcgen05 M=128 (latent dims, four blocks),
 //                                           N=64 heads, A = the same ckv stage read
 //                                           MN-major, B = P^T staged in shared memory
 // so O (64 x 512 fp32) lives in 256 tensor-memory columns as four 128-lane blocks and the
-// PV product runs at full tensor rate.  Softmax: one thread per head row (the M=64 S layout
-// puts heads 16q..16q+15 in lanes 32q..32q+15), online max/sum with O rescaled only when a
-// head's running max grows by more than 2^8.  The CTA writes the chunk's normalised partial
-// output and log-sum-exp; merge.cu combines chunks.
+// PV product runs at full tensor rate.  Softmax: two threads per head row (the M=64 S layout
+// puts heads 16q..16q+15 in lanes 32q..32q+15; lanes 32q+16.. take the second half of each
+// tile's tokens), online max/sum with O rescaled only when a head's running max grows by
+// more than 2^8.  A CTA that owns a whole sequence writes its final output and log-sum-exp;
+// one that owns a chunk writes the chunk's normalised partial output and log-sum-exp, and
+// merge.cu combines the chunks.
 //
 // Warp roles (288 threads): warps 0-3 softmax + epilogue, warps 4-7 producer (row ids and
 // cp.async gathers), warp 8 MMA issuer and tensor-memory owner.
@@ -257,9 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_f16(BF16, 64, kTile, false, false);
       constexpr uint32_t idesc_o = idesc_f16(BF16, 128, kH, true, false);
-      // S of tile j: two N=32 halves, one per stage, into S buffer j & 1
-      // (the two halves' accumulation chains are interleaved so the tensor core always
-      // has an independent MMA to start)
+      // S of tile j: one N=64 MMA per 16-column K step over its two stages (contiguous rows
+      // of every block in the block-major ring), into S buffer j & 1
       const uint64_t q_desc = sdesc_sw128(sQ, 16, 1024);
       const uint64_t kv_desc = sdesc_sw128(sKV, 16, 1024);
       const uint64_t kv_desc_mn = sdesc_sw128(sKV, kBlockStride, 1024);

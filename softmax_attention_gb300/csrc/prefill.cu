@@ -9,7 +9,9 @@
 // "perf: FlashAttention-3 style MLA PageAttention", change list items 1-3), rebuilt for
 // Blackwell: TMA loads into a multi-stage shared-memory ring, tcgen05.mma accumulating in
 // tensor memory, S/P double-buffered in tensor memory with P (16-bit) written over S, and O
-// resident in tensor memory for the whole KV loop.
+// resident in tensor memory for the whole KV loop.  The paged instantiation reads K/V
+// through a page table (chunked prefill against a paged cache): each page of a KV tile is
+// one 5-D TMA box, and each sequence has its own length.
 //
 // Warp roles (192 threads): warps 0-3 softmax + epilogue (thread t owns row t), warp 4 TMA
 // producer, warp 5 MMA issuer (one elected thread) and tensor-memory owner.
