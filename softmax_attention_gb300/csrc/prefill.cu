@@ -26,6 +26,7 @@ namespace {
 
 using prefill::kRows;
 constexpr int kThreads = 192;
+constexpr int kLptMaxSeqs = 64;  // paged: order sequences by length when there are at most this many
 
 // 5-D tiled TMA load (the paged K/V boxes below).
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
@@ -90,7 +91,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- work item: (query tile, split) x kv head x batch; heavier (later) tiles first ----
   const int split = blockIdx.x % p.n_splits;
   const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x) / p.n_splits;
-  const int hk = blockIdx.y, b = blockIdx.z;
+  const int hk = blockIdx.y;
+  int b = blockIdx.z;
+  if constexpr (PAGED) {
+    // Sequences have different lengths: hand them out longest first (blockIdx.z is a rank
+    // in decreasing length, ties by index), so the last CTAs to start are short ones.
+    // Thread i ranks sequence i; the one whose rank is this CTA's publishes its index.
+    __shared__ int lpt_seq;
+    if (p.B <= kLptMaxSeqs) {
+      if (threadIdx.x < p.B) {
+        const int li = p.kv_lens[threadIdx.x];
+        int rank = 0;
+        for (int j = 0; j < p.B; ++j) {
+          const int lj = p.kv_lens[j];
+          rank += (lj > li || (lj == li && j < static_cast<int>(threadIdx.x))) ? 1 : 0;
+        }
+        if (rank == static_cast<int>(blockIdx.z)) lpt_seq = threadIdx.x;
+      }
+      __syncthreads();
+      b = lpt_seq;
+    }
+  }
   const int q0 = qt * p.q_per_tile;
   const int q_last = min(p.Lq, q0 + p.q_per_tile) - 1;
   // keys of this sequence: dense Lkv, or the sequence's length in the paged cache
