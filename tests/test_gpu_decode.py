@@ -54,6 +54,9 @@ CASES = [
     (3, 8, 1, 64, 64, [64, 65, 2000]),    # G = 8, D = 64
     (2, 4, 2, 128, 8, [9, 100]),          # pages smaller than a 16-token block
     (2, 4, 2, 128, 1, [3, 40]),           # page_size 1
+    (2, 16, 1, 64, 16, [200, 33]),        # G = 16
+    (2, 4, 2, 256, 4, [50, 17]),          # G = 2, D = 256, 4-token pages
+    (1, 8, 4, 128, 256, [600]),           # pages larger than a 16-token block
 ]
 
 

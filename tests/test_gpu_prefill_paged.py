@@ -54,6 +54,9 @@ CASES = [
     (2, 8, 2, 30, [515, 90], 256, 8, True),            # D = 256, eight pages a tile
     (1, 4, 1, 20, [300], 128, 8, False),               # 8-key pages, one row group each
     (2, 8, 4, 10, [260, 129], 64, 128, True),          # D = 64, a page per tile
+    (4, 8, 2, 24, [500, 500, 200, 500], 128, 16, True),  # equal lengths (ties in the order)
+    (70, 4, 2, 3, [(37 * i) % 300 + 1 for i in range(70)], 64, 8, True),  # > 64 sequences:
+                                                        # no longest-first order
 ]
 
 
