@@ -364,6 +364,8 @@ def bench_decode(fa, c, steps, warmup, flush, dist, pk):
 
 
 MLA_GRID = ((128, 2048), (768, 1024), (64, 1024), (64, 2048), (128, 1024), (768, 2048))
+# the configured pair again with 64-token pages (page-sized TMA copies instead of row gathers)
+MLA_PAGED = ((128, 2048, 64), (768, 1024, 64))
 
 
 def bench_prefill_paged(fa, c, steps, warmup, flush, dist, pk):
@@ -450,7 +452,9 @@ def bench_mla(fa, c, steps, warmup, flush, dist, pk):
            # reads only
            "roofline": roofline("hbm", b["total" if direct else "kernel"] / (k_ms * 1e-3) / 1e9,
                                 pk["hbm"], "GB/s",
-                                profiled_traffic(f"mla_decode_b{c.B}_s{c.seq_len}.md", "mla"), pk),
+                                profiled_traffic(f"mla_decode_b{c.B}_s{c.seq_len}"
+                                                 + (f"_ps{c.page_size}" if c.page_size > 1 else "")
+                                                 + ".md", "mla"), pk),
            "kernel_ms": round(k_ms, 4)}
     del qnd, qpd, cd, kd, td, ld, out, lse, ws, op, ol
     torch.cuda.empty_cache()
@@ -571,13 +575,14 @@ def main():
                 paths["paged_gqa_prefill"] = bench_prefill_paged(fa, ppc, sub, args.warmup, flush,
                                                                  dist, pk)
             # the MLA grid of the flashinfer PR's results: batch {64, 128, 768} x {1024, 2048}
-            for batch, seq in (MLA_GRID if want("mla") else ()):
-                mc = workloads.mla_decode(batch, seq, seed=1 + dist.rank)
+            mla_points = [(b_, s_, 1) for b_, s_ in MLA_GRID] + list(MLA_PAGED)
+            for batch, seq, ps in (mla_points if want("mla") else ()):
+                mc = workloads.mla_decode(batch, seq, seed=1 + dist.rank, page_size=ps)
+                key = f"mla_decode_b{batch}_s{seq}" + (f"_ps{ps}" if ps > 1 else "")
                 try:
-                    paths[f"mla_decode_b{batch}_s{seq}"] = bench_mla(fa, mc, sub, args.warmup,
-                                                                      flush, dist, pk)
+                    paths[key] = bench_mla(fa, mc, sub, args.warmup, flush, dist, pk)
                 except fa.FAError as e:
-                    paths[f"mla_decode_b{batch}_s{seq}"] = {"unavailable": str(e)}
+                    paths[key] = {"unavailable": str(e)}
             sweep = {}
             for lq in (workloads.MQA_SWEEP_LQ if want("mqa") else ()):
                 mc = workloads.mqa_prefill(lq, seed=1 + dist.rank)

@@ -92,6 +92,9 @@ struct MlaParams {
   float* lse;             // [B,H] or nullptr (whole sequences)
   uint32_t* status;
   int f16;                // q, ckv and kpe are fp16 (else bf16)
+  // 64 when page_size is a multiple of 64: a full 64-token tile is a slice of one page and is
+  // copied with TMA boxes; 0: every stage is gathered row by row.  Set by launch_mla.
+  int tma_rows;
 };
 cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream);
 

@@ -6,14 +6,15 @@
 //   s_t = scale * (q_nope . ckv_t + q_pe . kpe_t),   out = softmax(s) . ckv
 // with 64 query heads sharing one latent head (Dc = 512, Dr = 64).
 //
-// One CTA handles one chunk of one sequence's tokens.  Token rows are gathered through the
-// page table with 16-byte cp.async copies by a producer warpgroup (LDGSTS-style gathers, the
-// page_size=1 choice of the flashinfer PR's results section; measured on GB300 they move
-// these 1152-byte rows faster than TMA tile::gather4) into a ring of 32-token stages; each
-// stage holds the 576-wide [ckv | kpe] rows of its tokens as nine 128-byte-swizzled
-// 64-column blocks, written at their swizzled addresses by the copying threads.  Like the flashinfer design the ring is shared by the
-// K and V roles (one pipeline, small tiles, several stages in flight), but the MMAs are
-// Blackwell's:
+// One CTA handles one chunk of one sequence's tokens, streamed through a ring of 32-token
+// stages; each stage holds the 576-wide [ckv | kpe] rows of its tokens as nine
+// 128-byte-swizzled 64-column blocks.  With page_size 1 (the flashinfer PR's results section)
+// rows are gathered through the page table with 16-byte cp.async copies by a producer
+// warpgroup, written at their swizzled addresses (LDGSTS-style gathers; measured on GB300
+// they move these 1152-byte rows faster than TMA tile::gather4).  With pages of 8, 16 or a
+// multiple of 32 tokens a full stage is whole page slices, copied by 2-D TMA boxes into the
+// same layout.  Like the flashinfer design the ring is shared by the K and V roles (one
+// pipeline, small tiles, several stages in flight), but the MMAs are Blackwell's:
 //   S  = Q [64 heads x 576] . KV^T         tcgen05 M=64 (heads), N=64 tokens (the two
 //                                           32-token stages of a tile), S in TMEM
 //   O^T += ckv^T [512 x tokens] . P^T       tcgen05 M=128 (latent dims, four blocks),
@@ -55,13 +56,16 @@ constexpr float kLn2 = 0.69314718055994530942f;
 constexpr int kQBytes = kH * (kDc + kDr) * 2;    // 73728
 constexpr int kBlk = kHalf * 128;                // one 64-column block of one stage
 constexpr int kStageBytes = kBlocks * kBlk;      // 36864
-// The ring is laid out block-major, [9 blocks][4 stages][32 rows][128 B], so the two stages
-// of a tile (2t, 2t+1) are 64 contiguous rows in every block: one N=64 MMA covers a tile.
-constexpr int kBlockStride = kStages * kBlk;     // 16384
+// The ring holds two tiles, each [9 blocks][64 rows][128 B]: the two 32-token stages of tile
+// t (2t, 2t+1) are the first and second 32 rows of every block of ring tile t % 2, so one
+// N=64 MMA covers a tile, and a tile's eight ckv blocks are one dense 64 KB region.
+constexpr int kBlockStride = kTile * 128;        // 8192: block to block within a tile
+constexpr int kTileBytes = kBlocks * kBlockStride;  // 73728: ring tile to ring tile
 constexpr int kPBytes = kH * kTile * 2;          // 8192
 constexpr int kQOff = 0;
 constexpr int kKVOff = kQOff + kQBytes;
-constexpr int kPOff = kKVOff + kStages * kStageBytes;
+constexpr int kPOff = kKVOff + 2 * kTileBytes;
+static_assert(2 * kTileBytes == kStages * kStageBytes, "two tiles of two stages");
 constexpr int kBarOff = kPOff + kPBytes;
 // q_full, kv_full[S], kv_empty[S], s_full[2], p_full, o_full, mma_done
 constexpr int kNumBars = 1 + 2 * kStages + 2 + 3;
@@ -84,9 +88,16 @@ __device__ __forceinline__ bool softmax_any(bool v) {
 }
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// Adds `bytes` to the barrier's expected transaction count without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_kernel(const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qp,
+               const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
                const MlaParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -165,6 +176,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 4 * 32) {
       tma_prefetch_desc(&tm_qn);
       tma_prefetch_desc(&tm_qp);
+      if (p.tma_rows > 0) {
+        tma_prefetch_desc(&tm_ckv);
+        tma_prefetch_desc(&tm_kpe);
+      }
       mbar_arrive_expect_tx(bar_q, kQBytes);
       for (int kb = 0; kb < kDc / 64; ++kb)
         tma_load_2d(sQ + kb * (kH * 128), &tm_qn, bar_q, kb * 64, b * kH);
@@ -214,12 +229,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (can_issue) {
         const int n = issued;
-        const uint32_t dst = sKV + (n % kStages) * kBlk;
+        const uint32_t dst = sKV + ((n >> 1) & 1) * kTileBytes + (n & 1) * kBlk;  // stage n
         if ((n >> 2) != cur_group) {
           cur_group = n >> 2;
           row_cur = page_to_row(page_next, cur_group);
           page_next = load_page(cur_group + 1);
         }
+        // Pages of a multiple of 64 tokens: a full 64-token tile is a 64-row slice of one
+        // page, and its eight ckv blocks arrive as one 3-D TMA box (64 columns x 64 rows x 8
+        // blocks: whole 1 KB rows, landing block after block in the ring tile) plus one kpe
+        // box, both 128-byte swizzled like the gathers.  Every producer thread reads the
+        // tile's page id (the same address), so all agree on the path without talking.  At
+        // the tile's first stage one thread waits for the second stage's slot as well, puts
+        // the whole tile's bytes on the first stage's full barrier and issues the two boxes;
+        // the second stage issues nothing.  Everyone still arrives on both stages when
+        // publishing, as for gathered stages.  Partial tiles and bad page ids are gathered.
+        bool by_tma = false;
+        int tile_row = 0;
+        if (p.tma_rows > 0) {
+          const int t0 = t_start + kHalf * (n & ~1);
+          if (t0 + kTile <= t_stop) {
+            const int page = __ldg(table + t0 / p.page_size);
+            by_tma = page >= 0 && page < p.num_pages;
+            tile_row = page * p.page_size + t0 % p.page_size;
+          }
+        }
+        if (by_tma) {
+          if ((n & 1) == 0 && threadIdx.x == 4 * 32) {
+            if (n + 1 >= kStages)
+              mbar_wait(bar_empty((n + 1) % kStages), (((n + 1) / kStages) - 1) & 1, p.status);
+            const uint32_t full = bar_full(n % kStages);
+            mbar_expect_tx(full, 2 * kStageBytes);
+            tma_load_3d(dst, &tm_ckv, full, 0, tile_row, 0);
+            tma_load_2d(dst + (kDc / 64) * kBlockStride, &tm_kpe, full, 0, tile_row);
+          }
+        } else {
         const int rsel = row_cur;
 #pragma unroll
         for (int t8 = 0; t8 < 8; ++t8) {
@@ -240,7 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           cp_async_16(dst + (kDc / 64) * kBlockStride + tok * 128 + ((cc ^ (tok & 7)) * 16),
                       kpe + static_cast<size_t>(row) * (kDr * 2) + cc * 16);
         }
-        cp_async_commit();
+        }
+        cp_async_commit();  // an empty group for a TMA stage keeps the per-thread count
         ++issued;
         t_last = global_timer_ns();
       } else if (published < issued) {
@@ -250,6 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++published;
         t_last = global_timer_ns();
       } else if (global_timer_ns() - t_last > kWaitLimitNs) {
+        // Nothing moved for the whole limit: this thread's gathers are waited for below, and
+        // a TMA stage it issued (microseconds of copying) landed long before.
         record_error(p.status, kDevTimeout);
         break;
       }
@@ -267,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t kv_desc_mn = sdesc_sw128(sKV, kBlockStride, 1024);
       const uint64_t p_desc = sdesc_sw128(sP, 16, 1024);
       auto issue_s = [&](int j) {
-        const uint64_t b0 = sdesc_add(kv_desc, ((2 * j) % kStages) * kBlk);
+        const uint64_t b0 = sdesc_add(kv_desc, (j & 1) * kTileBytes);
         const uint32_t d0 = tmem + kTmemS + (j & 1) * kTile;
 #pragma unroll
         for (int kk = 0; kk < kBlocks * 4; ++kk) {
@@ -279,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // O^T += ckv^T P^T for tile j, then release its two stages
       auto issue_pv = [&](int j) {
-        const uint64_t kv = sdesc_add(kv_desc_mn, ((2 * j) % kStages) * kBlk);
+        const uint64_t kv = sdesc_add(kv_desc_mn, (j & 1) * kTileBytes);
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks) {
           const uint64_t bd = sdesc_add(p_desc, ks * 32);
@@ -547,7 +594,8 @@ MlaPlan mla_plan(int B, int H, int max_seq_len) {
   return pl;
 }
 
-cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream) {
+cudaError_t launch_mla(const MlaParams& params, cudaStream_t stream) {
+  MlaParams p = params;
   if (p.H != kH || p.Dc != kDc || p.Dr != kDr || p.n_whole < 0 || p.n_whole > p.B)
     return cudaErrorInvalidValue;
   if (p.n_whole > 0 && (p.whole_chunk % kTile != 0 || p.whole_chunk > kMaxChunk))
@@ -574,6 +622,22 @@ cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream) {
                       CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
+  // Tile-sized TMA copies (see the producer) when a page holds whole 64-token tiles.  The
+  // ckv map walks (64 columns, row, 64-column block) so a box of 64 x 64 x 8 lands as the
+  // tile's eight blocks one after another.
+  CUtensorMap tckv = tqn, tkpe = tqp;  // placeholders when every stage is gathered
+  const int ps = p.page_size;
+  p.tma_rows = (ps > 0 && ps % kTile == 0) ? kTile : 0;
+  if (p.tma_rows > 0) {
+    const uint64_t rows = static_cast<uint64_t>(p.num_pages) * ps;
+    const uint64_t dims_c[3] = {64, rows, kDc / 64}, str_c[2] = {kDc * 2, 128};
+    const uint32_t box_c[3] = {64, kTile, kDc / 64};
+    const uint64_t dims_r[2] = {kDr, rows}, str_r[1] = {kDr * 2};
+    const uint32_t box_r[2] = {64, kTile};
+    if (!encode_tiled(&tckv, dt, 3, p.ckv, dims_c, str_c, box_c, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled(&tkpe, dt, 2, p.kpe, dims_r, str_r, box_r, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   auto kern = p.f16 ? mla_kernel<false> : mla_kernel<true>;
   cudaError_t e = ensure_smem_limit(kern, kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -581,7 +645,7 @@ cudaError_t launch_mla(const MlaParams& p, cudaStream_t stream) {
   if (ctas <= 0) return cudaSuccess;
   if (ctas > 0x7fffffffL) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(ctas));
-  kern<<<grid, kThreads, kSmemBytes, stream>>>(tqn, tqp, p);
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(tqn, tqp, tckv, tkpe, p);
   return cudaGetLastError();
 }
 

@@ -44,6 +44,9 @@ def _run(c: workloads.MlaCase, rows=None):
     ([17, 300, 1030], 16),
     ([200, 64], 64),
     ([0, 100], 1),          # one chunk per sequence: final output written directly
+    ([40, 200, 31], 8),     # 8-token pages: four TMA page slices per stage
+    ([100, 500, 33], 32),   # a stage is one 32-token page
+    ([300, 129], 128),      # a stage is a slice of a page
 ])
 def test_parity_shapes(lens, ps):
     c = workloads.MlaCase(B=len(lens), H=64, seq_len=None, seq_lens=lens, page_size=ps,
@@ -74,6 +77,38 @@ def test_mla_full_size_sampled(batch, seq):
     rows = list(range(0, c.B * c.H, 97 if batch == 768 else 41))
     out, lse, ro, rl = _run(c, rows=rows)
     check(out, lse, ro, rl, what=f"mla b{batch} s{seq} (sampled)")
+
+
+@pytest.mark.parametrize("ps", [8, 16, 64])
+def test_page_copies_equal_row_gathers_bit_exact(ps):
+    """Full stages of pages >= 8 tokens are copied with TMA boxes, pages of one token are
+    gathered row by row; both fill the stage ring with the same bytes, so the same tokens
+    give bit-identical results either way."""
+    c = workloads.MlaCase(B=3, H=64, seq_len=None, seq_lens=[700, 1500, 65], page_size=ps,
+                          seed=ps)
+    qn, qp, ckv, kpe, table, lens = workloads.mla_inputs(c)
+    P = ckv.shape[0]
+    ckv1 = ckv.reshape(P * ps, 1, c.Dc)
+    kpe1 = kpe.reshape(P * ps, 1, c.Dr)
+    t = torch.arange(c.max_len)
+    table1 = torch.full((c.B, c.max_len), -1, dtype=torch.int32)
+    for b in range(c.B):
+        n = int(lens[b])
+        pages = table[b, (t[:n] // ps)].long()
+        table1[b, :n] = (pages * ps + t[:n] % ps).to(torch.int32)
+    o1, l1 = fa.mla_decode_paged(*[x.cuda() for x in (qn, qp, ckv, kpe, table, lens)],
+                                 c.max_len, c.scale)
+    o2, l2 = fa.mla_decode_paged(*[x.cuda() for x in (qn, qp, ckv1, kpe1, table1, lens)],
+                                 c.max_len, c.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_mla_64_token_pages_full_size_sampled():
+    c = workloads.mla_decode(128, 2048, page_size=64)
+    rows = list(range(0, c.B * c.H, 53))
+    out, lse, ro, rl = _run(c, rows=rows)
+    check(out, lse, ro, rl, what="mla b128 s2048 ps64 (sampled)")
 
 
 def test_paged_equals_dense_gathered_bit_exact():

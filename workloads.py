@@ -271,10 +271,11 @@ def paged_gqa_decode(seed: int = 1) -> PagedCase:
                      min_len=1024, max_len=4096, sigma=0.5, seed=seed)
 
 
-def mla_decode(batch: int = 128, seq_len: int = 2048, seed: int = 1) -> MlaCase:
-    """64 heads, ckv 512 (K and V), kpe 64, bf16 N(0,1)*0.3, page_size 1, scale 1/sqrt(192);
-    batch 128 x seq 2048 or batch 768 x seq 1024."""
-    return MlaCase(B=batch, H=64, seq_len=seq_len, seed=seed)
+def mla_decode(batch: int = 128, seq_len: int = 2048, seed: int = 1,
+               page_size: int = 1) -> MlaCase:
+    """64 heads, ckv 512 (K and V), kpe 64, bf16 N(0,1)*0.3, scale 1/sqrt(192), page_size 1
+    unless given; batch 128 x seq 2048 or batch 768 x seq 1024 (and the grid around them)."""
+    return MlaCase(B=batch, H=64, seq_len=seq_len, seed=seed, page_size=page_size)
 
 
 MQA_SWEEP_LQ = (16, 64, 256, 1024, 4096, 16384)
