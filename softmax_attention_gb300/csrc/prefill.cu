@@ -49,11 +49,11 @@ struct Layout {
   static constexpr int kVOff = kKOff + STAGES * kKVBytes;
   static constexpr int kBarOff = kVOff + STAGES * kKVBytes;
   // q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full, o_full,
-  // mma_done
-  static constexpr int kNumBars = 1 + 4 * STAGES + 2 + 3;
+  // mma_done, q_in_tmem
+  static constexpr int kNumBars = 1 + 4 * STAGES + 2 + 3 + 1;
   static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 bytes
-  static_assert(D + 2 * BN <= 512, "tensor memory budget");
+  static_assert(D + 2 * BN + D / 2 <= 512, "tensor memory budget (O, two S/P buffers, Q)");
   static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_p = bars + 8u * (3 + 4 * STAGES);
   const uint32_t bar_o = bars + 8u * (4 + 4 * STAGES);
   const uint32_t bar_done = bars + 8u * (5 + 4 * STAGES);
+  const uint32_t bar_qt = bars + 8u * (6 + 4 * STAGES);  // Q copied into tensor memory
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBarOff + L::kNumBars * 8);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_p, 4 * 32);
     mbar_init(bar_o, 1);
     mbar_init(bar_done, 1);
+    mbar_init(bar_qt, 4 * 32);
     fence_barrier_init();
   }
   if (warp == 5) {
@@ -152,6 +154,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tm_o = tmem;           // O: columns [0, D)
   const uint32_t tm_s0 = tmem + D;      // S/P buffer b: columns [D + b*BN, D + (b+1)*BN)
+  // Q, the A operand of S: row r in lane r, element pairs packed per column (D/2 columns).
+  // Taking A from tensor memory leaves only K to be read from shared memory per S MMA.
+  const uint32_t tq_tmem = tmem + D + 2 * BN;
 
   if (warp == 4) {
     // ------------------------------- TMA producer ---------------------------------------
@@ -256,14 +261,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk % 4) * 32;
-          const uint64_t ad = sdesc_sw128(sQ + (kk / 4) * (kRows * 128) + off, 16, 1024);
           const uint64_t bd = sdesc_sw128(kbase + (kk / 4) * kCB + off, 16, kRG);
-          mma_ss(d_s, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+          mma_ts(d_s, tq_tmem + kk * 8, bd, idesc_s, kk > 0 ? 1u : 0u);
         }
         tc_commit(bar_s(jj & 1));
         tc_commit(bar_ke(jj % STAGES));
       };
-      bool ok = mbar_wait(bar_q, 0, p.status) && mbar_wait(bar_k(0), 0, p.status);
+      bool ok = mbar_wait(bar_qt, 0, p.status) && mbar_wait(bar_k(0), 0, p.status);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -299,7 +303,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int jj = 0; jj < n; ++jj) {
+    if (n > 0) {
+      // Copy this thread's Q row from the swizzled shared-memory tile into its tensor-memory
+      // lane: 64-column block kb, 16-byte chunk ch of row r sits at chunk ch ^ (r & 7).
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, p.status));
+      if (ok) {
+        const int r = threadIdx.x;
+        const uint8_t* qrow = smem + L::kQOff + r * 128;
+#pragma unroll 1
+        for (int kb = 0; kb < D / 64; ++kb) {
+          uint32_t w[32];
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint4 v = *reinterpret_cast<const uint4*>(qrow + kb * (kRows * 128) + ((ch ^ (r & 7)) * 16));
+            w[4 * ch] = v.x;
+            w[4 * ch + 1] = v.y;
+            w[4 * ch + 2] = v.z;
+            w[4 * ch + 3] = v.w;
+          }
+          tmem_st32(tq_tmem + lane_off + kb * 32, w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar_qt);
+      }
+    }
+    for (int jj = 0; ok && jj < n; ++jj) {
       const uint32_t t_s = tm_s0 + lane_off + (jj & 1) * BN;
       ok = __all_sync(0xffffffffu, mbar_wait(bar_s(jj & 1), (jj >> 1) & 1, p.status));
       if (!ok) break;
