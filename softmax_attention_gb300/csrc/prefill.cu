@@ -13,8 +13,15 @@
 // through a page table (chunked prefill against a paged cache): each page of a KV tile is
 // one 5-D TMA box, and each sequence has its own length.
 //
-// Warp roles (192 threads): warps 0-3 softmax + epilogue (thread t owns row t), warp 4 TMA
-// producer, warp 5 MMA issuer (one elected thread) and tensor-memory owner.
+// Warp roles (224 threads): warps 0-3 softmax + epilogue (thread t owns row t), warp 4 TMA
+// producer, warp 5 MMA issuer (one elected thread) and tensor-memory owner, warp 6 the
+// landing watcher.  Once a thread has committed MMAs, its next shared-memory access (an
+// mbarrier wait included) is held until those MMAs finish, so every wait the issuer makes
+// drains the tensor pipe.  The issuer therefore waits once per KV tile, on ready[j % STAGES],
+// whose phase completes when the softmax has written P_j (128 arrivals) and the watcher has
+// seen V_j and K_{j+2} land (1 arrival); it then issues P_j V_j and S_{j+2} back to back.
+// With two stages K_{j+2} can only load once S_j is done, too late to gate P_j V_j, so there
+// the watcher covers V_j alone and the issuer waits for K_{j+2} itself.
 #include <math.h>
 
 #include "internal.h"
@@ -25,7 +32,7 @@ namespace fa {
 namespace {
 
 using prefill::kRows;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kLptMaxSeqs = 64;  // paged: order sequences by length when there are at most this many
 
 // 5-D tiled TMA load (the paged K/V boxes below).
@@ -48,9 +55,9 @@ struct Layout {
   static constexpr int kKOff = kQBytes;
   static constexpr int kVOff = kKOff + STAGES * kKVBytes;
   static constexpr int kBarOff = kVOff + STAGES * kKVBytes;
-  // q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full, o_full,
+  // q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], ready[S], o_full,
   // mma_done, q_in_tmem
-  static constexpr int kNumBars = 1 + 4 * STAGES + 2 + 3 + 1;
+  static constexpr int kNumBars = 1 + 5 * STAGES + 2 + 3;
   static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 bytes
   static_assert(D + 2 * BN + D / 2 <= 512, "tensor memory budget (O, two S/P buffers, Q)");
@@ -63,6 +70,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using L = Layout<D, BN, STAGES>;
+  constexpr bool kWatchK = STAGES >= 3;  // ready[j] also covers K_{j+2}
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -75,10 +83,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_ke = [&](int s) { return bars + 8u * (1 + 2 * STAGES + s); };
   auto bar_ve = [&](int s) { return bars + 8u * (1 + 3 * STAGES + s); };
   auto bar_s = [&](int b) { return bars + 8u * (1 + 4 * STAGES + b); };
-  const uint32_t bar_p = bars + 8u * (3 + 4 * STAGES);
-  const uint32_t bar_o = bars + 8u * (4 + 4 * STAGES);
-  const uint32_t bar_done = bars + 8u * (5 + 4 * STAGES);
-  const uint32_t bar_qt = bars + 8u * (6 + 4 * STAGES);  // Q copied into tensor memory
+  // ready[s]: P_j written, V_j landed and K_{j+2} landed, for the tile j with j % S == s
+  auto bar_r = [&](int s) { return bars + 8u * (3 + 4 * STAGES + s); };
+  const uint32_t bar_o = bars + 8u * (3 + 5 * STAGES);
+  const uint32_t bar_done = bars + 8u * (4 + 5 * STAGES);
+  const uint32_t bar_qt = bars + 8u * (5 + 5 * STAGES);  // Q copied into tensor memory
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBarOff + L::kNumBars * 8);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -135,10 +144,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_v(s), 1);
       mbar_init(bar_ke(s), 1);
       mbar_init(bar_ve(s), 1);
+      mbar_init(bar_r(s), 4 * 32 + 1);
     }
     mbar_init(bar_s(0), 1);
     mbar_init(bar_s(1), 1);
-    mbar_init(bar_p, 4 * 32);
     mbar_init(bar_o, 1);
     mbar_init(bar_done, 1);
     mbar_init(bar_qt, 4 * 32);
@@ -267,21 +276,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(bar_s(jj & 1));
         tc_commit(bar_ke(jj % STAGES));
       };
+      // S_0 and S_1 up front; afterwards one wait per tile (ready[j]) and no other shared-
+      // memory access, since each would be held until the committed MMAs finish.
       bool ok = mbar_wait(bar_qt, 0, p.status) && mbar_wait(bar_k(0), 0, p.status);
       if (ok) {
         tc_fence_after();
         issue_s(0);
       }
+      if (ok && n > 1 && (ok = mbar_wait(bar_k(1), 0, p.status))) {
+        tc_fence_after();
+        issue_s(1);
+      }
       for (int jj = 0; ok && jj < n; ++jj) {
-        if (jj + 1 < n) {
-          const int s1 = (jj + 1) % STAGES;
-          if (!(ok = mbar_wait(bar_k(s1), ((jj + 1) / STAGES) & 1, p.status))) break;
-          tc_fence_after();
-          issue_s(jj + 1);
-        }
-        if (!(ok = mbar_wait(bar_p, jj & 1, p.status))) break;
         const int stage = jj % STAGES;
-        if (!(ok = mbar_wait(bar_v(stage), (jj / STAGES) & 1, p.status))) break;
+        if (!(ok = mbar_wait(bar_r(stage), (jj / STAGES) & 1, p.status))) break;
         tc_fence_after();
         const uint32_t vbase = sV + stage * L::kKVBytes;
         const uint32_t a_p = tm_s0 + (jj & 1) * BN;
@@ -292,10 +300,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(bar_o);
         tc_commit(bar_ve(stage));
+        // S_{j+2} goes into the buffer that holds P_j: the tensor pipe runs one thread's MMAs
+        // in order, so P_j V_j has read P_j before S_{j+2} overwrites it.
+        if (jj + 2 < n) {
+          if constexpr (!kWatchK) {
+            if (!(ok = mbar_wait(bar_k((jj + 2) % STAGES), ((jj + 2) / STAGES) & 1, p.status))) break;
+            tc_fence_after();
+          }
+          issue_s(jj + 2);
+        }
       }
       // Every MMA this thread issued must finish before tensor memory is released.
       tc_commit(bar_done);
       mbar_wait(bar_done, 0, nullptr);
+    }
+  } else if (warp == 6) {
+    // ------------------------------ landing watcher -------------------------------------
+    // One arrival on ready[j] once V_j and K_{j+2} have landed.  It can run ahead of the
+    // softmax by at most STAGES tiles: V_{j+STAGES} is only loaded after P_j V_j is done.
+    if (lane == 0 && n > 0) {
+      for (int jj = 0; jj < n; ++jj) {
+        const int stage = jj % STAGES;
+        if (!mbar_wait(bar_v(stage), (jj / STAGES) & 1, p.status)) break;
+        if (kWatchK && jj + 2 < n &&
+            !mbar_wait(bar_k((jj + 2) % STAGES), ((jj + 2) / STAGES) & 1, p.status))
+          break;
+        mbar_arrive(bar_r(stage));
+      }
     }
   } else {
     // ------------------------- softmax + epilogue (row per thread) ----------------------
@@ -368,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
       }
       tc_fence_before();
-      mbar_arrive(bar_p);
+      mbar_arrive(bar_r(jj % STAGES));
     }
     if (ok && n > 0) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (n - 1) & 1, p.status));
