@@ -319,7 +319,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // One arrival on ready[j] once V_j and K_{j+2} have landed.  It can run ahead of the
     // softmax by at most STAGES tiles: V_{j+STAGES} is only loaded after P_j V_j is done.
     if (lane == 0 && n > 0) {
-      for (int jj = 0; jj < n; ++jj) {
+      // K_0 and K_1 are otherwise waited for only by the issuer.  Their stages later hold
+      // K_STAGES and K_{STAGES+1}, which this warp does wait for; observing phase 0 first keeps
+      // those parity waits exact whatever order the loads complete in.
+      bool okw = !kWatchK ||
+                 (mbar_wait(bar_k(0), 0, p.status) && (n < 2 || mbar_wait(bar_k(1), 0, p.status)));
+      for (int jj = 0; okw && jj < n; ++jj) {
         const int stage = jj % STAGES;
         if (!mbar_wait(bar_v(stage), (jj / STAGES) & 1, p.status)) break;
         if (kWatchK && jj + 2 < n &&

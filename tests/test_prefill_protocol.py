@@ -1,0 +1,321 @@
+"""A discrete-event model of the prefill kernel's barrier protocol, checked on CPU.
+
+prefill_kernel (softmax_attention_gb300/csrc/prefill.cu) runs seven warps that only meet
+through mbarriers: a TMA producer, a landing watcher, one MMA-issuing thread and four softmax
+warps.  A mistake there hangs or races on the GPU, where it cannot be tried safely, so this
+module restates the protocol as agents over modelled barriers and runs it under random
+latencies.  For every run it checks that
+
+* every agent finishes (no deadlock);
+* every parity wait is unambiguous whenever it polls: the barrier has completed exactly the
+  awaited phase's predecessors or one more, never two phases past nor one short (either would
+  make the hardware's parity test answer wrongly);
+* no shared-memory stage or tensor-memory S/P buffer is read before its data is there, or
+  overwritten while a reader still needs it.
+
+The model follows the kernel's structure (one agent per role, the same barriers and phase
+arithmetic); the mutation tests at the end plant known protocol mistakes and check that the
+model reports them.
+"""
+import heapq
+import itertools
+import random
+
+import pytest
+
+
+class Hazard(AssertionError):
+    pass
+
+
+class Bar:
+    """An mbarrier: `count` arrivals plus a transaction count complete a phase."""
+
+    def __init__(self, name, count):
+        self.name, self.count, self.pending, self.tx, self.done = name, count, count, 0, 0
+
+    def arrive(self, expect=0):
+        self.tx += expect
+        self.pending -= 1
+        if self.pending < 0:
+            raise Hazard(f"{self.name}: more arrivals than its count in one phase")
+        self._check()
+
+    def expect(self, nbytes):
+        self.tx += nbytes
+
+    def complete_tx(self, nbytes):
+        self.tx -= nbytes
+        self._check()
+
+    def _check(self):
+        if self.pending == 0 and self.tx == 0:
+            self.done += 1
+            self.pending = self.count
+
+    def passed(self, phase):
+        """Parity wait for `phase`: true once it completed; ambiguous states are errors."""
+        if self.done not in (phase, phase + 1):
+            raise Hazard(f"{self.name}: waiting for phase {phase} with {self.done} completed")
+        return self.done == phase + 1
+
+
+class Sim:
+    def __init__(self, rng):
+        self.rng, self.t, self.events, self.waiters = rng, 0.0, [], []
+        self.seq = itertools.count()
+        self.finished = set()
+
+    def at(self, dt, fn):
+        heapq.heappush(self.events, (self.t + dt, next(self.seq), fn))
+
+    def start(self, name, gen):
+        self._step(name, gen)
+
+    def _step(self, name, gen):
+        while True:
+            try:
+                req = next(gen)
+            except StopIteration:
+                self.finished.add(name)
+                return
+            if req[0] == "delay":
+                self.at(req[1], lambda: self._step(name, gen))
+                return
+            if not req[1]():  # "wait"
+                self.waiters.append((name, gen, req[1]))
+                return
+
+    def _poll(self):
+        progress = True
+        while progress:
+            progress = False
+            for w in list(self.waiters):
+                if w in self.waiters and w[2]():
+                    self.waiters.remove(w)
+                    self._step(w[0], w[1])
+                    progress = True
+
+    def run(self):
+        self._poll()
+        while self.events:
+            self.t, _, fn = heapq.heappop(self.events)
+            fn()
+            self._poll()
+        if self.waiters:
+            raise Hazard("deadlock: " + ", ".join(w[0] for w in self.waiters))
+
+
+class TensorPipe:
+    """One issuing thread's MMAs run in issue order; a commit arrives when all earlier finish."""
+
+    def __init__(self, sim):
+        self.sim, self.free_at = sim, 0.0
+
+    def mma(self, dur, on_start, on_end):
+        start = max(self.sim.t, self.free_at)
+        self.free_at = start + dur
+        self.sim.at(start - self.sim.t, on_start)
+        self.sim.at(self.free_at - self.sim.t, on_end)
+
+    def commit(self, bar):
+        self.sim.at(max(0.0, self.free_at - self.sim.t), bar.arrive)
+
+
+def run_protocol(n, stages, seed, *, paged_tail=False, mutate=None):
+    """Runs one CTA's KV loop of n tiles with `stages` K/V stages; raises Hazard on a fault."""
+    rng = random.Random(seed)
+    sim = Sim(rng)
+    pipe = TensorPipe(sim)
+    watch_k = stages >= 3                                 # ready[j] also covers K_{j+2}
+    watcher_k = watch_k and mutate != "watcher_skips_k"
+    watcher_v = mutate != "watcher_skips_v"
+    B = lambda name, c=1: Bar(name, c)
+    bar_q, bar_qt = B("q"), B("q_in_tmem", 128)
+    bar_k = [B(f"k_full{s}") for s in range(stages)]
+    bar_v = [B(f"v_full{s}") for s in range(stages)]
+    bar_ke = [B(f"k_empty{s}") for s in range(stages)]
+    bar_ve = [B(f"v_empty{s}") for s in range(stages)]
+    bar_s = [B("s_full0"), B("s_full1")]
+    bar_r = [B(f"ready{s}", 128 + (0 if mutate == "ready_count_128" else 1)) for s in range(stages)]
+    bar_o = B("o_full")
+
+    kstage, vstage = [None] * stages, [None] * stages   # (tile, landed)
+    sbuf = [[None] * 4 for _ in range(2)]               # per buffer, per warp quarter
+    s_done, pv_done = set(), set()
+    lat = lambda lo, hi: rng.uniform(lo, hi)
+
+    def check(cond, what):
+        if not cond:
+            raise Hazard(what)
+
+    def tma(bar, store, s, j, reader_done):
+        if j >= stages:
+            check(j - stages in reader_done, f"load of tile {j} over a stage still in use")
+        store[s] = (j, False)
+
+        def land():
+            store[s] = (j, True)
+            bar.complete_tx(1)
+        sim.at(lat(0.2, 3.0), land)
+
+    def producer():
+        bar_q.arrive(expect=1)
+        sim.at(lat(0.2, 2.0), lambda: bar_q.complete_tx(1))
+        for j in range(n):
+            s = j % stages
+            if j >= stages:
+                yield ("wait", lambda s=s, j=j: bar_ke[s].passed(j // stages - 1))
+            bar_k[s].arrive(expect=1)
+            tma(bar_k[s], kstage, s, j, s_done)
+            if j >= stages:
+                yield ("wait", lambda s=s, j=j: bar_ve[s].passed(j // stages - 1))
+            bar_v[s].arrive(expect=1)
+            tma(bar_v[s], vstage, s, j, pv_done)
+            yield ("delay", lat(0.0, 0.1))
+
+    def watcher():
+        if watcher_k and mutate != "watcher_skips_k01":
+            # K_0 and K_1 share barriers with K_S and K_{S+1}, which the watcher waits for
+            yield ("wait", lambda: bar_k[0].passed(0))
+            if n > 1:
+                yield ("wait", lambda: bar_k[1].passed(0))
+        for j in range(n):
+            s = j % stages
+            if watcher_v:
+                yield ("wait", lambda s=s, j=j: bar_v[s].passed(j // stages))
+            if watcher_k and j + 2 < n:
+                s2 = (j + 2) % stages
+                yield ("wait", lambda s2=s2, j=j: bar_k[s2].passed((j + 2) // stages))
+            bar_r[s].arrive()
+
+    def issue_s(j):
+        b, s = j & 1, j % stages
+
+        def start():
+            check(kstage[s] == (j, True), f"S_{j} reads K stage {s} holding {kstage[s]}")
+            if j >= 2:
+                check(j - 2 in pv_done, f"S_{j} overwrites P_{j - 2} before P V read it")
+
+        def end():
+            s_done.add(j)
+            for w in range(4):
+                sbuf[b][w] = ("S", j)
+        pipe.mma(lat(0.2, 0.6), start, end)
+        pipe.commit(bar_s[b])
+        pipe.commit(bar_ke[s])
+
+    def issue_pv(j):
+        b, s = j & 1, j % stages
+
+        def start():
+            check(all(q == ("P", j) for q in sbuf[b]), f"P_{j} V_{j} reads {sbuf[b]}")
+            check(vstage[s] == (j, True), f"P_{j} V_{j} reads V stage {s} holding {vstage[s]}")
+
+        pipe.mma(lat(0.2, 0.6), start, lambda: pv_done.add(j))
+        pipe.commit(bar_o)
+        pipe.commit(bar_ve[s])
+
+    def mma():
+        yield ("wait", lambda: bar_qt.passed(0))
+        yield ("wait", lambda: bar_k[0].passed(0))
+        issue_s(0)
+        if n > 1:
+            yield ("wait", lambda: bar_k[1].passed(0))
+            issue_s(1)
+        for j in range(n):
+            s = j % stages
+            if mutate == "s_before_pv" and j + 2 < n:
+                if not watch_k:
+                    yield ("wait", lambda j=j: bar_k[(j + 2) % stages].passed((j + 2) // stages))
+                yield ("wait", lambda s=s, j=j: bar_r[s].passed(j // stages))
+                issue_s(j + 2)
+                issue_pv(j)
+                continue
+            yield ("wait", lambda s=s, j=j: bar_r[s].passed(j // stages))
+            issue_pv(j)
+            if j + 2 < n:
+                if not watch_k:
+                    s2 = (j + 2) % stages
+                    yield ("wait", lambda s2=s2, j=j: bar_k[s2].passed((j + 2) // stages))
+                issue_s(j + 2)
+
+    def softmax(w):
+        yield ("wait", lambda: bar_q.passed(0))
+        yield ("delay", lat(0.05, 0.2))
+        for _ in range(32):
+            bar_qt.arrive()
+        for j in range(n):
+            b, s = j & 1, j % stages
+            yield ("wait", lambda b=b, j=j: bar_s[b].passed(j >> 1))
+            check(sbuf[b][w] == ("S", j), f"softmax {w} reads S_{j} from {sbuf[b][w]}")
+            yield ("delay", lat(0.3, 1.0))
+            # The kernel waits every tile.  Skipping the wait on tiles with no rescale is unsafe
+            # with a single barrier: the epilogue's wait for the last P V could then pass on
+            # the phase before it (the skip_o_waits mutation).
+            if j > 0 and not (mutate == "skip_o_waits" and rng.random() < 0.8):
+                yield ("wait", lambda j=j: bar_o.passed(j - 1))
+                check(j - 1 in pv_done, f"softmax {w} rescales O before P_{j - 1} V_{j - 1}")
+            sbuf[b][w] = ("P", j)
+            if paged_tail and j == n - 1:
+                yield ("wait", lambda s=s, j=j: bar_v[s].passed(j // stages))
+            for _ in range(32):
+                bar_r[s].arrive()
+        if n > 0:
+            yield ("wait", lambda: bar_o.passed(n - 1))
+            check(n - 1 in pv_done, "epilogue reads O before the last P V")
+
+    if n > 0:
+        sim.start("producer", producer())
+        sim.start("watcher", watcher())
+        sim.start("mma", mma())
+        for w in range(4):
+            sim.start(f"softmax{w}", softmax(w))
+    sim.run()
+    expected = {"producer", "watcher", "mma"} | {f"softmax{w}" for w in range(4)} if n else set()
+    check(sim.finished == expected, f"unfinished: {expected - sim.finished}")
+
+
+@pytest.mark.parametrize("stages", [2, 3, 5])
+@pytest.mark.parametrize("n", [0, 1, 2, 3, 4, 5, 7, 10])
+def test_protocol_is_safe(stages, n):
+    for seed in range(40):
+        run_protocol(n, stages, seed)
+        run_protocol(n, stages, seed + 1000, paged_tail=True)
+
+
+def _fails(n, stages, mutate):
+    for seed in range(200):
+        try:
+            run_protocol(n, stages, seed, mutate=mutate)
+        except Hazard:
+            return True
+    return False
+
+
+def test_model_catches_missing_k_landing_wait():
+    # ready[j] must cover K_{j+2} when the issuer does not wait for it itself
+    assert _fails(8, 3, "watcher_skips_k")
+
+
+def test_model_catches_s_issued_over_unread_p():
+    # S_{j+2} shares P_j's buffer, so it has to follow P_j V_j in the tensor pipe
+    assert _fails(8, 3, "s_before_pv")
+
+
+def test_model_catches_watcher_not_observing_k0_k1():
+    # without it, the wait for K_S can pass on K_0's phase when loads complete out of order
+    assert _fails(8, 3, "watcher_skips_k01")
+
+
+def test_model_catches_watcher_not_waiting_for_v():
+    assert _fails(8, 3, "watcher_skips_v")
+
+
+def test_model_catches_ready_count_without_the_watcher():
+    # 128 + 1 arrivals per phase; with a count of 128 a phase can close before every P row
+    assert _fails(8, 3, "ready_count_128")
+
+
+def test_model_catches_skipped_o_waits_on_one_barrier():
+    assert _fails(9, 3, "skip_o_waits")
