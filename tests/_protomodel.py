@@ -1,6 +1,8 @@
 """Discrete-event core for the barrier-protocol models in test_*_protocol.py (test code only).
 
-Agents are generators that yield ("delay", dt) or ("wait", predicate); barriers model
+Agents are generators that yield ("delay", dt), ("wait", predicate) or ("twait", predicate,
+limit); a bounded wait resumes the agent with True once the predicate holds, or with False
+when `limit` time passes first (the kernels' time-limited mbarrier waits).  Barriers model
 mbarrier phases (arrival count plus transaction count) and check every parity wait for
 ambiguity; the tensor pipe runs one issuing thread's MMAs in order and lands a commit's
 arrival when every earlier MMA has finished.
@@ -38,8 +40,14 @@ class Bar:
             self.done += 1
             self.pending = self.count
 
-    def passed(self, phase):
-        """Parity wait for `phase`: true once it completed; ambiguous states are errors."""
+    def passed(self, phase, hw=False):
+        """Parity wait for `phase`: true once it completed; ambiguous states are errors.
+
+        hw=True answers as the hardware's parity test does (the current phase's parity
+        differs from the awaited one's) without the ambiguity check, for waits whose
+        consequences the caller checks otherwise."""
+        if hw:
+            return self.done % 2 != phase % 2
         if self.done not in (phase, phase + 1):
             raise Hazard(f"{self.name}: waiting for phase {phase} with {self.done} completed")
         return self.done == phase + 1
@@ -50,6 +58,7 @@ class Sim:
         self.rng, self.t, self.events, self.waiters = rng, 0.0, [], []
         self.seq = itertools.count()
         self.finished = set()
+        self.finish_time = {}
 
     def at(self, dt, fn):
         heapq.heappush(self.events, (self.t + dt, next(self.seq), fn))
@@ -57,19 +66,29 @@ class Sim:
     def start(self, name, gen):
         self._step(name, gen)
 
-    def _step(self, name, gen):
+    def _step(self, name, gen, value=None):
         while True:
             try:
-                req = next(gen)
+                req = gen.send(value)
             except StopIteration:
                 self.finished.add(name)
+                self.finish_time[name] = self.t
                 return
             if req[0] == "delay":
-                self.at(req[1], lambda: self._step(name, gen))
+                self.at(req[1], lambda: self._step(name, gen, None))
                 return
-            if not req[1]():  # "wait"
-                self.waiters.append((name, gen, req[1]))
-                return
+            if req[1]():  # "wait" or "twait": already true
+                value = True
+                continue
+            w = (name, gen, req[1])
+            self.waiters.append(w)
+            if req[0] == "twait":
+                def expire(w=w):
+                    if w in self.waiters:
+                        self.waiters.remove(w)
+                        self._step(w[0], w[1], False)
+                self.at(req[2], expire)
+            return
 
     def _poll(self):
         progress = True
@@ -78,7 +97,7 @@ class Sim:
             for w in list(self.waiters):
                 if w in self.waiters and w[2]():
                     self.waiters.remove(w)
-                    self._step(w[0], w[1])
+                    self._step(w[0], w[1], True)
                     progress = True
 
     def run(self):

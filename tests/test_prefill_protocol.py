@@ -24,16 +24,22 @@ import pytest
 from tests._protomodel import Hazard, Sim, TensorPipe, Bar
 
 
-def run_protocol(n, stages, seed, *, paged_tail=False, mutate=None):
-    """Runs one CTA's KV loop of n tiles with `stages` K/V stages; raises Hazard on a fault."""
+def run_protocol(n, stages, seed, *, paged_tail=False, mutate=None, fault=None):
+    """Runs one CTA's KV loop of n tiles with `stages` K/V stages; raises Hazard on a fault.
+
+    fault = (agent, tile) stops that agent at that tile, as if one of its waits had run out
+    ("softmax1", "mma" or "watcher"); every wait is then bounded and the others take the
+    kernel's error paths.  Returns the agents that recorded an error.
+    """
     rng = random.Random(seed)
     sim = Sim(rng)
     pipe = TensorPipe(sim)
+    limit = 50.0 if fault else 1e9   # latencies below are at most a few units
     watch_k = stages >= 3                                 # ready[j] also covers K_{j+2}
     watcher_k = watch_k and mutate != "watcher_skips_k"
     watcher_v = mutate != "watcher_skips_v"
     B = lambda name, c=1: Bar(name, c)
-    bar_q, bar_qt = B("q"), B("q_in_tmem", 128)
+    bar_q, bar_qt, bar_done = B("q"), B("q_in_tmem", 128), B("mma_done")
     bar_k = [B(f"k_full{s}") for s in range(stages)]
     bar_v = [B(f"v_full{s}") for s in range(stages)]
     bar_ke = [B(f"k_empty{s}") for s in range(stages)]
@@ -45,11 +51,19 @@ def run_protocol(n, stages, seed, *, paged_tail=False, mutate=None):
     kstage, vstage = [None] * stages, [None] * stages   # (tile, landed)
     sbuf = [[None] * 4 for _ in range(2)]               # per buffer, per warp quarter
     s_done, pv_done = set(), set()
+    errors = set()
+    last_landing = [0.0]
     lat = lambda lo, hi: rng.uniform(lo, hi)
 
     def check(cond, what):
         if not cond:
             raise Hazard(what)
+
+    def wait(pred):
+        return ("twait", pred, limit)
+
+    def stops(agent, j):
+        return fault is not None and fault == (agent, j)
 
     def tma(bar, store, s, j, reader_done):
         if j >= stages:
@@ -59,36 +73,66 @@ def run_protocol(n, stages, seed, *, paged_tail=False, mutate=None):
         def land():
             store[s] = (j, True)
             bar.complete_tx(1)
-        sim.at(lat(0.2, 3.0), land)
+        dt = lat(0.2, 3.0)
+        last_landing[0] = max(last_landing[0], sim.t + dt)
+        sim.at(dt, land)
 
     def producer():
         bar_q.arrive(expect=1)
-        sim.at(lat(0.2, 2.0), lambda: bar_q.complete_tx(1))
+        dt = lat(0.2, 2.0)
+        last_landing[0] = max(last_landing[0], sim.t + dt)
+        sim.at(dt, lambda: bar_q.complete_tx(1))
+        issued, k_only = 0, -1
         for j in range(n):
             s = j % stages
-            if j >= stages:
-                yield ("wait", lambda s=s, j=j: bar_ke[s].passed(j // stages - 1))
+            if j >= stages and not (yield wait(lambda s=s, j=j: bar_ke[s].passed(j // stages - 1))):
+                errors.add("producer")
+                break
             bar_k[s].arrive(expect=1)
             tma(bar_k[s], kstage, s, j, s_done)
-            if j >= stages:
-                yield ("wait", lambda s=s, j=j: bar_ve[s].passed(j // stages - 1))
+            if j >= stages and not (yield wait(lambda s=s, j=j: bar_ve[s].passed(j // stages - 1))):
+                errors.add("producer")
+                k_only = j
+                break
             bar_v[s].arrive(expect=1)
             tma(bar_v[s], vstage, s, j, pv_done)
+            issued = j + 1
             yield ("delay", lat(0.0, 0.1))
+        if issued < n:
+            # A wait ran out: let the copies still in flight land before the CTA exits.  These
+            # waits take the hardware's parity answer: when the producer stopped between a
+            # tile's K and V, that K reused the oldest drained tile's K stage, whose barrier is
+            # then two phases on, so the wait for the older K sees "not yet" and runs out its
+            # limit (the copies have landed; the end-of-run checks confirm nothing is in flight).
+            yield wait(lambda: bar_q.passed(0, hw=True))
+            for jj in range(max(0, issued - stages), issued):
+                yield wait(lambda jj=jj: bar_k[jj % stages].passed(jj // stages, hw=True))
+                yield wait(lambda jj=jj: bar_v[jj % stages].passed(jj // stages, hw=True))
+            if k_only >= 0:
+                yield wait(lambda: bar_k[k_only % stages].passed(k_only // stages, hw=True))
 
     def watcher():
         if watcher_k and mutate != "watcher_skips_k01":
             # K_0 and K_1 share barriers with K_S and K_{S+1}, which the watcher waits for
-            yield ("wait", lambda: bar_k[0].passed(0))
-            if n > 1:
-                yield ("wait", lambda: bar_k[1].passed(0))
+            if not (yield wait(lambda: bar_k[0].passed(0))):
+                errors.add("watcher")
+                return
+            if n > 1 and not (yield wait(lambda: bar_k[1].passed(0))):
+                errors.add("watcher")
+                return
         for j in range(n):
             s = j % stages
-            if watcher_v:
-                yield ("wait", lambda s=s, j=j: bar_v[s].passed(j // stages))
+            if stops("watcher", j):
+                errors.add("watcher")
+                return
+            if watcher_v and not (yield wait(lambda s=s, j=j: bar_v[s].passed(j // stages))):
+                errors.add("watcher")
+                return
             if watcher_k and j + 2 < n:
                 s2 = (j + 2) % stages
-                yield ("wait", lambda s2=s2, j=j: bar_k[s2].passed((j + 2) // stages))
+                if not (yield wait(lambda s2=s2, j=j: bar_k[s2].passed((j + 2) // stages))):
+                    errors.add("watcher")
+                    return
             bar_r[s].arrive()
 
     def issue_s(j):
@@ -119,14 +163,21 @@ def run_protocol(n, stages, seed, *, paged_tail=False, mutate=None):
         pipe.commit(bar_ve[s])
 
     def mma():
-        yield ("wait", lambda: bar_qt.passed(0))
-        yield ("wait", lambda: bar_k[0].passed(0))
-        issue_s(0)
-        if n > 1:
-            yield ("wait", lambda: bar_k[1].passed(0))
-            issue_s(1)
+        ok = yield wait(lambda: bar_qt.passed(0))
+        ok = ok and (yield wait(lambda: bar_k[0].passed(0)))
+        if ok:
+            issue_s(0)
+        if ok and n > 1:
+            ok = yield wait(lambda: bar_k[1].passed(0))
+            if ok:
+                issue_s(1)
         for j in range(n):
+            if not ok:
+                break
             s = j % stages
+            if stops("mma", j):
+                ok = False
+                break
             if mutate == "s_before_pv" and j + 2 < n:
                 if not watch_k:
                     yield ("wait", lambda j=j: bar_k[(j + 2) % stages].passed((j + 2) // stages))
@@ -134,38 +185,57 @@ def run_protocol(n, stages, seed, *, paged_tail=False, mutate=None):
                 issue_s(j + 2)
                 issue_pv(j)
                 continue
-            yield ("wait", lambda s=s, j=j: bar_r[s].passed(j // stages))
+            if not (ok := (yield wait(lambda s=s, j=j: bar_r[s].passed(j // stages)))):
+                break
             issue_pv(j)
             if j + 2 < n:
                 if not watch_k:
                     s2 = (j + 2) % stages
-                    yield ("wait", lambda s2=s2, j=j: bar_k[s2].passed((j + 2) // stages))
+                    if not (ok := (yield wait(lambda s2=s2, j=j: bar_k[s2].passed((j + 2) // stages)))):
+                        break
                 issue_s(j + 2)
+        if not ok:
+            errors.add("mma")
+        # every MMA issued must finish before tensor memory is released
+        pipe.commit(bar_done)
+        yield wait(lambda: bar_done.passed(0))
 
     def softmax(w):
-        yield ("wait", lambda: bar_q.passed(0))
-        yield ("delay", lat(0.05, 0.2))
-        for _ in range(32):
-            bar_qt.arrive()
+        ok = yield wait(lambda: bar_q.passed(0))
+        if ok:
+            yield ("delay", lat(0.05, 0.2))
+            for _ in range(32):
+                bar_qt.arrive()
         for j in range(n):
+            if not ok:
+                break
             b, s = j & 1, j % stages
-            yield ("wait", lambda b=b, j=j: bar_s[b].passed(j >> 1))
+            if stops(f"softmax{w}", j):
+                ok = False
+                break
+            if not (ok := (yield wait(lambda b=b, j=j: bar_s[b].passed(j >> 1)))):
+                break
             check(sbuf[b][w] == ("S", j), f"softmax {w} reads S_{j} from {sbuf[b][w]}")
             yield ("delay", lat(0.3, 1.0))
             # The kernel waits every tile.  Skipping the wait on tiles with no rescale is unsafe
             # with a single barrier: the epilogue's wait for the last P V could then pass on
             # the phase before it (the skip_o_waits mutation).
             if j > 0 and not (mutate == "skip_o_waits" and rng.random() < 0.8):
-                yield ("wait", lambda j=j: bar_o.passed(j - 1))
+                if not (ok := (yield wait(lambda j=j: bar_o.passed(j - 1)))):
+                    break
                 check(j - 1 in pv_done, f"softmax {w} rescales O before P_{j - 1} V_{j - 1}")
             sbuf[b][w] = ("P", j)
             if paged_tail and j == n - 1:
-                yield ("wait", lambda s=s, j=j: bar_v[s].passed(j // stages))
+                if not (ok := (yield wait(lambda s=s, j=j: bar_v[s].passed(j // stages)))):
+                    break
             for _ in range(32):
                 bar_r[s].arrive()
-        if n > 0:
-            yield ("wait", lambda: bar_o.passed(n - 1))
-            check(n - 1 in pv_done, "epilogue reads O before the last P V")
+        if ok and n > 0:
+            ok = yield wait(lambda: bar_o.passed(n - 1))
+            if ok:
+                check(n - 1 in pv_done, "epilogue reads O before the last P V")
+        if not ok:
+            errors.add(f"softmax{w}")
 
     if n > 0:
         sim.start("producer", producer())
@@ -176,6 +246,11 @@ def run_protocol(n, stages, seed, *, paged_tail=False, mutate=None):
     sim.run()
     expected = {"producer", "watcher", "mma"} | {f"softmax{w}" for w in range(4)} if n else set()
     check(sim.finished == expected, f"unfinished: {expected - sim.finished}")
+    if n:
+        exit_time = max(sim.finish_time.values())
+        check(last_landing[0] <= exit_time, "a copy lands after every warp has finished")
+        check(pipe.free_at <= exit_time, "an MMA runs after every warp has finished")
+    return errors
 
 
 @pytest.mark.parametrize("stages", [2, 3, 5])
@@ -221,3 +296,14 @@ def test_model_catches_ready_count_without_the_watcher():
 
 def test_model_catches_skipped_o_waits_on_one_barrier():
     assert _fails(9, 3, "skip_o_waits")
+
+
+@pytest.mark.parametrize("agent", ["softmax1", "mma", "watcher"])
+@pytest.mark.parametrize("stages", [2, 3])
+def test_error_paths_end_with_nothing_in_flight(agent, stages):
+    # a warp stopping mid-loop (as after a wait that ran out): every other wait is bounded,
+    # the producer lets its copies in flight land and the issuer's MMAs finish before exit
+    for seed in range(30):
+        n = 7
+        errors = run_protocol(n, stages, seed, fault=(agent, seed % n))
+        assert agent in errors and len(errors) > 1
