@@ -47,6 +47,14 @@ import workloads  # noqa: E402
 
 METRIC = "attention TFLOP/s (prefill) and KV GB/s (decode) + % of GB300 roofline"
 FLUSH_BYTES = 512 << 20
+# GB300 data-sheet figures the targets are stated against (about 8 TB/s of HBM3e and about
+# 2.2 PFLOP/s of dense bf16; the nominal 2.25 is used, and 8.0 rather than 7.9 TB/s, so each
+# fraction against them is the lower one).  Every roofline reports its fraction of the
+# measured peak (copy / cuBLAS) and, beside it, of these.
+SPEC_PEAKS = {"hbm": 8000.0, "bf16": 2250.0}
+# The headline workload, named the same way by both arms.
+WORKLOAD = ("gqa_prefill_chunk: B=1 Hq=32 Hkv=8 D=128 Lq=512 at 15872..16383 Lkv=16384 "
+            "causal bf16 N(0,1)*0.5 scale 1/sqrt(128)")
 
 
 # ------------------------------------------------------------------------------------------
@@ -215,9 +223,17 @@ def time_graph(fn, steps: int, warmup: int, flush, dist: Dist):
 
 
 def roofline(bound, achieved, peak, unit, traffic, pk):
+    spec = SPEC_PEAKS["bf16" if unit == "TFLOP/s" else "hbm"]
     return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
             "frac": round(achieved / peak, 4), "traffic": traffic,
-            "peak_source": f"{pk['source']} ({'burst' if unit == 'TFLOP/s' else 'copy'})"}
+            "peak_source": f"{pk['source']} ({'burst' if unit == 'TFLOP/s' else 'copy'})",
+            "peak_spec": spec, "frac_spec": round(achieved / spec, 4)}
+
+
+def summary(value, unit, ms, kernel_ms, rl):
+    """One config's entry in the compact per-config record of the result line."""
+    return {"value": round(value, 1), "unit": unit, "ms": round(ms, 4),
+            "kernel_ms": round(kernel_ms, 4), "frac": rl["frac"], "frac_spec": rl["frac_spec"]}
 
 
 # ------------------------------------------------------------------------------------------
@@ -329,36 +345,64 @@ def decode_bytes(c: workloads.PagedCase, lens) -> dict:
 
 
 def bench_decode(fa, c, steps, warmup, flush, dist, pk):
+    """Whole call through the automatic path (KV GB/s of the call's algorithmic bytes); the
+    roofline takes the dominant kernel alone where the call has a second (merge) launch.  The
+    other decode kernel's whole call is timed beside it for comparison."""
     dev = torch.device("cuda")
     q, kp, vp, table, lens = workloads.paged_inputs(c)
     qd, kd, vd, td, ld = (t.to(dev) for t in (q, kp, vp, table, lens))
     max_len = int(lens.max())
     out = torch.empty_like(qd)
     lse = torch.empty(c.B, c.Hq, dtype=torch.float32, device=dev)
-    ws = torch.empty(fa.fa_decode_workspace_size(c.B, c.Hq, c.D, max_len), dtype=torch.uint8,
-                     device=dev)
-    chunk = fa.fa_decode_chunk_tokens(c.B, c.Hq, max_len)
-    n_chunks = -(-max_len // chunk)
-    op = torch.empty(c.B * c.Hq, n_chunks, c.D, dtype=torch.float32, device=dev)
-    ol = torch.empty(c.B * c.Hq, n_chunks, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, fa.fa_decode_workspace_size(c.B, c.Hq, c.D, max_len)),
+                     dtype=torch.uint8, device=dev)
+    plan = fa.fa_decode_get_plan(qd, kd, vd, td, ld, max_len)
+    other = fa.FA_DECODE_CUDA_CORES if plan["path"] == fa.FA_DECODE_TENSOR_CORES \
+        else fa.FA_DECODE_TENSOR_CORES
 
-    def full():
-        fa.fa_decode_paged(qd, kd, vd, td, ld, max_len, c.sm_scale, out=out, lse=lse, workspace=ws)
-
-    def states():
-        fa.fa_decode_paged_states(qd, kd, vd, td, ld, max_len, c.sm_scale, o_parts=op, lse_parts=ol)
+    def call(path):
+        def f():
+            fa.fa_decode_paged(qd, kd, vd, td, ld, max_len, c.sm_scale, out=out, lse=lse,
+                               workspace=ws, path=path)
+        return f
 
     b = decode_bytes(c, lens)
-    ms_k, _, _ = time_graph(states, steps, warmup, flush, dist)
-    ms_f, _, mode = time_graph(full, steps, warmup, flush, dist)
-    k_ms, f_ms = dist.max(statistics.mean(ms_k)), dist.max(statistics.mean(ms_f))
+    ms_f, _, mode = time_graph(call(fa.FA_DECODE_AUTO), steps, warmup, flush, dist)
+    f_ms = dist.max(statistics.mean(ms_f))
+    if plan["launches"] == 1:
+        k_ms, k_bytes = f_ms, b["total"]
+    elif plan["path"] == fa.FA_DECODE_CUDA_CORES:
+        chunk = fa.fa_decode_chunk_tokens(c.B, c.Hq, max_len)
+        n_chunks = -(-max_len // chunk)
+        op = torch.empty(c.B * c.Hq, n_chunks, c.D, dtype=torch.float32, device=dev)
+        ol = torch.empty(c.B * c.Hq, n_chunks, dtype=torch.float32, device=dev)
+
+        def states():
+            fa.fa_decode_paged_states(qd, kd, vd, td, ld, max_len, c.sm_scale, o_parts=op,
+                                      lse_parts=ol)
+        ms_k, _, _ = time_graph(states, steps, warmup, flush, dist)
+        k_ms, k_bytes = dist.max(statistics.mean(ms_k)), b["kernel"]
+        del op, ol
+    else:
+        k_ms, k_bytes = f_ms, b["total"]
+    try:
+        ms_o, _, _ = time_graph(call(other), steps, warmup, flush, dist)
+        o_ms = dist.max(statistics.mean(ms_o))
+        alt = {"path": "tensor cores" if other == fa.FA_DECODE_TENSOR_CORES else "CUDA cores",
+               "value": round(b["total"] / (o_ms * 1e-3) / 1e9, 1), "ms": round(o_ms, 4)}
+    except fa.FAError as e:
+        alt = {"unavailable": str(e)}
+    tc = plan["path"] == fa.FA_DECODE_TENSOR_CORES
     res = {"value": round(b["total"] / (f_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-           "ms": round(f_ms, 4), "bytes": b["total"], "chunk": chunk, "mode": mode,
-           "launches_per_step": 2,
-           "roofline": roofline("hbm", b["kernel"] / (k_ms * 1e-3) / 1e9, pk["hbm"], "GB/s",
-                                profiled_traffic("decode_paged_gqa.md", "decode"), pk),
-           "kernel_ms": round(k_ms, 4)}
-    del qd, kd, vd, td, ld, out, lse, ws, op, ol
+           "ms": round(f_ms, 4), "bytes": b["total"], "mode": mode,
+           "path": "tensor cores" if tc else "CUDA cores", "n_splits": plan["n_splits"],
+           "launches_per_step": plan["launches"],
+           "roofline": roofline("hbm", k_bytes / (k_ms * 1e-3) / 1e9, pk["hbm"], "GB/s",
+                                profiled_traffic("decode_paged_gqa_tc.md" if tc
+                                                 else "decode_paged_gqa.md",
+                                                 "prefill" if tc else "decode"), pk),
+           "kernel_ms": round(k_ms, 4), "other_path": alt}
+    del qd, kd, vd, td, ld, out, lse, ws
     torch.cuda.empty_cache()
     return res
 
@@ -490,8 +534,8 @@ def cpu_baseline(c, budget_s: float = 12.0):
     dt, fl = oracle_rate(c, q, k, v, n, offset=7)
     return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"{n} of {c.B * c.Hq * c.Lq} query rows (strided over heads and "
-                      f"queries), all their visible keys; {dt:.1f} s"}
+            "sample": f"{n} of {c.B * c.Hq * c.Lq} query rows, strided, all visible keys; "
+                      f"{dt:.1f} s"}
 
 
 def run_reference(args, dist: Dist):
@@ -517,8 +561,8 @@ def run_reference(args, dist: Dist):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(t_sum / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "gqa_prefill_chunk: B=1 Hq=32 Hkv=8 D=128 Lq=512 Lkv=16384 "
-                               "causal bf16 inputs", "sample_rows_per_step": rows_per_step},
+        "config": {"workload": WORKLOAD, "flops_per_step": prefill_flops(c),
+                   "parallelism": "replica x1"},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
                          "kind": "oracle",
                          "sample": f"{rows_per_step} query rows per step of "
@@ -530,6 +574,18 @@ def run_reference(args, dist: Dist):
 
 
 # ------------------------------------------------------------------------------------------
+def mqa_point(r, mc, pk):
+    """Roofline of one multi-query sweep point: HBM-bound where its arithmetic intensity is
+    below the ridge point of the measured peaks, tensor-bound above it."""
+    bytes_ = (mc.Lq * mc.Hq * 2 + 2 * mc.Lkv * mc.Hkv) * mc.D * 2 + mc.Lq * mc.Hq * 4
+    bound = "hbm" if r["flops"] / bytes_ < pk["bf16"] * 1e3 / pk["hbm"] else "tensor"
+    ach = (bytes_ / (r["ms"] * 1e-3) / 1e9) if bound == "hbm" else r["tflops"]
+    return {"value": round(r["tflops"], 2), "unit": "TFLOP/s", "ms": round(r["ms"], 4),
+            "splits": r["splits"], "launches_per_step": r["launches_per_step"],
+            "roofline": roofline(bound, ach, pk["hbm"] if bound == "hbm" else pk["bf16"],
+                                 "GB/s" if bound == "hbm" else "TFLOP/s", None, pk)}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -563,42 +619,49 @@ def main():
         clocks.start()
         c = workloads.gqa_prefill_chunk(seed=1 + dist.rank)
         head = bench_prefill(fa, c, args.steps, args.warmup, flush, dist, pk, e2e=True)
+        head_rl = roofline("tensor", head["tflops"], pk["bf16"], "TFLOP/s",
+                           profiled_traffic("prefill_gqa_chunk.md", "prefill"), pk)
+        # every configured workload's figure, compact: the last key of the result line
+        configs = {"C2": summary(head["tflops"], "TFLOP/s", head["ms"], head["ms"], head_rl)}
         paths = {}
         if not args.quick or args.only:
             sub = max(20, args.steps // 4) if not args.quick else 3
             want = (lambda name: args.only in (None, name))
             if want("decode"):
                 pc = workloads.paged_gqa_decode(seed=1 + dist.rank)
-                paths["paged_gqa_decode"] = bench_decode(fa, pc, sub, args.warmup, flush, dist, pk)
-            if want("paged"):
-                ppc = workloads.paged_gqa_prefill(seed=1 + dist.rank)
-                paths["paged_gqa_prefill"] = bench_prefill_paged(fa, ppc, sub, args.warmup, flush,
-                                                                 dist, pk)
+                r = bench_decode(fa, pc, sub, args.warmup, flush, dist, pk)
+                paths["paged_gqa_decode"] = r
+                configs["C3"] = dict(summary(r["value"], "GB/s", r["ms"], r["kernel_ms"],
+                                             r["roofline"]), path=r["path"])
             # the MLA grid of the flashinfer PR's results: batch {64, 128, 768} x {1024, 2048}
             mla_points = [(b_, s_, 1) for b_, s_ in MLA_GRID] + list(MLA_PAGED)
             for batch, seq, ps in (mla_points if want("mla") else ()):
                 mc = workloads.mla_decode(batch, seq, seed=1 + dist.rank, page_size=ps)
                 key = f"mla_decode_b{batch}_s{seq}" + (f"_ps{ps}" if ps > 1 else "")
                 try:
-                    paths[key] = bench_mla(fa, mc, sub, args.warmup, flush, dist, pk)
+                    r = bench_mla(fa, mc, sub, args.warmup, flush, dist, pk)
                 except fa.FAError as e:
                     paths[key] = {"unavailable": str(e)}
+                    continue
+                paths[key] = r
+                name = {(128, 2048, 1): "C4a", (768, 1024, 1): "C4b"}.get((batch, seq, ps))
+                if name:
+                    configs[name] = summary(r["value"], "GB/s", r["ms"], r["kernel_ms"],
+                                            r["roofline"])
             sweep = {}
             for lq in (workloads.MQA_SWEEP_LQ if want("mqa") else ()):
                 mc = workloads.mqa_prefill(lq, seed=1 + dist.rank)
                 r = bench_prefill(fa, mc, sub, args.warmup, flush, dist, pk)
-                bytes_ = (mc.Lq * mc.Hq * 2 + 2 * mc.Lkv * mc.Hkv) * mc.D * 2 + mc.Lq * mc.Hq * 4
-                ai = r["flops"] / bytes_
-                bound = "hbm" if ai < pk["bf16"] * 1e3 / pk["hbm"] else "tensor"
-                ach = (bytes_ / (r["ms"] * 1e-3) / 1e9) if bound == "hbm" else r["tflops"]
-                sweep[str(lq)] = {"value": round(r["tflops"], 2), "unit": "TFLOP/s",
-                                  "ms": round(r["ms"], 4), "splits": r["splits"],
-                                  "roofline": roofline(bound, ach,
-                                                       pk["hbm"] if bound == "hbm" else pk["bf16"],
-                                                       "GB/s" if bound == "hbm" else "TFLOP/s",
-                                                       None, pk)}
+                sweep[str(lq)] = mqa_point(r, mc, pk)
             if sweep:
                 paths["mqa_prefill_sweep"] = sweep
+                configs["C5"] = {lq: summary(v["value"], "TFLOP/s", v["ms"], v["ms"],
+                                             v["roofline"]) for lq, v in sweep.items()}
+            if want("paged"):
+                ppc = workloads.paged_gqa_prefill(seed=1 + dist.rank)
+                r = bench_prefill_paged(fa, ppc, sub, args.warmup, flush, dist, pk)
+                paths["paged_gqa_prefill"] = r
+                configs["N1"] = summary(r["value"], "TFLOP/s", r["ms"], r["ms"], r["roofline"])
         clk = clocks.stop() if dist.rank == 0 else None
         flops = head["flops"]
         total_tflops = dist.world * flops / (head["ms"] * 1e-3) / 1e12
@@ -606,26 +669,27 @@ def main():
         if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
             cpu = cpu_baseline(c)
         if dist.rank == 0:
-            traffic = profiled_traffic("prefill_gqa_chunk.md", "prefill")
+            # Verbose per-path detail first, on a line of its own; the result line (last) keeps
+            # to the compact per-config record so that it stays short.
+            print("detail " + json.dumps({"paths": paths, "p10_ms": round(head["p10_ms"], 4),
+                                          "p90_ms": round(head["p90_ms"], 4),
+                                          "e2e_overlap": head["e2e"].pop("overlap", None)}),
+                  flush=True)
             line = {
                 "metric": METRIC, "value": round(total_tflops, 2), "unit": "TFLOP/s",
                 "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(head["ms"], 4), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": "gqa_prefill_chunk: B=1 Hq=32 Hkv=8 D=128 Lq=512 "
-                                       "(positions 15872..16383) Lkv=16384 causal, bf16 "
-                                       "N(0,1)*0.5, scale 1/sqrt(128)",
-                           "flops_per_step": flops, "kv_splits": head["splits"],
+                "config": {"workload": WORKLOAD, "flops_per_step": flops,
+                           "parallelism": f"replica x{dist.world}", "kv_splits": head["splits"],
                            "l2": "flushed (512 MB write) before every timed step",
-                           "launch": head["mode"], "parallelism": f"replica x{dist.world}"},
-                "roofline": roofline("tensor", flops / (head["ms"] * 1e-3) / 1e12, pk["bf16"],
-                                     "TFLOP/s", traffic, pk),
+                           "launch": head["mode"]},
+                "roofline": head_rl,
                 "cpu_baseline": cpu,
                 "e2e": head["e2e"],
                 "gpu_launches": head["launches_per_step"] * args.steps,
                 "clocks": clk,
-                "p10_ms": round(head["p10_ms"], 4), "p90_ms": round(head["p90_ms"], 4),
-                "paths": paths,
+                "configs": configs,
             }
             print(json.dumps(line), flush=True)
     finally:

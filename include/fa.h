@@ -23,7 +23,10 @@
  *   - argument errors are detected on the host before anything is enqueued: the call
  *     returns a nonzero fa_status and fa_last_error() describes it.  Errors found on the
  *     device (a page id out of range, a wait that ran out) are recorded in a sticky status
- *     word read by fa_get_device_status(); the kernel skips the offending access.
+ *     word read by fa_get_device_status(); the kernel skips the offending access;
+ *   - the library keeps per-device facts for the life of the process (the SM count, kernel
+ *     attributes, the device addresses of its status word and scratch array), so a
+ *     cudaDeviceReset inside the process is not supported.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -113,9 +116,20 @@ int fa_prefill_num_splits(const fa_prefill_args* args);
  *            page page_table[b, t / page_size]; entries past the sequence are not read
  *   seq_lens [B] int32 (device), each in [0, max_seq_len]
  *   out [B, Hq, D] bf16;  lse [B, Hq] fp32 or NULL
- *   D in {64, 128, 256}; page_size a power of two; max_seq_len <= max_pages*page_size is a
- *   host-side bound used to size the grid (no device-to-host read).
- *   workspace >= fa_decode_workspace_size(B, Hq, D, max_seq_len) bytes.
+ *   D in {64, 128, 256}; Hq / Hkv <= 128; page_size a power of two; max_seq_len <=
+ *   max_pages*page_size is a host-side bound used to size the grid (no device-to-host read).
+ *   workspace >= fa_decode_workspace_size(B, Hq, D, max_seq_len) bytes (an upper bound over
+ *   both kernels below; fa_decode_get_plan gives the exact figure), 256-byte aligned.
+ * Two kernels serve it (fa_decode_get_plan says which one a call takes):
+ *   - CUDA cores: fixed chunks of fa_decode_chunk_tokens() tokens per CTA, each writing a
+ *     partial state, then the merge (fa_merge_states).  Power-of-two groups G = Hq / Hkv of
+ *     at most 16 with G * D <= 1024, any power-of-two page size;
+ *   - tensor cores: the paged attention kernel of fa_prefill_paged with one query per
+ *     sequence (the G heads of a kv head in one 128-row tile, tcgen05 MMAs), its KV loop split
+ *     and merged only when the (sequence, kv head) units cover less than half the SMs.  Any
+ *     G <= 128; page sizes that are powers of two from 8 to 128 (64 when D = 256).
+ *   The automatic choice takes the tensor cores when the units fill the GPU unsplit or when
+ *   the CUDA-core kernel cannot take G, the CUDA cores otherwise.
  */
 int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                     const int32_t* page_table, const int32_t* seq_lens, void* out, float* lse,
@@ -125,8 +139,15 @@ int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
 
 size_t fa_decode_workspace_size(int B, int Hq, int D, int max_seq_len);
 
+typedef enum fa_decode_path {
+  FA_DECODE_AUTO = 0,         /* the library chooses (see fa_decode_paged) */
+  FA_DECODE_CUDA_CORES = 1,   /* chunked split-KV kernel on the CUDA cores, then the merge */
+  FA_DECODE_TENSOR_CORES = 2  /* paged attention kernel on the tensor cores */
+} fa_decode_path;
+
 /* fa_decode_paged with the element type as an argument: the same fields, plus dtype
- * FA_BF16 or FA_FP16 for q, the pages and out (the split states and lse stay fp32). */
+ * FA_BF16 or FA_FP16 for q, the pages and out (the split states and lse stay fp32), and the
+ * kernel to use (FA_DECODE_AUTO unless a test or benchmark wants one of them). */
 typedef struct fa_decode_args {
   const void* q;
   const void* k_pages;
@@ -140,9 +161,23 @@ typedef struct fa_decode_args {
   fa_dtype dtype;
   void* workspace;
   size_t workspace_bytes;
+  fa_decode_path path;
 } fa_decode_args;
 
 int fa_decode_paged_ex(const fa_decode_args* args, void* stream);
+
+/* What a decode call with these arguments does on the current device: the kernel it runs
+ * (never FA_DECODE_AUTO), the KV splits per (sequence, kv head), the kernels it enqueues
+ * (a merge follows split work) and the workspace bytes it needs.  Only sizes, dtype and path
+ * are read.  Returns FA_OK, or the error the call itself would return for these sizes. */
+typedef struct fa_decode_plan {
+  fa_decode_path path;
+  int n_splits;
+  int launches;
+  size_t workspace_bytes;
+} fa_decode_plan;
+
+int fa_decode_get_plan(const fa_decode_args* args, fa_decode_plan* plan);
 
 /*
  * fa_decode_paged for callers that cannot allocate device memory (the pages describe no
@@ -151,10 +186,13 @@ int fa_decode_paged_ex(const fa_decode_args* args, void* stream);
  * device array inside the library, which every GPU that loads the library keeps reserved
  * until the process exits.  Use it where allocating is not possible, e.g. a runtime whose
  * arena allocator owns all device memory, or a serving loop that must not allocate.
- *   - Problems whose fa_decode_workspace_size(B, Hq, D, max_seq_len) exceeds 32 MiB are
- *     rejected with FA_ERR_WORKSPACE before anything is enqueued.
+ *   - The arguments are checked as fa_decode_paged checks them.  A problem whose scratch
+ *     (fa_decode_get_plan's workspace_bytes for these sizes, automatic path) exceeds 32 MiB
+ *     is then rejected with FA_ERR_WORKSPACE before anything is enqueued.
  *   - The first call on each device looks up the array's device address (a
- *     cudaGetSymbolAddress call); make that first call before any stream capture.
+ *     cudaGetSymbolAddress call) and keeps it for the life of the process; make that first
+ *     call before any stream capture, and do not use this entry point across a
+ *     cudaDeviceReset (the kept address may then no longer be the array's).
  *   - Calls make no allocation of any kind.
  *   - Every call uses the same array: two calls whose kernels overlap on the GPU (different
  *     streams, or different threads without ordering) race on it and give wrong results.
@@ -166,12 +204,12 @@ int fa_decode_paged_noalloc(const void* q, const void* k_pages, const void* v_pa
                             int max_pages_per_seq, int num_pages, int max_seq_len, float scale,
                             void* stream);
 
-/* Tokens per split-KV chunk that fa_decode_paged uses for these sizes on the current device
- * (a multiple of 64; depends only on B, Hq, max_seq_len and the SM count). */
+/* Tokens per split-KV chunk of the CUDA-core decode kernel for these sizes on the current
+ * device (a multiple of 64; depends only on B, Hq, max_seq_len and the SM count). */
 int fa_decode_chunk_tokens(int B, int Hq, int max_seq_len);
 
 /*
- * fa_decode_paged without the final merge: writes the split-KV state of every query row
+ * The CUDA-core decode kernel without the final merge: writes the split-KV state of every query row
  * r = b*Hq + h and chunk c (tokens [c*chunk, (c+1)*chunk) of the sequence, chunk =
  * fa_decode_chunk_tokens(B, Hq, max_seq_len)): the normalised partial output
  * o_parts[r, c, :] (fp32) and its log-sum-exp lse_parts[r, c] (natural log).  Chunks at or

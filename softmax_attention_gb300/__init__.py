@@ -34,6 +34,7 @@ EXPORTS = (
     "fa_prefill", "fa_prefill_ex", "fa_prefill_workspace_size", "fa_prefill_num_splits",
     "fa_prefill_paged", "fa_prefill_paged_workspace_size",
     "fa_decode_paged", "fa_decode_paged_ex", "fa_decode_workspace_size", "fa_decode_chunk_tokens",
+    "fa_decode_get_plan",
     "fa_decode_paged_noalloc",
     "fa_decode_paged_states", "mla_decode_paged", "mla_decode_workspace_size",
     "mla_decode_chunk_tokens", "mla_decode_paged_states", "mla_decode_paged_ex", "fa_merge_states",
@@ -71,8 +72,17 @@ class DecodeArgs(ctypes.Structure):
         ("page_size", ctypes.c_int), ("max_pages_per_seq", ctypes.c_int),
         ("num_pages", ctypes.c_int), ("max_seq_len", ctypes.c_int),
         ("scale", ctypes.c_float), ("dtype", ctypes.c_int), ("workspace", ctypes.c_void_p),
-        ("workspace_bytes", ctypes.c_size_t),
+        ("workspace_bytes", ctypes.c_size_t), ("path", ctypes.c_int),
     ]
+
+
+class DecodePlan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("n_splits", ctypes.c_int), ("launches", ctypes.c_int),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+# fa_decode_path
+FA_DECODE_AUTO, FA_DECODE_CUDA_CORES, FA_DECODE_TENSOR_CORES = 0, 1, 2
 
 
 class MlaArgs(ctypes.Structure):
@@ -120,6 +130,8 @@ def load_library(path: str | None = None):
         lib.fa_decode_paged.argtypes = [_vp] * 7 + [_i] * 8 + [_f, _vp, _sz, _vp]
         lib.fa_decode_paged_ex.restype = _i
         lib.fa_decode_paged_ex.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
+        lib.fa_decode_get_plan.restype = _i
+        lib.fa_decode_get_plan.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.POINTER(DecodePlan)]
         lib.mla_decode_paged_ex.restype = _i
         lib.mla_decode_paged_ex.argtypes = [ctypes.POINTER(MlaArgs), _vp]
         lib.fa_decode_workspace_size.restype = _sz
@@ -319,10 +331,41 @@ def fa_decode_workspace_size(B, Hq, D, max_seq_len) -> int:
     return load_library().fa_decode_workspace_size(B, Hq, D, max_seq_len)
 
 
+def decode_args(q, k_pages, v_pages, page_table, seq_lens, max_seq_len: int,
+                scale: float | None = None, out=None, lse=None, workspace=None,
+                path: int = FA_DECODE_AUTO) -> DecodeArgs:
+    """Argument struct of fa_decode_paged_ex (sizes from the tensors' shapes)."""
+    B, Hq, D = q.shape
+    num_pages, Hkv, page_size, _ = k_pages.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError(f"expected bfloat16 or float16, got {q.dtype}")
+    return DecodeArgs(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(seq_lens),
+                      _ptr(out), _ptr(lse), B, Hq, Hkv, D, page_size, page_table.shape[1],
+                      num_pages, int(max_seq_len), float(scale), _DT[q.dtype], _ptr(workspace),
+                      0 if workspace is None else workspace.numel() * workspace.element_size(),
+                      int(path))
+
+
+def fa_decode_get_plan(q, k_pages, v_pages, page_table, seq_lens, max_seq_len: int,
+                       path: int = FA_DECODE_AUTO) -> dict:
+    """What a decode call with these tensors does: {"path", "n_splits", "launches",
+    "workspace_bytes"} (path 1 = CUDA cores, 2 = tensor cores)."""
+    lib = load_library()
+    a = decode_args(q, k_pages, v_pages, page_table, seq_lens, max_seq_len, path=path)
+    pl = DecodePlan()
+    _check(lib.fa_decode_get_plan(ctypes.byref(a), ctypes.byref(pl)))
+    return {"path": pl.path, "n_splits": pl.n_splits, "launches": pl.launches,
+            "workspace_bytes": pl.workspace_bytes}
+
+
 def fa_decode_paged(q, k_pages, v_pages, page_table, seq_lens, max_seq_len: int,
-                    scale: float | None = None, out=None, lse=None, workspace=None, stream=None):
+                    scale: float | None = None, out=None, lse=None, workspace=None, stream=None,
+                    path: int = FA_DECODE_AUTO):
     """Split-KV paged GQA decode.  q [B,Hq,D] bf16 or fp16; pages [num_pages,Hkv,page_size,D]
-    in q's dtype; page_table [B,max_pages] int32; seq_lens [B] int32 (device)."""
+    in q's dtype; page_table [B,max_pages] int32; seq_lens [B] int32 (device).  path: 0 the
+    library's choice, 1 the CUDA-core kernel, 2 the tensor-core kernel."""
     lib = load_library()
     if q.dtype not in (torch.bfloat16, torch.float16):
         raise ValueError(f"expected bfloat16 or float16, got {q.dtype}")
@@ -330,9 +373,6 @@ def fa_decode_paged(q, k_pages, v_pages, page_table, seq_lens, max_seq_len: int,
     _need_dtype(torch.int32, page_table, seq_lens)
     _need_cuda(q, k_pages, v_pages, page_table, seq_lens)
     B, Hq, D = q.shape
-    num_pages, Hkv, page_size, _ = k_pages.shape
-    if scale is None:
-        scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -340,11 +380,11 @@ def fa_decode_paged(q, k_pages, v_pages, page_table, seq_lens, max_seq_len: int,
     _need_dtype(q.dtype, out)
     _need_dtype(torch.float32, lse)
     _need_cuda(out, lse)
-    ws = _workspace(lib.fa_decode_workspace_size(B, Hq, D, max_seq_len), q.device, workspace)
-    a = DecodeArgs(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(seq_lens),
-                   _ptr(out), _ptr(lse), B, Hq, Hkv, D, page_size, page_table.shape[1], num_pages,
-                   int(max_seq_len), float(scale), _DT[q.dtype], _ptr(ws),
-                   0 if ws is None else ws.numel())
+    need = fa_decode_get_plan(q, k_pages, v_pages, page_table, seq_lens, max_seq_len,
+                              path)["workspace_bytes"]
+    ws = _workspace(need, q.device, workspace)
+    a = decode_args(q, k_pages, v_pages, page_table, seq_lens, max_seq_len, scale, out, lse, ws,
+                    path)
     _check(lib.fa_decode_paged_ex(ctypes.byref(a), _stream(stream)))
     return out, lse
 

@@ -437,8 +437,22 @@ size_t fa_prefill_paged_workspace_size(int B, int Hq, int Hkv, int Lq, int D, in
 
 size_t fa_decode_workspace_size(int B, int Hq, int D, int max_seq_len) {
   if (B <= 0 || Hq <= 0 || D <= 0 || max_seq_len <= 0) return 0;
+  // Enough for either decode path whatever Hkv and the page size are: the CUDA-core path's
+  // chunk states, or the tensor-core path's split states, which are largest with one kv head
+  // (the fewest (sequence, kv head) units, so the most splits).
   const int chunk = decode_chunk(B, Hq, max_seq_len);
-  return split_ws_bytes((long)B * Hq, (max_seq_len + chunk - 1) / chunk, D);
+  const size_t cc = split_ws_bytes((long)B * Hq, (max_seq_len + chunk - 1) / chunk, D);
+  fa_prefill_args p;
+  memset(&p, 0, sizeof p);
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = 1;
+  p.Lq = 1;
+  p.Lkv = max_seq_len;
+  p.D = D;
+  p.dtype = FA_BF16;
+  const size_t tc = plan_prefill(&p).total_bytes;
+  return cc > tc ? cc : tc;
 }
 
 int fa_decode_chunk_tokens(int B, int Hq, int max_seq_len) {
@@ -455,13 +469,11 @@ int check_decode(const void* q, const void* k_pages, const void* v_pages, const 
                  int max_pages_per_seq, int num_pages, int max_seq_len, float scale) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
     return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: need B >= 0, Hq, Hkv > 0, Hq %% Hkv == 0");
-  const int G = Hq / Hkv;
   if (D != 64 && D != 128 && D != 256)
     return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: D must be 64, 128 or 256 (got %d)", D);
-  if (G > 16 || (G & (G - 1)) != 0 || G * D > 1024)
-    return fail(FA_ERR_UNSUPPORTED,
-                "fa_decode_paged: query heads per kv head must be a power of two with "
-                "G*D <= 1024 (got G=%d, D=%d)", G, D);
+  if (Hq / Hkv > 128)
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: query heads per kv head must be <= 128 (got %d)",
+                Hq / Hkv);
   if (page_size <= 0 || (page_size & (page_size - 1)) != 0)
     return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: page_size must be a power of two (got %d)",
                 page_size);
@@ -479,6 +491,114 @@ int check_decode(const void* q, const void* k_pages, const void* v_pages, const 
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages))
     return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: q, k_pages, v_pages must be 16-byte aligned");
   return FA_OK;
+}
+
+// The two decode kernels.  The CUDA-core split-KV kernel (decode.cu) takes power-of-two
+// groups of at most 16 query heads per kv head with G*D <= 1024 and any power-of-two page
+// size.  The paged attention kernel (prefill.cu with one query per sequence: the group's
+// heads packed into its 128-row tile, S and P V on the tensor cores) takes any group of at
+// most 128 heads and pages of 8 tokens up to its key tile.
+bool cc_decode_supports(int G, int D) { return G <= 16 && (G & (G - 1)) == 0 && G * D <= 1024; }
+
+bool tc_decode_supports(int G, int D, int page_size, int num_pages, int Hkv) {
+  return G <= 128 && page_size >= 8 && page_size <= prefill_block_n(D) &&
+         (page_size & (page_size - 1)) == 0 && (long)num_pages * Hkv <= 2147483647L;
+}
+
+// fa_prefill_ex arguments of a decode call on the tensor-core path: Lq = 1, the query being
+// the sequence's last position, so it sees all of the sequence's keys.
+fa_prefill_args decode_as_prefill(const fa_decode_args* a) {
+  fa_prefill_args p;
+  memset(&p, 0, sizeof p);
+  p.q = a->q;
+  p.k = a->k_pages;
+  p.v = a->v_pages;
+  p.out = a->out;
+  p.lse = a->lse;
+  p.B = a->B;
+  p.Hq = a->Hq;
+  p.Hkv = a->Hkv;
+  p.Lq = 1;
+  p.Lkv = a->max_seq_len;
+  p.D = a->D;
+  p.scale = a->scale;
+  p.dtype = a->dtype;
+  p.workspace = a->workspace;
+  p.workspace_bytes = a->workspace_bytes;
+  p.page_table = a->page_table;
+  p.seq_lens = a->seq_lens;
+  p.page_size = a->page_size;
+  p.max_pages = a->max_pages_per_seq;
+  p.num_pages = a->num_pages;
+  return p;
+}
+
+struct DecodePlan {
+  fa_decode_path path;
+  int chunk, n_chunks;   // CUDA-core path: tokens per chunk, chunks of the longest sequence
+  int n_splits;          // KV splits per (sequence, kv head)
+  int launches;
+  size_t ws_bytes;
+};
+
+// Chooses the kernel for a validated decode call.  Automatic choice: the tensor-core path
+// when the (sequence, kv head) units alone fill the GPU (its planner then splits nothing) or
+// when the CUDA-core kernel cannot take the group size; otherwise the CUDA-core kernel,
+// whose fixed-size chunks spread few long sequences over every SM.  No key at all
+// (max_seq_len == 0): only the merge runs, writing empty rows.
+int plan_decode(const fa_decode_args* a, DecodePlan* pl) {
+  const int G = a->Hq / a->Hkv;
+  const bool cc = cc_decode_supports(G, a->D);
+  const bool tc = tc_decode_supports(G, a->D, a->page_size, a->num_pages, a->Hkv);
+  memset(pl, 0, sizeof *pl);
+  if (a->path != FA_DECODE_AUTO && a->path != FA_DECODE_CUDA_CORES &&
+      a->path != FA_DECODE_TENSOR_CORES)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: unknown path %d", (int)a->path);
+  if (a->path == FA_DECODE_CUDA_CORES && !cc)
+    return fail(FA_ERR_UNSUPPORTED,
+                "fa_decode_paged: the CUDA-core path needs a power-of-two group of at most 16 "
+                "heads with G*D <= 1024 (got G=%d, D=%d)", G, a->D);
+  if (a->path == FA_DECODE_TENSOR_CORES && !tc)
+    return fail(FA_ERR_UNSUPPORTED,
+                "fa_decode_paged: the tensor-core path needs page_size a power of two in "
+                "[8, %d] (got %d)", prefill_block_n(a->D), a->page_size);
+  if (!cc && !tc)
+    return fail(FA_ERR_UNSUPPORTED,
+                "fa_decode_paged: G=%d needs the tensor-core path, which takes page sizes that "
+                "are powers of two in [8, %d] (got %d)", G, prefill_block_n(a->D), a->page_size);
+  const int sms = num_sms() > 0 ? num_sms() : 148;
+  bool use_tc = a->path == FA_DECODE_TENSOR_CORES ||
+                (a->path == FA_DECODE_AUTO && tc && (!cc || 2L * a->B * a->Hkv > sms));
+  if (a->max_seq_len == 0) {
+    pl->path = use_tc ? FA_DECODE_TENSOR_CORES : FA_DECODE_CUDA_CORES;
+    pl->launches = a->B > 0 ? 1 : 0;
+    return FA_OK;
+  }
+  if (use_tc) {
+    const fa_prefill_args p = decode_as_prefill(a);
+    const PrefillPlan pp = plan_prefill(&p);
+    pl->path = FA_DECODE_TENSOR_CORES;
+    pl->n_splits = pp.n_splits;
+    pl->launches = a->B > 0 ? 1 + (pp.n_splits > 1) : 0;
+    pl->ws_bytes = a->B > 0 ? pp.total_bytes : 0;
+    return FA_OK;
+  }
+  pl->path = FA_DECODE_CUDA_CORES;
+  pl->chunk = decode_chunk(a->B > 0 ? a->B : 1, a->Hq, a->max_seq_len);
+  pl->n_chunks = (a->max_seq_len + pl->chunk - 1) / pl->chunk;
+  pl->n_splits = pl->n_chunks;
+  pl->launches = a->B > 0 ? 2 : 0;
+  pl->ws_bytes = a->B > 0 ? split_ws_bytes((long)a->B * a->Hq, pl->n_chunks, a->D) : 0;
+  return FA_OK;
+}
+
+int check_decode_struct(const fa_decode_args* a) {
+  if (!a) return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: null argument struct");
+  if (a->dtype != FA_BF16 && a->dtype != FA_FP16)
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: dtype must be FA_BF16 or FA_FP16");
+  return check_decode(a->q, a->k_pages, a->v_pages, a->page_table, a->seq_lens, a->B, a->Hq,
+                      a->Hkv, a->D, a->page_size, a->max_pages_per_seq, a->num_pages,
+                      a->max_seq_len, a->scale);
 }
 
 cudaError_t decode_states(const void* q, const void* k_pages, const void* v_pages,
@@ -596,43 +716,73 @@ int merge_chunks(float* o_part, float* lse_part, const int32_t* seq_lens, int ro
 }
 
 }  // namespace
+
+int validate_decode_call(const fa_decode_args* a) {
+  int rc = check_decode_struct(a);
+  if (rc != FA_OK || a->B == 0) return rc;
+  if (!a->out || !aligned16(a->out))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: out must be a 16-byte aligned pointer");
+  return FA_OK;
+}
+
 }  // namespace fa
 
 extern "C" {
 
 int fa_decode_paged_ex(const fa_decode_args* a, void* stream) {
-  if (!a) return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: null argument struct");
-  if (a->dtype != FA_BF16 && a->dtype != FA_FP16)
-    return fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: dtype must be FA_BF16 or FA_FP16");
-  const int B = a->B, Hq = a->Hq, D = a->D, max_seq_len = a->max_seq_len;
-  int rc = check_decode(a->q, a->k_pages, a->v_pages, a->page_table, a->seq_lens, B, Hq, a->Hkv,
-                        D, a->page_size, a->max_pages_per_seq, a->num_pages, max_seq_len, a->scale);
-  if (rc != FA_OK || B == 0) return rc;
-  if (!a->out || !aligned16(a->out))
-    return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: out must be a 16-byte aligned pointer");
-  const int chunk = decode_chunk(B, Hq, max_seq_len > 0 ? max_seq_len : 1);
-  const int n_chunks = max_seq_len > 0 ? (max_seq_len + chunk - 1) / chunk : 0;
-  const size_t need = n_chunks > 0 ? split_ws_bytes((long)B * Hq, n_chunks, D) : 0;
-  if (need > 0 && (!a->workspace || a->workspace_bytes < need))
-    return fail(FA_ERR_WORKSPACE, "fa_decode_paged: workspace of %zu bytes needed (got %zu)", need,
-                a->workspace ? a->workspace_bytes : (size_t)0);
-  if (need > 0 && (reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0)
+  int rc = validate_decode_call(a);
+  if (rc != FA_OK || a->B == 0) return rc;
+  DecodePlan pl;
+  rc = plan_decode(a, &pl);
+  if (rc != FA_OK) return rc;
+  const int B = a->B, Hq = a->Hq, D = a->D;
+  if (pl.ws_bytes > 0 && (!a->workspace || a->workspace_bytes < pl.ws_bytes))
+    return fail(FA_ERR_WORKSPACE, "fa_decode_paged: workspace of %zu bytes needed (got %zu)",
+                pl.ws_bytes, a->workspace ? a->workspace_bytes : (size_t)0);
+  if (pl.ws_bytes > 0 && (reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0)
     return fail(FA_ERR_INVALID_ARG, "fa_decode_paged: workspace must be 256-byte aligned");
   uint32_t* status = device_status_ptr();
   if (!status) return fail(FA_ERR_CUDA, "fa_decode_paged: no usable CUDA device");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool f16 = a->dtype == FA_FP16;
+  if (pl.path == FA_DECODE_TENSOR_CORES && a->max_seq_len > 0) {
+    const fa_prefill_args p = decode_as_prefill(a);
+    return run_prefill(&p, st);
+  }
   float *o_part = nullptr, *lse_part = nullptr;
-  if (n_chunks > 0) {
-    carve(a->workspace, (long)B * Hq, n_chunks, D, &o_part, &lse_part);
+  if (pl.n_chunks > 0) {
+    carve(a->workspace, (long)B * Hq, pl.n_chunks, D, &o_part, &lse_part);
     cudaError_t e = decode_states(a->q, a->k_pages, a->v_pages, a->page_table, a->seq_lens,
-                                  o_part, lse_part, chunk, n_chunks, B, Hq, a->Hkv, D,
+                                  o_part, lse_part, pl.chunk, pl.n_chunks, B, Hq, a->Hkv, D,
                                   a->page_size, a->max_pages_per_seq, a->num_pages, a->scale,
                                   status, st, f16);
     if (e != cudaSuccess) return cuda_fail("fa_decode_paged (decode kernel)", e);
   }
-  return merge_chunks(o_part, lse_part, a->seq_lens, Hq, chunk, n_chunks, a->out, a->lse, B * Hq,
-                      D, st, "fa_decode_paged (merge kernel)", f16 ? Dtype::FP16 : Dtype::BF16);
+  // with no key anywhere (n_chunks == 0) the merge alone writes the empty rows
+  return merge_chunks(o_part, lse_part, a->seq_lens, Hq, pl.chunk, pl.n_chunks, a->out, a->lse,
+                      B * Hq, D, st, "fa_decode_paged (merge kernel)", f16 ? Dtype::FP16 : Dtype::BF16);
+}
+
+int fa_decode_get_plan(const fa_decode_args* a, fa_decode_plan* plan) {
+  if (!plan) return fail(FA_ERR_INVALID_ARG, "fa_decode_get_plan: null plan");
+  if (!a) return fail(FA_ERR_INVALID_ARG, "fa_decode_get_plan: null argument struct");
+  const fa_decode_args b = *a;
+  // sizes only: the pointers are not read
+  int rc = check_decode(reinterpret_cast<const void*>(4096), reinterpret_cast<const void*>(4096),
+                        reinterpret_cast<const void*>(4096), reinterpret_cast<const int32_t*>(4096),
+                        reinterpret_cast<const int32_t*>(4096), b.B, b.Hq, b.Hkv, b.D, b.page_size,
+                        b.max_pages_per_seq, b.num_pages, b.max_seq_len, b.scale);
+  if (rc == FA_OK && b.dtype != FA_BF16 && b.dtype != FA_FP16)
+    rc = fail(FA_ERR_UNSUPPORTED, "fa_decode_paged: dtype must be FA_BF16 or FA_FP16");
+  if (rc != FA_OK) return rc;
+  DecodePlan pl;
+  rc = plan_decode(&b, &pl);
+  if (rc != FA_OK) return rc;
+  plan->path = pl.path;
+  plan->n_splits = pl.n_splits;
+  plan->launches = pl.launches;
+  plan->workspace_bytes = pl.ws_bytes;
+  return FA_OK;
 }
 
 int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
@@ -642,7 +792,7 @@ int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                     size_t workspace_bytes, void* stream) {
   const fa_decode_args a = {q, k_pages, v_pages, page_table, seq_lens, out, lse, B, Hq, Hkv, D,
                             page_size, max_pages_per_seq, num_pages, max_seq_len, scale, FA_BF16,
-                            workspace, workspace_bytes};
+                            workspace, workspace_bytes, FA_DECODE_AUTO};
   return fa_decode_paged_ex(&a, stream);
 }
 
@@ -654,6 +804,10 @@ int fa_decode_paged_states(const void* q, const void* k_pages, const void* v_pag
   int rc = check_decode(q, k_pages, v_pages, page_table, seq_lens, B, Hq, Hkv, D, page_size,
                         max_pages_per_seq, num_pages, max_seq_len, scale);
   if (rc != FA_OK || B == 0 || max_seq_len == 0) return rc;
+  if (!cc_decode_supports(Hq / Hkv, D))
+    return fail(FA_ERR_UNSUPPORTED,
+                "fa_decode_paged_states: the split states come from the CUDA-core kernel, which "
+                "needs a power-of-two group of at most 16 heads with G*D <= 1024");
   const int chunk = decode_chunk(B, Hq, max_seq_len);
   const int want = (max_seq_len + chunk - 1) / chunk;
   if (n_chunks != want)
@@ -827,6 +981,6 @@ int fa_selftest_wait_timeout(unsigned timeout_us, void* stream) {
 
 const char* fa_last_error(void) { return g_err; }
 
-int fa_version(void) { return 300; }
+int fa_version(void) { return 400; }
 
 }  // extern "C"

@@ -12,7 +12,8 @@
 // its kNoAllocScratchBytes until the process exits.  Its address is a device address that
 // host code can only learn through cudaGetSymbolAddress (the array's name in host code is a
 // host-side stand-in, not a device pointer); that lookup happens once per device, on the
-// first call made with that device current.
+// first call made with that device current, and the address is kept for the life of the
+// process (a device reset inside the process is not supported; see include/fa.h).
 #include <cuda_runtime.h>
 #include <stdio.h>
 
@@ -68,23 +69,32 @@ extern "C" int fa_decode_paged_noalloc(const void* q, const void* k_pages, const
                                        void* out, float* lse, int B, int Hq, int Hkv, int D,
                                        int page_size, int max_pages_per_seq, int num_pages,
                                        int max_seq_len, float scale, void* stream) {
-  // The partial states this problem needs must fit the fixed array; larger problems are
-  // refused before anything touches the device.
-  const size_t need = fa_decode_workspace_size(B, Hq, D, max_seq_len);
-  if (need > fa::kNoAllocScratchBytes) {
+  fa_decode_args a = {q, k_pages, v_pages, page_table, seq_lens, out, lse, B, Hq, Hkv, D,
+                      page_size, max_pages_per_seq, num_pages, max_seq_len, scale, FA_BF16,
+                      nullptr, 0, FA_DECODE_AUTO};
+  // The arguments are checked first, exactly as fa_decode_paged checks them, so a malformed
+  // call gets the error that names its bad argument.
+  int rc = fa::validate_decode_call(&a);
+  if (rc != FA_OK || B == 0) return rc;
+  // The scratch this problem needs (the plan fa_decode_paged would follow) must fit the
+  // fixed array; larger problems are refused before anything touches the device.
+  fa_decode_plan plan;
+  rc = fa_decode_get_plan(&a, &plan);
+  if (rc != FA_OK) return rc;
+  if (plan.workspace_bytes > fa::kNoAllocScratchBytes) {
     char msg[256];
     snprintf(msg, sizeof msg,
              "fa_decode_paged_noalloc: this problem needs %zu bytes of scratch but the built-in "
              "array holds %zu; call fa_decode_paged with a caller workspace instead",
-             need, fa::kNoAllocScratchBytes);
+             plan.workspace_bytes, fa::kNoAllocScratchBytes);
     return fa::set_error(FA_ERR_WORKSPACE, msg);
   }
   void* scratch = nullptr;
-  int rc = fa::scratch_address(&scratch);
+  rc = fa::scratch_address(&scratch);
   if (rc != FA_OK) return rc;
-  // The decode kernel writes every partial state the merge later reads, so no part of the
+  // Both decode kernels write every partial state the merge later reads, so no part of the
   // array has to start at zero and stale contents from an earlier call are never read.
-  return fa_decode_paged(q, k_pages, v_pages, page_table, seq_lens, out, lse, B, Hq, Hkv, D,
-                         page_size, max_pages_per_seq, num_pages, max_seq_len, scale, scratch,
-                         fa::kNoAllocScratchBytes, stream);
+  a.workspace = scratch;
+  a.workspace_bytes = fa::kNoAllocScratchBytes;
+  return fa_decode_paged_ex(&a, stream);
 }

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+struct fa_decode_args;
+
 namespace fa {
 
 // Element types of the public ABI (same numbering as fa_dtype in include/fa.h).
@@ -128,6 +130,10 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 
 // fp32 -> fp16 element conversion (used for fp32 prefill inputs).
 cudaError_t launch_f32_to_f16(const float* src, void* dst, size_t n, cudaStream_t stream);
+
+// Checks a decode call's arguments (sizes, dtype, pointers, alignment of q, pages and out)
+// as fa_decode_paged_ex does; sets the error text and returns the fa_status code.
+int validate_decode_call(const fa_decode_args* a);
 
 // ---------------------------------------------------------------------------------------
 // Shared host helpers

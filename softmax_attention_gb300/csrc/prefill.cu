@@ -250,10 +250,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (lane == 0 && issued < n) {
-        // A wait ran out: let the copies already in flight land before the CTA exits.
+        // A wait ran out: let the copies already in flight land before the CTA exits.  A K
+        // issued without its V (k_only) reused the stage of K_{k_only - STAGES} and was issued
+        // only after S_{k_only - STAGES}, that older K's reader, had finished: the older K has
+        // landed, and its barrier may be two phases on, where a parity wait would read "not
+        // yet" and run out its limit.  It is not waited for.
         mbar_wait(bar_q, 0, nullptr);
         for (int jj = max(0, issued - STAGES); jj < issued; ++jj) {
-          mbar_wait(bar_k(jj % STAGES), (jj / STAGES) & 1, nullptr);
+          if (!(k_only >= 0 && jj == k_only - STAGES))
+            mbar_wait(bar_k(jj % STAGES), (jj / STAGES) & 1, nullptr);
           mbar_wait(bar_v(jj % STAGES), (jj / STAGES) & 1, nullptr);
         }
         if (k_only >= 0) mbar_wait(bar_k(k_only % STAGES), (k_only / STAGES) & 1, nullptr);

@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version(lib):
-    assert lib.fa_version() == 300  # 0.3.0: decode and MLA argument structs with a dtype
+    assert lib.fa_version() == 400  # 0.4.0: the decode path field and fa_decode_get_plan
 
 
 def _args(**kw):
@@ -101,8 +101,9 @@ def test_workspace_sizes_are_consistent(lib):
 
 @pytest.mark.parametrize("args,code", [
     (dict(D=80), fa.FA_ERR_UNSUPPORTED),
-    (dict(Hq=32, Hkv=1), fa.FA_ERR_UNSUPPORTED),    # G=32 > 16
-    (dict(Hq=12, Hkv=4), fa.FA_ERR_UNSUPPORTED),    # G=3 not a power of two
+    (dict(Hq=32, Hkv=1, page_size=4, max_pages=1024), fa.FA_ERR_UNSUPPORTED),  # G=32
+    (dict(Hq=12, Hkv=4, page_size=256), fa.FA_ERR_UNSUPPORTED),  # G=3: tensor cores only
+    (dict(Hq=256, Hkv=1), fa.FA_ERR_UNSUPPORTED),   # G > 128
     (dict(page_size=12), fa.FA_ERR_INVALID_ARG),
     (dict(max_seq_len=5000), fa.FA_ERR_INVALID_ARG),  # > max_pages * page_size
     (dict(ws_bytes=16), fa.FA_ERR_WORKSPACE),
@@ -192,3 +193,57 @@ def test_prefill_paged_workspace_follows_the_dense_plan(lib):
     assert lib.fa_prefill_paged_workspace_size(1, 8, 1, 16, 128, 16384) > 0
     assert lib.fa_prefill_paged_workspace_size(0, 8, 1, 16, 128, 16384) == 0
     assert lib.fa_prefill_paged_workspace_size(1, 8, 1, 16, 128, 0) == 0
+
+
+def _decode_args(**kw):
+    a = fa.DecodeArgs()
+    a.B, a.Hq, a.Hkv, a.D, a.page_size = 128, 32, 8, 128, 16
+    a.max_pages_per_seq, a.num_pages, a.max_seq_len = 256, 40000, 4096
+    a.scale, a.dtype = 0.1, fa.FA_BF16
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def _plan(lib, **kw):
+    pl = fa.DecodePlan()
+    rc = lib.fa_decode_get_plan(ctypes.byref(_decode_args(**kw)), ctypes.byref(pl))
+    return rc, pl
+
+
+def test_decode_plan_chooses_a_kernel(lib):
+    # 128 sequences x 8 kv heads fill the GPU: tensor cores, unsplit, no workspace
+    rc, pl = _plan(lib)
+    assert rc == fa.FA_OK
+    assert (pl.path, pl.n_splits, pl.launches, pl.workspace_bytes) == \
+        (fa.FA_DECODE_TENSOR_CORES, 1, 1, 0)
+    # few sequences: the chunked CUDA-core kernel and the merge, chunk states in the workspace
+    rc, pl = _plan(lib, B=2)
+    assert rc == fa.FA_OK and pl.path == fa.FA_DECODE_CUDA_CORES and pl.launches == 2
+    assert pl.workspace_bytes >= 2 * 32 * pl.n_splits * (128 + 1) * 4
+    # a group the CUDA-core kernel cannot take goes to the tensor cores even when small
+    rc, pl = _plan(lib, B=2, Hq=12, Hkv=4)
+    assert rc == fa.FA_OK and pl.path == fa.FA_DECODE_TENSOR_CORES
+    # page sizes the tensor-core kernel cannot take go to the CUDA cores
+    rc, pl = _plan(lib, page_size=1, max_pages_per_seq=4096)
+    assert rc == fa.FA_OK and pl.path == fa.FA_DECODE_CUDA_CORES
+    # forced paths, and their refusals
+    rc, pl = _plan(lib, path=fa.FA_DECODE_CUDA_CORES)
+    assert rc == fa.FA_OK and pl.path == fa.FA_DECODE_CUDA_CORES
+    assert _plan(lib, path=fa.FA_DECODE_TENSOR_CORES, page_size=4, max_pages_per_seq=1024)[0] \
+        == fa.FA_ERR_UNSUPPORTED
+    assert _plan(lib, path=fa.FA_DECODE_CUDA_CORES, Hq=24, Hkv=8)[0] == fa.FA_ERR_UNSUPPORTED
+    assert _plan(lib, path=7)[0] == fa.FA_ERR_INVALID_ARG
+
+
+def test_decode_workspace_size_bounds_every_plan(lib):
+    for B, Hq, Hkv, D, ps, L in ((2, 32, 8, 128, 16, 4096), (1, 12, 4, 128, 16, 9000),
+                                 (3, 8, 1, 256, 64, 20000), (128, 32, 8, 128, 16, 4096),
+                                 (5, 64, 4, 64, 8, 3000), (2, 8, 2, 128, 1, 1000)):
+        bound = lib.fa_decode_workspace_size(B, Hq, D, L)
+        for path in (fa.FA_DECODE_AUTO, fa.FA_DECODE_CUDA_CORES, fa.FA_DECODE_TENSOR_CORES):
+            rc, pl = _plan(lib, B=B, Hq=Hq, Hkv=Hkv, D=D, page_size=ps,
+                           max_pages_per_seq=-(-L // ps), num_pages=4096, max_seq_len=L,
+                           path=path)
+            if rc == fa.FA_OK:
+                assert pl.workspace_bytes <= bound, (B, Hq, Hkv, D, ps, L, path)

@@ -99,17 +99,22 @@ def run_protocol(n, stages, seed, *, paged_tail=False, mutate=None, fault=None):
             issued = j + 1
             yield ("delay", lat(0.0, 0.1))
         if issued < n:
-            # A wait ran out: let the copies still in flight land before the CTA exits.  These
-            # waits take the hardware's parity answer: when the producer stopped between a
-            # tile's K and V, that K reused the oldest drained tile's K stage, whose barrier is
-            # then two phases on, so the wait for the older K sees "not yet" and runs out its
-            # limit (the copies have landed; the end-of-run checks confirm nothing is in flight).
-            yield wait(lambda: bar_q.passed(0, hw=True))
+            # A wait ran out: let the copies still in flight land before the CTA exits.  When
+            # the producer stopped between a tile's K and V, that K (K_{k_only}) reused the
+            # stage of K_{k_only - stages}, and it was issued only after S_{k_only - stages},
+            # the reader of that older K, had finished: the older K has landed, and its
+            # barrier may already be two phases on, so the drain does not wait for it.  Every
+            # other drain wait is exact (the ambiguity check applies) and must not run out.
+            drain = [(bar_q, 0)]
             for jj in range(max(0, issued - stages), issued):
-                yield wait(lambda jj=jj: bar_k[jj % stages].passed(jj // stages, hw=True))
-                yield wait(lambda jj=jj: bar_v[jj % stages].passed(jj // stages, hw=True))
+                if not (k_only >= 0 and jj == k_only - stages and mutate != "drain_waits_stale_k"):
+                    drain.append((bar_k[jj % stages], jj // stages))
+                drain.append((bar_v[jj % stages], jj // stages))
             if k_only >= 0:
-                yield wait(lambda: bar_k[k_only % stages].passed(k_only // stages, hw=True))
+                drain.append((bar_k[k_only % stages], k_only // stages))
+            for bar, phase in drain:
+                if not (yield wait(lambda bar=bar, phase=phase: bar.passed(phase))):
+                    errors.add("drain ran out")
 
     def watcher():
         if watcher_k and mutate != "watcher_skips_k01":
@@ -307,3 +312,17 @@ def test_error_paths_end_with_nothing_in_flight(agent, stages):
         n = 7
         errors = run_protocol(n, stages, seed, fault=(agent, seed % n))
         assert agent in errors and len(errors) > 1
+        assert "drain ran out" not in errors
+
+
+def test_model_catches_drain_waiting_for_a_reused_k_stage():
+    # the drain's wait for the K whose stage the last K reused reads a barrier two phases on
+    def fails():
+        for seed in range(200):
+            for agent in ("softmax1", "mma", "watcher"):
+                try:
+                    run_protocol(7, 3, seed, mutate="drain_waits_stale_k", fault=(agent, seed % 7))
+                except Hazard:
+                    return True
+        return False
+    assert fails()
