@@ -18,6 +18,9 @@ silent):
 * ``mla_decode_paged``: latent-form MLA, where ckv serves as K and V and q_pe . kpe is added
   to each score ("perf: FlashAttention-3 style MLA PageAttention", change list item 4).
 * ``merge``: combination of attention states over disjoint key sets.
+* ``gated_delta``: the gated delta rule of gated-delta linear attention, evaluated one token
+  after another (``gdn_oracle.c``; "perf(kernels): speed up linear-attention prefill ~2.6x",
+  hip-ep PR, Test plan: the per-token oracle its chunked prefill kernel is checked against).
 """
 from __future__ import annotations
 
@@ -31,8 +34,11 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fa_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+_GD_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_GD_LIB_PATH = os.path.join(_HERE, "_build", "liboracle_gdn.so")
 _lock = threading.Lock()
 _lib = None
+_gd_lib = None
 
 _DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2, torch.float64: 3}
 
@@ -40,15 +46,36 @@ _i64 = ctypes.c_int64
 _p = ctypes.c_void_p
 
 
+def _build_one(src: str, lib: str, force: bool) -> str:
+    os.makedirs(os.path.dirname(lib), exist_ok=True)
+    if force or not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(src):
+        tmp = lib + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-o", tmp, src, "-lm"])
+        os.replace(tmp, lib)
+    return lib
+
+
 def build(force: bool = False) -> str:
-    """Compile fa_oracle.c into a shared library (gcc, -O2, OpenMP); return its path."""
-    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
-        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-        subprocess.check_call(
-            ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"])
-        os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    """Compile fa_oracle.c and gdn_oracle.c into shared libraries (gcc, -O2, OpenMP); return
+    the attention oracle's path."""
+    _build_one(_GD_SRC, _GD_LIB_PATH, force)
+    return _build_one(_SRC, _LIB_PATH, force)
+
+
+def _load_gd():
+    global _gd_lib
+    with _lock:
+        if _gd_lib is None:
+            # GDN_ORACLE_LIB lets the oracle's own mutation test point at a deliberately
+            # broken build of gdn_oracle.c; nothing else sets it.
+            path = os.environ.get("GDN_ORACLE_LIB") or _build_one(_GD_SRC, _GD_LIB_PATH, False)
+            lib = ctypes.CDLL(path)
+            lib.oracle_gated_delta.restype = ctypes.c_int
+            lib.oracle_gated_delta.argtypes = [
+                _p, _p, _p, ctypes.c_int, _p, _p, ctypes.c_int, _p,
+                _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_double, _p, _p]
+            _gd_lib = lib
+    return _gd_lib
 
 
 def _load():
@@ -270,3 +297,36 @@ def merge(o_parts, lse_parts):
     if rc != 0:
         raise ValueError("oracle_merge rejected its arguments")
     return out, lse
+
+
+def gated_delta(q, k, v, g, beta, *, scale=None, initial_state=None):
+    """Gated delta rule, token by token.  q, k [B,Hk,T,dk]; v [B,Hv,T,dv] (one dtype);
+    g (log decay), beta [B,Hv,T]; initial_state [B,Hv,dv,dk] or None (zero).  Value head h
+    reads query/key head h // (Hv // Hk).  Returns fp64 (out [B,Hv,T,dv], final state
+    [B,Hv,dv,dk])."""
+    lib = _load_gd()
+    q, k, v = _cpu(q), _cpu(k), _cpu(v)
+    g, beta = _cpu(g), _cpu(beta)
+    if not (q.dtype == k.dtype == v.dtype) or g.dtype != beta.dtype:
+        raise TypeError("q, k, v must share a dtype, and g, beta another")
+    B, Hk, T, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[3]
+    if k.shape != q.shape or v.shape != (B, Hv, T, dv) or g.shape != (B, Hv, T) or \
+            beta.shape != (B, Hv, T) or Hv % Hk:
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = dk ** -0.5
+    s0 = None
+    if initial_state is not None:
+        s0 = _cpu(initial_state).to(torch.float64)
+        if s0.shape != (B, Hv, dv, dk):
+            raise ValueError("initial_state must be [B,Hv,dv,dk]")
+    out = torch.empty(B, Hv, T, dv, dtype=torch.float64)
+    st = torch.empty(B, Hv, dv, dk, dtype=torch.float64)
+    rc = lib.oracle_gated_delta(q.data_ptr(), k.data_ptr(), v.data_ptr(), _code(q),
+                                g.data_ptr(), beta.data_ptr(), _code(g),
+                                s0.data_ptr() if s0 is not None else None,
+                                B, T, Hk, Hv, dk, dv, float(scale), out.data_ptr(), st.data_ptr())
+    if rc != 0:
+        raise ValueError("oracle_gated_delta rejected its arguments")
+    return out, st

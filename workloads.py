@@ -303,3 +303,58 @@ def causal_pairs(Lq: int, Lkv: int) -> int:
     for i in range(Lq):
         total += max(0, min(Lkv, i + off + 1))
     return total
+
+
+# ----------------------------------------------------------------------------------------
+# Gated-delta linear-attention prefill inputs (a second workload, not softmax attention)
+# ----------------------------------------------------------------------------------------
+@dataclass
+class GatedDeltaCase:
+    """q, k [B,Hk,T,dk] and v [B,Hv,T,dv] in `dtype`; g (log decay) and beta [B,Hv,T] fp32;
+    an optional fp32 initial state [B,Hv,dv,dk]."""
+    B: int
+    T: int
+    Hk: int
+    Hv: int
+    dk: int = 128
+    dv: int = 128
+    dtype: torch.dtype = torch.bfloat16
+    sigma_v: float = 1.0
+    g_min: float = -0.25
+    g_max: float = -0.005
+    with_state: bool = False
+    seed: int = 1
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.dk)
+
+
+def gated_delta_inputs(c: GatedDeltaCase):
+    """Returns (q, k, v, g, beta, initial_state or None).  Query and key rows are drawn
+    N(0,1), scaled to unit L2 norm in fp32 (the model normalises them before the recurrence)
+    and then rounded to `dtype`; v ~ N(0,1)*sigma_v; g ~ U(g_min, g_max) (decays
+    alpha = e^g of about 0.78..0.995); beta = sigmoid(N(0,1)); the initial state, when asked
+    for, ~ N(0,1)*0.1."""
+    g_ = _gen(c.seed)
+
+    def unit_rows(shape):
+        x = torch.randn(*shape, generator=g_, dtype=torch.float32)
+        return (x / x.norm(dim=-1, keepdim=True)).to(c.dtype)
+
+    q = unit_rows((c.B, c.Hk, c.T, c.dk))
+    k = unit_rows((c.B, c.Hk, c.T, c.dk))
+    v = normal((c.B, c.Hv, c.T, c.dv), c.sigma_v, c.dtype, g_)
+    g = c.g_min + (c.g_max - c.g_min) * torch.rand(c.B, c.Hv, c.T, generator=g_,
+                                                   dtype=torch.float32)
+    beta = torch.sigmoid(torch.randn(c.B, c.Hv, c.T, generator=g_, dtype=torch.float32))
+    s0 = None
+    if c.with_state:
+        s0 = normal((c.B, c.Hv, c.dv, c.dk), 0.1, torch.float32, g_)
+    return q, k, v, g, beta, s0
+
+
+def gated_delta_prefill(seed: int = 1) -> GatedDeltaCase:
+    """Chunked linear-attention prefill of the hip-ep PR's shape class: one 1842-token
+    sequence, dk = dv = 128, 16 query/key heads and 32 value heads, bf16, fp32 gates."""
+    return GatedDeltaCase(B=1, T=1842, Hk=16, Hv=32, seed=seed)
