@@ -407,6 +407,42 @@ def bench_decode(fa, c, steps, warmup, flush, dist, pk):
     return res
 
 
+def gated_delta_bytes(c: workloads.GatedDeltaCase) -> int:
+    """Algorithmic bytes of one call: q, k, v, g, beta read once, out and the final state
+    written once."""
+    qk = 2 * c.B * c.Hk * c.T * c.dk * 2
+    v_out = 2 * c.B * c.Hv * c.T * c.dv * 2
+    gb = 2 * c.B * c.Hv * c.T * 4
+    return qk + v_out + gb + c.B * c.Hv * c.dv * c.dk * 4
+
+
+def bench_gated_delta(fa, c, steps, warmup, flush, dist, pk):
+    """Gated-delta chunked prefill: the whole call (chunk preparation and the recurrence
+    kernel), KV GB/s of its algorithmic bytes against the HBM peak, and tokens per second."""
+    dev = torch.device("cuda")
+    q, k, v, g, beta, _ = (t.to(dev) if t is not None else None
+                           for t in workloads.gated_delta_inputs(c))
+    out = torch.empty(c.B, c.Hv, c.T, c.dv, dtype=torch.bfloat16, device=dev)
+    st = torch.empty(c.B, c.Hv, c.dv, c.dk, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, fa.gated_delta_workspace_size(q, k, v, g, beta)), dtype=torch.uint8,
+                     device=dev)
+
+    def call():
+        fa.gated_delta_prefill(q, k, v, g, beta, scale=c.scale, out=out, final_state=st,
+                               workspace=ws)
+
+    ms, _, mode = time_graph(call, steps, warmup, flush, dist)
+    f_ms = dist.max(statistics.mean(ms))
+    nbytes = gated_delta_bytes(c)
+    res = {"value": round(nbytes / (f_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms": round(f_ms, 4),
+           "tokens_per_s": round(c.B * c.T / (f_ms * 1e-3), 1), "bytes": nbytes,
+           "launches_per_step": 2, "mode": mode,
+           "roofline": roofline("hbm", nbytes / (f_ms * 1e-3) / 1e9, pk["hbm"], "GB/s", None, pk)}
+    del q, k, v, g, beta, out, st, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 MLA_GRID = ((128, 2048), (768, 1024), (64, 1024), (64, 2048), (128, 1024), (768, 2048))
 # the configured pair again with 64-token pages (page-sized TMA copies instead of row gathers)
 MLA_PAGED = ((128, 2048, 64), (768, 1024, 64))
@@ -596,7 +632,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="CPU time budget of the --impl reference run (all steps)")
-    ap.add_argument("--only", choices=("decode", "paged", "mla", "mqa"), default=None,
+    ap.add_argument("--only", choices=("decode", "paged", "mla", "mqa", "gdn"), default=None,
                     help="run the headline plus only this path (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -662,6 +698,11 @@ def main():
                 r = bench_prefill_paged(fa, ppc, sub, args.warmup, flush, dist, pk)
                 paths["paged_gqa_prefill"] = r
                 configs["N1"] = summary(r["value"], "TFLOP/s", r["ms"], r["ms"], r["roofline"])
+            if want("gdn"):
+                gc = workloads.gated_delta_prefill(seed=1 + dist.rank)
+                r = bench_gated_delta(fa, gc, sub, args.warmup, flush, dist, pk)
+                paths["gated_delta_prefill"] = r
+                configs["N3"] = summary(r["value"], "GB/s", r["ms"], r["ms"], r["roofline"])
         clk = clocks.stop() if dist.rank == 0 else None
         flops = head["flops"]
         total_tflops = dist.world * flops / (head["ms"] * 1e-3) / 1e12

@@ -311,6 +311,47 @@ int fa_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
 size_t fa_prefill_paged_workspace_size(int B, int Hq, int Hkv, int Lq, int D, int max_seq_len);
 
 /*
+ * Gated-delta linear attention, chunked prefill: the gated-delta chunked linear-attention
+ * prefill of hip-ep PR "perf(kernels): speed up linear-attention prefill ~2.6x" (Summary;
+ * checked there against a per-token oracle).  The page does not write the recurrence; the
+ * one computed is the gated delta rule (Gated Delta Networks, 2024), per value head h with a
+ * state S of dv rows by dk columns:
+ *     S_t = S_{t-1} alpha_t (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   alpha_t = e^{g_t}
+ *     o_t = S_t (scale q_t)
+ * Value head h reads query/key head h / (Hv / Hk).  S starts from initial_state (or zero);
+ * the state after the last token is written to final_state when given.  L2 normalisation of
+ * q and k, which models apply before the recurrence, is the caller's.
+ *   q, k [B, Hk, T, dk] bf16;  v [B, Hv, T, dv] bf16;  g, beta [B, Hv, T] fp32
+ *   initial_state, final_state [B, Hv, dv, dk] fp32 or NULL;  out [B, Hv, T, dv] bf16
+ *   dk == dv == 128; Hv % Hk == 0; B * Hv * (T + 64) < 2^31.
+ *   workspace >= gated_delta_workspace_size(args) bytes, 256-byte aligned (chunk operands:
+ *   about 0.9 KB per token and value head).
+ * The prefill runs in 64-token chunks: a kernel prepares every chunk of every head in
+ * parallel, then one CTA per (batch, value head) carries the state through its chunks on the
+ * tensor cores (bf16 operands, fp32 accumulation and state).
+ */
+typedef struct gated_delta_args {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  const float* initial_state;
+  void* out;
+  float* final_state;
+  int B, T, Hk, Hv, dk, dv;
+  float scale;           /* applied to q; 1/sqrt(dk) is the usual value */
+  fa_dtype dtype;        /* FA_BF16 */
+  void* workspace;
+  size_t workspace_bytes;
+} gated_delta_args;
+
+int gated_delta_prefill(const gated_delta_args* args, void* stream);
+
+/* Workspace bytes gated_delta_prefill needs for these sizes (pointers are not read). */
+size_t gated_delta_workspace_size(const gated_delta_args* args);
+
+/*
  * Merge of attention states over disjoint key sets (the split-KV combine):
  *   lse = ln sum_s e^{lse_s},   out = sum_s e^{lse_s - lse} o_s
  *   o_parts [rows, max_splits, D] fp32 (normalised partial outputs), lse_parts

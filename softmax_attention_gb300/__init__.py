@@ -39,6 +39,7 @@ EXPORTS = (
     "fa_decode_paged_states", "mla_decode_paged", "mla_decode_workspace_size",
     "mla_decode_chunk_tokens", "mla_decode_paged_states", "mla_decode_paged_ex", "fa_merge_states",
     "fa_get_device_status", "fa_selftest_wait_timeout", "fa_last_error", "fa_version",
+    "gated_delta_prefill", "gated_delta_workspace_size",
 )
 
 
@@ -95,6 +96,18 @@ class MlaArgs(ctypes.Structure):
         ("page_size", ctypes.c_int), ("max_pages_per_seq", ctypes.c_int),
         ("num_pages", ctypes.c_int), ("max_seq_len", ctypes.c_int),
         ("scale", ctypes.c_float), ("dtype", ctypes.c_int), ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+class GatedDeltaArgs(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("initial_state", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("final_state", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("T", ctypes.c_int), ("Hk", ctypes.c_int), ("Hv", ctypes.c_int),
+        ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("scale", ctypes.c_float),
+        ("dtype", ctypes.c_int), ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
     ]
 
@@ -160,6 +173,10 @@ def load_library(path: str | None = None):
         lib.fa_last_error.argtypes = []
         lib.fa_version.restype = _i
         lib.fa_version.argtypes = []
+        lib.gated_delta_prefill.restype = _i
+        lib.gated_delta_prefill.argtypes = [ctypes.POINTER(GatedDeltaArgs), _vp]
+        lib.gated_delta_workspace_size.restype = _sz
+        lib.gated_delta_workspace_size.argtypes = [ctypes.POINTER(GatedDeltaArgs)]
         _lib = lib
         return lib
 
@@ -536,3 +553,48 @@ def fa_selftest_wait_timeout(timeout_us: int, stream=None) -> int:
 
 def fa_last_error() -> str:
     return load_library().fa_last_error().decode(errors="replace")
+
+
+def gated_delta_args(q, k, v, g, beta, *, scale=None, initial_state=None, out=None,
+                     final_state=None, workspace=None) -> GatedDeltaArgs:
+    """Argument struct of gated_delta_prefill (sizes from the tensors' shapes)."""
+    B, Hk, T, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[3]
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    if q.dtype not in _DT:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    return GatedDeltaArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                          _ptr(out), _ptr(final_state), B, T, Hk, Hv, dk, dv, float(scale),
+                          _DT[q.dtype], _ptr(workspace),
+                          0 if workspace is None else workspace.numel() * workspace.element_size())
+
+
+def gated_delta_workspace_size(q, k, v, g, beta) -> int:
+    return load_library().gated_delta_workspace_size(
+        ctypes.byref(gated_delta_args(q, k, v, g, beta)))
+
+
+def gated_delta_prefill(q, k, v, g, beta, *, scale=None, initial_state=None, out=None,
+                        final_state=None, want_state=True, workspace=None, stream=None):
+    """Chunked prefill of gated-delta linear attention.  q, k [B,Hk,T,dk] bf16; v [B,Hv,T,dv]
+    bf16; g (log decay), beta [B,Hv,T] fp32; initial_state [B,Hv,dv,dk] fp32 or None.
+    Returns (out [B,Hv,T,dv] bf16, final state [B,Hv,dv,dk] fp32 or None)."""
+    lib = load_library()
+    _need_dtype(torch.bfloat16, q, k, v, out)
+    _need_dtype(torch.float32, g, beta, initial_state, final_state)
+    _need_cuda(q, k, v, g, beta, initial_state, out, final_state)
+    B, Hk, T, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[3]
+    if out is None:
+        out = torch.empty(B, Hv, T, dv, dtype=torch.bfloat16, device=q.device)
+    if final_state is None and want_state:
+        final_state = torch.empty(B, Hv, dv, dk, dtype=torch.float32, device=q.device)
+    a = gated_delta_args(q, k, v, g, beta, scale=scale, initial_state=initial_state, out=out,
+                         final_state=final_state)
+    ws = _workspace(lib.gated_delta_workspace_size(ctypes.byref(a)), q.device, workspace)
+    if ws is not None:
+        a.workspace = ws.data_ptr()
+        a.workspace_bytes = ws.numel() * ws.element_size()
+    _check(lib.gated_delta_prefill(ctypes.byref(a), _stream(stream)))
+    return out, final_state

@@ -1,0 +1,642 @@
+// gated_delta.cu -- chunked prefill of gated-delta linear attention on sm_103a.
+//
+// The hip-ep PR "perf(kernels): speed up linear-attention prefill ~2.6x" (Summary) speeds up
+// a gated-delta chunked linear-attention prefill; the recurrence it computes is the gated
+// delta rule, with a state S of dv rows by dk columns per value head:
+//   S_t = S_{t-1} alpha_t (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   o_t = S_t (scale q_t)
+// with alpha_t = exp(g_t).  Over a chunk of C = 64 tokens with cumulative log decays
+// gamma_i = g_1 + ... + g_i (Gamma_i = e^gamma_i) and the state S entering the chunk, the
+// chunk's writes u_i = beta_i (v_i - alpha_i S_{i-1} k_i) satisfy
+//   (I + A) U = beta (V - Gamma K S^T),   A_ij = beta_i (Gamma_i / Gamma_j) k_i.k_j (j < i)
+// so, with X = (I + A)^-1 applied to beta Gamma K (= W) and to beta V (= U~):
+//   U = U~ - W S^T
+//   O = Gamma (scale Q) S^T + P U,        P_ij = scale (Gamma_i / Gamma_j) q_i.k_j (j <= i)
+//   S <- Gamma_C S + U^T (Gamma_C / Gamma_j) K
+// Two kernels:
+//   1. chunk preparation (every chunk of every head in parallel, CUDA cores, fp32): the
+//      Gram products K K^T and Q K^T, the triangular solve for W and U~ (each thread one
+//      right-hand-side column, held in registers), P; written to a workspace (W and P in
+//      bf16 as tensor-core operands, U~ and the decays in fp32);
+//   2. the recurrence across chunks (one CTA per (batch, value head), tensor cores): the state
+//      lives in tensor memory in fp32 (dv lanes x dk columns), with a bf16 copy in shared
+//      memory as the A operand; per chunk  U^T = U~^T - S W^T,  O^T = S Q^T (scaled per token)
+//      + U^T P^T,  S += (U^T scaled per token) K,  with the chunk's W, Q, K and P streamed by
+//      TMA through a two-stage ring.
+// The output O and the final state are written per chunk; no chunk's state is kept.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/fa.h"
+#include "internal.h"
+#include "sm103.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kC = 64;     // tokens per chunk
+constexpr int kDk = 128;
+constexpr int kDv = 128;
+
+struct GdnParams {
+  const uint16_t* q;     // [B,Hk,T,dk] bf16
+  const uint16_t* k;     // [B,Hk,T,dk] bf16
+  const uint16_t* v;     // [B,Hv,T,dv] bf16
+  const float* g;        // [B,Hv,T]
+  const float* beta;     // [B,Hv,T]
+  const float* s0;       // [B,Hv,dv,dk] or nullptr
+  uint16_t* out;         // [B,Hv,T,dv] bf16
+  float* s_final;        // [B,Hv,dv,dk] or nullptr
+  int B, T, Hk, Hv, n_chunks, Tpad;
+  float scale;
+  uint16_t* w_ws;        // [B*Hv*Tpad, dk] bf16
+  float* u_ws;           // [B*Hv*Tpad, dv] fp32
+  uint16_t* p_ws;        // [B*Hv*Tpad, C] bf16 (rows of each chunk's P)
+  float* gam_ws;         // [B*Hv*Tpad] fp32 cumulative log decay within the chunk
+  uint32_t* status;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// ------------------------------------------------------------------------------------------
+// Kernel 1: chunk preparation.  One CTA per (chunk, value head, batch), 256 threads.
+// ------------------------------------------------------------------------------------------
+constexpr int kPrepThreads = 256;
+constexpr int kRowF = kDk + 4;    // padded fp32 row of a K/Q/V tile in shared memory
+constexpr int kTriF = kC + 4;     // padded fp32 row of A and P (float4-aligned)
+constexpr int kPrepSmem = (2 * kC * kRowF + 2 * kC * kTriF + 3 * kC) * 4;
+
+__global__ void __launch_bounds__(kPrepThreads, 2) gdn_prep_kernel(const GdnParams p) {
+  extern __shared__ __align__(16) float sm[];
+  float* Ks = sm;                      // [C][kRowF]
+  float* QVs = Ks + kC * kRowF;        // [C][kRowF]: Q, then V
+  float* As = QVs + kC * kRowF;        // [C][kTriF]
+  float* Ps = As + kC * kTriF;         // [C][kTriF]
+  float* gam = Ps + kC * kTriF;        // [C]
+  float* bet = gam + kC;               // [C]
+  float* graw = bet + kC;              // [C]
+
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  const int hk = h / (p.Hv / p.Hk);
+  const int t0 = c * kC, n = min(kC, p.T - t0);
+  const size_t bh = static_cast<size_t>(b) * p.Hv + h;
+  const uint16_t* krow = p.k + (static_cast<size_t>(b * p.Hk + hk) * p.T + t0) * kDk;
+  const uint16_t* qrow = p.q + (static_cast<size_t>(b * p.Hk + hk) * p.T + t0) * kDk;
+  const uint16_t* vrow = p.v + (bh * p.T + t0) * kDv;
+
+  // rows of 128 bf16 -> fp32 shared-memory rows; rows past the sequence are zero
+  auto load_rows = [&](const uint16_t* src, float* dst) {
+    for (int e = tid; e < kC * (kDk / 8); e += kPrepThreads) {
+      const int r = e / (kDk / 8), c8 = (e % (kDk / 8)) * 8;
+      uint4 w = make_uint4(0, 0, 0, 0);
+      if (r < n) w = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * kDk + c8);
+      float4* d = reinterpret_cast<float4*>(dst + r * kRowF + c8);
+      d[0] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+      d[1] = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+    }
+  };
+  load_rows(krow, Ks);
+  load_rows(qrow, QVs);
+  if (tid < kC) {
+    const bool ok = tid < n;
+    graw[tid] = ok ? p.g[bh * p.T + t0 + tid] : 0.f;   // padding: no decay, no write
+    bet[tid] = ok ? p.beta[bh * p.T + t0 + tid] : 0.f;
+  }
+  __syncthreads();
+  // cumulative log decay within the chunk (inclusive scan by warp 0, two tokens per lane)
+  if (tid < 32) {
+    const float a = graw[2 * tid], a2 = graw[2 * tid + 1];
+    float s = a + a2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, s, o);
+      if (tid >= o) s += y;
+    }
+    const float excl = s - (a + a2);
+    gam[2 * tid] = excl + a;
+    gam[2 * tid + 1] = excl + a + a2;
+  }
+  __syncthreads();
+
+  // Gram products: thread (ti, tj) computes rows ti + 16a and columns tj + 16b (a, b < 4)
+  {
+    const int ti = tid & 15, tj = tid >> 4;
+    float kk[4][4], qk[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) kk[a][bb] = qk[a][bb] = 0.f;
+#pragma unroll 2
+    for (int d = 0; d < kDk; d += 4) {
+      float4 ki[4], qi[4], kj[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        ki[a] = *reinterpret_cast<const float4*>(Ks + (ti + 16 * a) * kRowF + d);
+        qi[a] = *reinterpret_cast<const float4*>(QVs + (ti + 16 * a) * kRowF + d);
+        kj[a] = *reinterpret_cast<const float4*>(Ks + (tj + 16 * a) * kRowF + d);
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) {
+          kk[a][bb] += ki[a].x * kj[bb].x + ki[a].y * kj[bb].y + ki[a].z * kj[bb].z + ki[a].w * kj[bb].w;
+          qk[a][bb] += qi[a].x * kj[bb].x + qi[a].y * kj[bb].y + qi[a].z * kj[bb].z + qi[a].w * kj[bb].w;
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        const int i = ti + 16 * a, j = tj + 16 * bb;
+        const float r = j <= i ? expf(gam[i] - gam[j]) : 0.f;
+        As[i * kTriF + j] = j < i ? bet[i] * r * kk[a][bb] : 0.f;
+        Ps[i * kTriF + j] = (j <= i && i < n) ? p.scale * r * qk[a][bb] : 0.f;
+      }
+  }
+  __syncthreads();
+  // P to the workspace as bf16 (row-major, 128 bytes per row), then V over Q
+  {
+    uint16_t* pdst = p.p_ws + (bh * p.Tpad + t0) * kC;
+    for (int e = tid; e < kC * kC / 8; e += kPrepThreads) {
+      const int r = e / (kC / 8), c8 = (e % (kC / 8)) * 8;
+      const float* s = Ps + r * kTriF + c8;
+      *reinterpret_cast<uint4*>(pdst + r * kC + c8) =
+          make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]), pack_bf16x2(s[4], s[5]),
+                     pack_bf16x2(s[6], s[7]));
+    }
+  }
+  load_rows(vrow, QVs);
+  __syncthreads();
+
+  // Triangular solve (I + A) X = R by forward substitution, one right-hand-side column per
+  // thread, the column in registers: columns 0..127 give W (R = beta Gamma K), columns
+  // 128..255 give U~ (R = beta V).  A's rows are read as broadcast float4s; entries at and
+  // above the diagonal are zero, so every row runs over whole groups of four.
+  {
+    const bool wcol = tid < kDk;
+    const float* rsrc = wcol ? Ks + tid : QVs + (tid - kDk);
+    float x[kC];
+#pragma unroll
+    for (int i = 0; i < kC; ++i) x[i] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kC; ++i) {
+      float acc = bet[i] * rsrc[i * kRowF];
+      if (wcol) acc *= expf(gam[i]);
+#pragma unroll
+      for (int m4 = 0; m4 < (i + 3) / 4; ++m4) {
+        const float4 a = *reinterpret_cast<const float4*>(As + i * kTriF + 4 * m4);
+        acc -= a.x * x[4 * m4] + a.y * x[4 * m4 + 1] + a.z * x[4 * m4 + 2] + a.w * x[4 * m4 + 3];
+      }
+      x[i] = acc;
+    }
+    const size_t row0 = bh * p.Tpad + t0;
+    if (wcol) {
+      uint16_t* wdst = p.w_ws + row0 * kDk + tid;
+#pragma unroll
+      for (int i = 0; i < kC; ++i) {
+        const __nv_bfloat16 hv = __float2bfloat16_rn(x[i]);
+        wdst[static_cast<size_t>(i) * kDk] = *reinterpret_cast<const uint16_t*>(&hv);
+      }
+    } else {
+      float* udst = p.u_ws + row0 * kDv + (tid - kDk);
+#pragma unroll
+      for (int i = 0; i < kC; ++i) udst[static_cast<size_t>(i) * kDv] = x[i];
+    }
+    if (tid < kC) p.gam_ws[row0 + tid] = gam[tid];
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Kernel 2: the recurrence across chunks.  One CTA per (value head, batch), 192 threads:
+// warps 0-3 own the state rows (thread d = tensor-memory lane d = value dim d), warp 4 loads
+// the chunk operands with TMA, warp 5 issues the MMAs and owns the tensor memory.
+// ------------------------------------------------------------------------------------------
+constexpr int kStateThreads = 192;
+constexpr int kBlkTok = kC * 128;                // one 64-column block of a 64-row tile
+constexpr int kStageW = 0;
+constexpr int kStageQ = kStageW + 2 * kBlkTok;
+constexpr int kStageK = kStageQ + 2 * kBlkTok;
+constexpr int kStageP = kStageK + 2 * kBlkTok;
+constexpr int kStageBytes = kStageP + kBlkTok;   // 57344: W, Q, K (16 KB each), P (8 KB)
+constexpr int kSbfOff = 2 * kStageBytes;         // S as bf16, [128 rows][2 blocks of 128 B]
+constexpr int kSBlk = kDv * 128;                 // 16384: one 64-column block of S
+constexpr int kUtOff = kSbfOff + 2 * kSBlk;      // U^T, [128 rows][128 B]
+constexpr int kUptOff = kUtOff + kSBlk;          // U^T with each token's decay to the chunk end
+constexpr int kGamOff = kUptOff + kSBlk;         // two chunks' decays, fp32
+constexpr int kBarOff = kGamOff + 2 * kC * 4;
+// full[2], empty[2], s_ready, u_ready, u_done, o_done, mma_done
+constexpr int kNumBars = 9;
+constexpr int kStateSmem = kBarOff + kNumBars * 8 + 16 + 1024;
+static_assert(kStateSmem <= 232448, "shared memory budget");
+constexpr uint32_t kTmS = 0, kTmU = 128, kTmO1 = 192, kTmO2 = 256;
+
+__device__ __forceinline__ void state_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__global__ void __launch_bounds__(kStateThreads, 1)
+    gdn_state_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_p,
+                     const GdnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t s_base = smem_addr(smem);
+  const uint32_t bars = s_base + kBarOff;
+  auto bar_full = [&](int s) { return bars + 8u * s; };
+  auto bar_empty = [&](int s) { return bars + 8u * (2 + s); };
+  const uint32_t bar_sready = bars + 8u * 4, bar_uready = bars + 8u * 5;
+  const uint32_t bar_udone = bars + 8u * 6, bar_odone = bars + 8u * 7, bar_done = bars + 8u * 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + kNumBars * 8);
+  float* gam_s = reinterpret_cast<float*>(smem + kGamOff);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int hk = h / (p.Hv / p.Hk);
+  const size_t bh = static_cast<size_t>(b) * p.Hv + h;
+  const int nc = p.n_chunks;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    mbar_init(bar_sready, 128);
+    mbar_init(bar_uready, 128);
+    mbar_init(bar_udone, 1);
+    mbar_init(bar_odone, 1);
+    mbar_init(bar_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ---------------------------------- TMA producer ------------------------------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_w);
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_p);
+      int issued = 0;
+      for (int c = 0; c < nc; ++c) {
+        const int st = c & 1;
+        if (c >= 2 && !mbar_wait(bar_empty(st), ((c >> 1) - 1) & 1, p.status)) break;
+        const uint32_t base = s_base + st * kStageBytes;
+        const int row = static_cast<int>(bh * p.Tpad) + c * kC;
+        mbar_arrive_expect_tx(bar_full(st), kStageBytes);
+        for (int cb = 0; cb < 2; ++cb) {
+          tma_load_2d(base + kStageW + cb * kBlkTok, &tm_w, bar_full(st), cb * 64, row);
+          tma_load_3d(base + kStageQ + cb * kBlkTok, &tm_q, bar_full(st), cb * 64, c * kC, b * p.Hk + hk);
+          tma_load_3d(base + kStageK + cb * kBlkTok, &tm_k, bar_full(st), cb * 64, c * kC, b * p.Hk + hk);
+        }
+        tma_load_2d(base + kStageP, &tm_p, bar_full(st), 0, row);
+        issued = c + 1;
+      }
+      // a wait ran out: let the copies in flight land before the CTA exits
+      for (int c = max(0, issued - 2); c < issued && issued < nc; ++c)
+        mbar_wait(bar_full(c & 1), (c >> 1) & 1, nullptr);
+    }
+  } else if (warp == 5) {
+    // ---------------------------------- MMA issuer --------------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_n64 = idesc_f16(true, 128, 64, false, false);
+      constexpr uint32_t idesc_s = idesc_f16(true, 128, 128, false, true);
+      const uint32_t sbf = s_base + kSbfOff, ut = s_base + kUtOff, upt = s_base + kUptOff;
+      bool ok = true;
+      for (int c = 0; ok && c < nc; ++c) {
+        const int st = c & 1;
+        const uint32_t base = s_base + st * kStageBytes;
+        if (!(ok = mbar_wait(bar_full(st), (c >> 1) & 1, p.status))) break;
+        if (!(ok = mbar_wait(bar_sready, c & 1, p.status))) break;
+        tc_fence_after();
+        // S W^T -> D_U (M = 128 value dims, N = 64 tokens, K = 128 key dims)
+#pragma unroll
+        for (int kk = 0; kk < kDk / 16; ++kk) {
+          const uint32_t off = (kk / 4) * kSBlk + (kk % 4) * 32;
+          mma_ss(tmem + kTmU, sdesc_sw128(sbf + off, 16, 1024),
+                 sdesc_sw128(base + kStageW + (kk / 4) * kBlkTok + (kk % 4) * 32, 16, 1024),
+                 idesc_n64, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bar_udone);
+        // S Q^T -> D_O1
+#pragma unroll
+        for (int kk = 0; kk < kDk / 16; ++kk) {
+          const uint32_t off = (kk / 4) * kSBlk + (kk % 4) * 32;
+          mma_ss(tmem + kTmO1, sdesc_sw128(sbf + off, 16, 1024),
+                 sdesc_sw128(base + kStageQ + (kk / 4) * kBlkTok + (kk % 4) * 32, 16, 1024),
+                 idesc_n64, kk > 0 ? 1u : 0u);
+        }
+        if (!(ok = mbar_wait(bar_uready, c & 1, p.status))) break;
+        tc_fence_after();
+        // U^T P^T -> D_O2 (N = 64 query tokens, K = 64 key tokens)
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk)
+          mma_ss(tmem + kTmO2, sdesc_sw128(ut + kk * 32, 16, 1024),
+                 sdesc_sw128(base + kStageP + kk * 32, 16, 1024), idesc_n64, kk > 0 ? 1u : 0u);
+        // D_S += U'^T K (N = 128 key dims, K = 64 tokens; K read MN-major)
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk)
+          mma_ss(tmem + kTmS, sdesc_sw128(upt + kk * 32, 16, 1024),
+                 sdesc_sw128(base + kStageK + kk * 2048, kBlkTok, 1024), idesc_s, 1u);
+        tc_commit(bar_odone);
+        tc_commit(bar_empty(st));
+      }
+      tc_commit(bar_done);
+      mbar_wait(bar_done, 0, nullptr);
+    }
+  } else {
+    // ------------------------- state rows: thread d = value dim d -----------------------
+    const int d = threadIdx.x;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    uint8_t* sbf = smem + kSbfOff;
+    uint8_t* utp = smem + kUtOff;
+    uint8_t* uptp = smem + kUptOff;
+    const float* gam_g = p.gam_ws + bh * p.Tpad;
+    // Row d of a K-major 128-byte-swizzled tile: 16-byte chunk ch sits at chunk ch ^ (d % 8).
+    auto put_row32 = [&](uint8_t* blk, int ch0, const float (&v)[32]) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(blk + d * 128 + (((ch0 + q) ^ (d & 7)) * 16)) =
+            make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                       pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+    };
+    // The state entering chunk 0: the initial state (or zero) as the bf16 operand, and in
+    // tensor memory already multiplied by chunk 0's decay to its end (the MMA adds to it).
+    {
+      const float g_end = expf(gam_g[kC - 1]);
+#pragma unroll 1
+      for (int pc = 0; pc < 4; ++pc) {
+        float s[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          s[e] = p.s0 ? p.s0[(bh * kDv + d) * kDk + pc * 32 + e] : 0.f;
+        put_row32(sbf + (pc / 2) * kSBlk, (pc % 2) * 4, s);
+        uint32_t w[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(s[e] * g_end);
+        tmem_st32(tmem + kTmS + lane_off + pc * 32, w);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_sready);
+    }
+    bool ok = true;
+    // U~ of the next chunk, loaded ahead into registers (row i, column d)
+    float ut[kC];
+    {
+      const float* ub = p.u_ws + (bh * p.Tpad) * kDv + d;
+#pragma unroll
+      for (int i = 0; i < kC; ++i) ut[i] = ub[static_cast<size_t>(i) * kDv];
+    }
+#pragma unroll 1
+    for (int c = 0; c < nc; ++c) {
+      float* gm = gam_s + (c & 1) * kC;
+      if (d < kC / 4)
+        reinterpret_cast<float4*>(gm)[d] = reinterpret_cast<const float4*>(gam_g + c * kC)[d];
+      state_sync();
+      const float g_end = gm[kC - 1];
+      // ---- U^T = U~^T - S W^T, and U'^T = U^T with token i scaled by Gamma_C / Gamma_i ----
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_udone, c & 1, p.status));
+      tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t du[32];
+        tmem_ld32(tmem + kTmU + lane_off + half * 32, du);
+        tmem_ld_wait();
+        float u[32], up[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int i = half * 32 + e;
+          u[e] = ut[i] - __uint_as_float(du[e]);
+          up[e] = u[e] * expf(g_end - gm[i]);
+        }
+        put_row32(utp, half * 4, u);
+        put_row32(uptp, half * 4, up);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_uready);
+      // ---- O = Gamma_i scale S q_i + (P U)_i, then the state for the next chunk ----
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_odone, c & 1, p.status));
+      tc_fence_after();
+      const int t0 = c * kC, n = min(kC, p.T - t0);
+      if (c + 1 < nc) {  // next chunk's U~, in flight while this chunk finishes
+        const float* ub = p.u_ws + (bh * p.Tpad + (c + 1) * kC) * kDv + d;
+#pragma unroll
+        for (int i = 0; i < kC; ++i) ut[i] = ub[static_cast<size_t>(i) * kDv];
+      }
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t o1[32], o2[32];
+        tmem_ld32(tmem + kTmO1 + lane_off + half * 32, o1);
+        tmem_ld32(tmem + kTmO2 + lane_off + half * 32, o2);
+        tmem_ld_wait();
+        if (ok) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int i = half * 32 + e;
+            if (i < n) {
+              const float o = expf(gm[i]) * p.scale * __uint_as_float(o1[e]) + __uint_as_float(o2[e]);
+              const __nv_bfloat16 hv = __float2bfloat16_rn(o);
+              p.out[(bh * p.T + t0 + i) * kDv + d] = *reinterpret_cast<const uint16_t*>(&hv);
+            }
+          }
+        }
+      }
+      const bool last = c + 1 == nc;
+      const float g_next = last ? 1.f : expf(gam_g[(c + 1) * kC + kC - 1]);
+#pragma unroll 1
+      for (int pc = 0; pc < 4; ++pc) {
+        uint32_t w[32];
+        tmem_ld32(tmem + kTmS + lane_off + pc * 32, w);
+        tmem_ld_wait();
+        float s[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(w[e]);
+        if (last) {
+          if (ok && p.s_final) {
+            float4* dst = reinterpret_cast<float4*>(p.s_final + (bh * kDv + d) * kDk + pc * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dst[e] = make_float4(s[4 * e], s[4 * e + 1], s[4 * e + 2], s[4 * e + 3]);
+          }
+        } else {
+          put_row32(sbf + (pc / 2) * kSBlk, (pc % 2) * 4, s);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(s[e] * g_next);
+          tmem_st32(tmem + kTmS + lane_off + pc * 32, w);
+        }
+      }
+      if (!last) {
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar_sready);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+struct GdnPlan {
+  int n_chunks, Tpad;
+  size_t off_w, off_u, off_p, off_g, total;
+};
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+GdnPlan plan_gdn(const gated_delta_args* a) {
+  GdnPlan pl{};
+  pl.n_chunks = (a->T + kC - 1) / kC;
+  pl.Tpad = pl.n_chunks * kC;
+  const size_t rows = static_cast<size_t>(a->B) * a->Hv * pl.Tpad;
+  pl.off_w = 0;
+  pl.off_u = align256(pl.off_w + rows * kDk * 2);
+  pl.off_p = align256(pl.off_u + rows * kDv * 4);
+  pl.off_g = align256(pl.off_p + rows * kC * 2);
+  pl.total = align256(pl.off_g + rows * 4);
+  return pl;
+}
+
+int fail_gd(int code, const char* msg) { return set_error(code, msg); }
+
+int validate_gdn(const gated_delta_args* a, bool pointers) {
+  char msg[200];
+  if (!a) return fail_gd(FA_ERR_INVALID_ARG, "gated_delta_prefill: null argument struct");
+  if (a->B < 0 || a->T < 0 || a->Hk <= 0 || a->Hv <= 0 || a->Hv % a->Hk != 0) {
+    snprintf(msg, sizeof msg, "gated_delta_prefill: need B, T >= 0, Hk, Hv > 0, Hv %% Hk == 0 "
+             "(got %d, %d, %d, %d)", a->B, a->T, a->Hk, a->Hv);
+    return fail_gd(FA_ERR_INVALID_ARG, msg);
+  }
+  if (a->dk != kDk || a->dv != kDv) {
+    snprintf(msg, sizeof msg, "gated_delta_prefill: dk and dv must be 128 (got %d, %d)", a->dk, a->dv);
+    return fail_gd(FA_ERR_UNSUPPORTED, msg);
+  }
+  if (a->dtype != FA_BF16)
+    return fail_gd(FA_ERR_UNSUPPORTED, "gated_delta_prefill: dtype must be FA_BF16");
+  if (a->B > 65535 || a->Hv > 65535 ||
+      static_cast<long>(a->B) * a->Hv * (static_cast<long>(a->T) + kC) > 2147483647L)
+    return fail_gd(FA_ERR_UNSUPPORTED, "gated_delta_prefill: B * Hv * T must fit in int32");
+  if (!(a->scale == a->scale) || isinf(a->scale))
+    return fail_gd(FA_ERR_INVALID_ARG, "gated_delta_prefill: scale must be finite");
+  if (!pointers || a->B == 0 || a->T == 0) return FA_OK;
+  if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->out)
+    return fail_gd(FA_ERR_INVALID_ARG, "gated_delta_prefill: null q/k/v/g/beta/out pointer");
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!al16(a->q) || !al16(a->k) || !al16(a->v) || !al16(a->g) || !al16(a->beta) ||
+      !al16(a->out) || !al16(a->initial_state) || !al16(a->final_state))
+    return fail_gd(FA_ERR_INVALID_ARG, "gated_delta_prefill: tensors must be 16-byte aligned");
+  return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+size_t gated_delta_workspace_size(const gated_delta_args* a) {
+  if (validate_gdn(a, false) != FA_OK || a->B == 0 || a->T == 0) return 0;
+  return plan_gdn(a).total;
+}
+
+int gated_delta_prefill(const gated_delta_args* a, void* stream) {
+  int rc = validate_gdn(a, true);
+  if (rc != FA_OK || a->B == 0) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (a->T == 0) {
+    // no token: the final state is the initial one (or zero)
+    if (!a->final_state) return FA_OK;
+    const size_t bytes = static_cast<size_t>(a->B) * a->Hv * kDv * kDk * 4;
+    cudaError_t e = a->initial_state
+                        ? cudaMemcpyAsync(a->final_state, a->initial_state, bytes, cudaMemcpyDeviceToDevice, st)
+                        : cudaMemsetAsync(a->final_state, 0, bytes, st);
+    if (e != cudaSuccess) return fail_gd(FA_ERR_CUDA, "gated_delta_prefill: state copy failed");
+    return FA_OK;
+  }
+  const GdnPlan pl = plan_gdn(a);
+  char msg[200];
+  if (!a->workspace || a->workspace_bytes < pl.total) {
+    snprintf(msg, sizeof msg, "gated_delta_prefill: workspace of %zu bytes needed (got %zu)",
+             pl.total, a->workspace ? a->workspace_bytes : static_cast<size_t>(0));
+    return fail_gd(FA_ERR_WORKSPACE, msg);
+  }
+  if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0)
+    return fail_gd(FA_ERR_INVALID_ARG, "gated_delta_prefill: workspace must be 256-byte aligned");
+  uint32_t* status = device_status_ptr();
+  if (!status) return fail_gd(FA_ERR_CUDA, "gated_delta_prefill: no usable CUDA device");
+  uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+  GdnParams p{};
+  p.q = static_cast<const uint16_t*>(a->q);
+  p.k = static_cast<const uint16_t*>(a->k);
+  p.v = static_cast<const uint16_t*>(a->v);
+  p.g = a->g;
+  p.beta = a->beta;
+  p.s0 = a->initial_state;
+  p.out = static_cast<uint16_t*>(a->out);
+  p.s_final = a->final_state;
+  p.B = a->B;
+  p.T = a->T;
+  p.Hk = a->Hk;
+  p.Hv = a->Hv;
+  p.n_chunks = pl.n_chunks;
+  p.Tpad = pl.Tpad;
+  p.scale = a->scale;
+  p.w_ws = reinterpret_cast<uint16_t*>(ws + pl.off_w);
+  p.u_ws = reinterpret_cast<float*>(ws + pl.off_u);
+  p.p_ws = reinterpret_cast<uint16_t*>(ws + pl.off_p);
+  p.gam_ws = reinterpret_cast<float*>(ws + pl.off_g);
+  p.status = status;
+
+  CUtensorMap tw, tq, tk, tp;
+  const uint64_t rows = static_cast<uint64_t>(a->B) * a->Hv * pl.Tpad;
+  {
+    const uint64_t dims[2] = {kDk, rows}, str[1] = {kDk * 2};
+    const uint32_t box[2] = {64, kC};
+    if (!encode_tiled(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.w_ws, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail_gd(FA_ERR_CUDA, "gated_delta_prefill: tensor map (W) rejected");
+  }
+  {
+    const uint64_t dims[2] = {kC, rows}, str[1] = {kC * 2};
+    const uint32_t box[2] = {64, kC};
+    if (!encode_tiled(&tp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.p_ws, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail_gd(FA_ERR_CUDA, "gated_delta_prefill: tensor map (P) rejected");
+  }
+  {
+    const uint64_t dims[3] = {kDk, static_cast<uint64_t>(a->T), static_cast<uint64_t>(a->B) * a->Hk};
+    const uint64_t str[2] = {kDk * 2, static_cast<uint64_t>(a->T) * kDk * 2};
+    const uint32_t box[3] = {64, kC, 1};
+    if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a->q, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a->k, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail_gd(FA_ERR_CUDA, "gated_delta_prefill: tensor map (Q/K) rejected");
+  }
+  cudaError_t e = ensure_smem_limit(gdn_prep_kernel, kPrepSmem);
+  if (e == cudaSuccess) e = ensure_smem_limit(gdn_state_kernel, kStateSmem);
+  if (e != cudaSuccess) return fail_gd(FA_ERR_CUDA, "gated_delta_prefill: shared memory limit");
+  gdn_prep_kernel<<<dim3(pl.n_chunks, a->Hv, a->B), kPrepThreads, kPrepSmem, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_gd(FA_ERR_CUDA, "gated_delta_prefill: chunk kernel launch failed");
+  gdn_state_kernel<<<dim3(a->Hv, a->B), kStateThreads, kStateSmem, st>>>(tw, tq, tk, tp, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_gd(FA_ERR_CUDA, "gated_delta_prefill: state kernel launch failed");
+  return FA_OK;
+}
+
+}  // extern "C"
