@@ -13,15 +13,17 @@
 //   O = Gamma (scale Q) S^T + P U,        P_ij = scale (Gamma_i / Gamma_j) q_i.k_j (j <= i)
 //   S <- Gamma_C S + U^T (Gamma_C / Gamma_j) K
 // Two kernels:
-//   1. chunk preparation (every chunk of every head in parallel, CUDA cores, fp32): the
-//      Gram products K K^T and Q K^T, the triangular solve for W and U~ (each thread one
-//      right-hand-side column, held in registers), P; written to a workspace (W and P in
-//      bf16 as tensor-core operands, U~ and the decays in fp32);
+//   1. chunk preparation (every chunk of every head in parallel): the Gram products Q K^T
+//      and K K^T in one tensor-core MMA (the chunk's Q and K rows stacked as a 128-row A
+//      operand against its K rows), the triangular solve for W and U~ on the CUDA cores in
+//      fp32 (each thread one right-hand-side column, held in registers), P, and the per-token
+//      decay factors Gamma_i and Gamma_C / Gamma_i; written to a workspace (W and P in bf16
+//      as tensor-core operands, U~ and the factors in fp32);
 //   2. the recurrence across chunks (one CTA per (batch, value head), tensor cores): the state
 //      lives in tensor memory in fp32 (dv lanes x dk columns), with a bf16 copy in shared
 //      memory as the A operand; per chunk  U^T = U~^T - S W^T,  O^T = S Q^T (scaled per token)
-//      + U^T P^T,  S += (U^T scaled per token) K,  with the chunk's W, Q, K and P streamed by
-//      TMA through a two-stage ring.
+//      + U^T P^T,  S <- Gamma_C S + (U^T scaled per token) K,  with the chunk's W, Q, K, P and
+//      decay factors streamed by TMA through a two-stage ring.
 // The output O and the final state are written per chunk; no chunk's state is kept.
 #include <math.h>
 #include <stdio.h>
@@ -52,122 +54,153 @@ struct GdnParams {
   uint16_t* w_ws;        // [B*Hv*Tpad, dk] bf16
   float* u_ws;           // [B*Hv*Tpad, dv] fp32
   uint16_t* p_ws;        // [B*Hv*Tpad, C] bf16 (rows of each chunk's P)
-  float* gam_ws;         // [B*Hv*Tpad] fp32 cumulative log decay within the chunk
+  float* f_ws;           // [B*Hv*n_chunks, 2C] fp32: Gamma_i, then Gamma_C / Gamma_i
   uint32_t* status;
 };
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
 // ------------------------------------------------------------------------------------------
-// Kernel 1: chunk preparation.  One CTA per (chunk, value head, batch), 256 threads.
+// Kernel 1: chunk preparation.  One CTA per (chunk, value head, batch), 256 threads.  Thread
+// 0 loads the chunk's Q, K and V rows with TMA (128-byte swizzled, rows past the sequence
+// read as zero) and issues the Gram MMA; warps 0-3 read its rows back; all threads solve.
 // ------------------------------------------------------------------------------------------
 constexpr int kPrepThreads = 256;
-constexpr int kRowF = kDk + 4;    // padded fp32 row of a K/Q/V tile in shared memory
-constexpr int kTriF = kC + 4;     // padded fp32 row of A and P (float4-aligned)
-constexpr int kPrepSmem = (2 * kC * kRowF + 2 * kC * kTriF + 3 * kC) * 4;
+constexpr int kTriF = kC + 4;                  // padded fp32 row of A (float4-aligned)
+constexpr int kPQK = 0;                        // [Q rows; K rows]: 2 column blocks of 128 x 128 B
+constexpr int kPV = kPQK + 2 * 128 * 128;      // V rows: 2 column blocks of 64 x 128 B
+constexpr int kPA = kPV + 2 * kC * 128;        // A, fp32 [C][kTriF]
+constexpr int kPSmall = kPA + kC * kTriF * 4;  // gamma, beta, raw g: 3 x C fp32
+constexpr int kPBar = kPSmall + 3 * kC * 4;    // two mbarriers + the tensor-memory slot
+constexpr int kPrepSmem = kPBar + 32 + 1024;
 
-__global__ void __launch_bounds__(kPrepThreads, 2) gdn_prep_kernel(const GdnParams p) {
-  extern __shared__ __align__(16) float sm[];
-  float* Ks = sm;                      // [C][kRowF]
-  float* QVs = Ks + kC * kRowF;        // [C][kRowF]: Q, then V
-  float* As = QVs + kC * kRowF;        // [C][kTriF]
-  float* Ps = As + kC * kTriF;         // [C][kTriF]
-  float* gam = Ps + kC * kTriF;        // [C]
-  float* bet = gam + kC;               // [C]
-  float* graw = bet + kC;              // [C]
+// Element (row r, column col) of a K-major 128-byte-swizzled bf16 tile made of 64-column
+// blocks of `rows` rows each (the layout TMA writes and the MMA reads).
+__device__ __forceinline__ float swz_at(const uint8_t* tile, int rows, int r, int col) {
+  const int cb = col >> 6, ch = (col >> 3) & 7;
+  const uint16_t bits = *reinterpret_cast<const uint16_t*>(
+      tile + cb * rows * 128 + r * 128 + ((ch ^ (r & 7)) * 16) + (col & 7) * 2);
+  return __uint_as_float(static_cast<uint32_t>(bits) << 16);
+}
+
+__global__ void __launch_bounds__(kPrepThreads, 2)
+    gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const GdnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t s_base = smem_addr(smem);
+  float* As = reinterpret_cast<float*>(smem + kPA);
+  float* gam = reinterpret_cast<float*>(smem + kPSmall);
+  float* bet = gam + kC;
+  float* graw = bet + kC;
+  const uint32_t bar_ld = s_base + kPBar, bar_mma = s_base + kPBar + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPBar + 16);
 
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  const int warp = tid / 32;
   const int hk = h / (p.Hv / p.Hk);
   const int t0 = c * kC, n = min(kC, p.T - t0);
   const size_t bh = static_cast<size_t>(b) * p.Hv + h;
-  const uint16_t* krow = p.k + (static_cast<size_t>(b * p.Hk + hk) * p.T + t0) * kDk;
-  const uint16_t* qrow = p.q + (static_cast<size_t>(b * p.Hk + hk) * p.T + t0) * kDk;
-  const uint16_t* vrow = p.v + (bh * p.T + t0) * kDv;
 
-  // rows of 128 bf16 -> fp32 shared-memory rows; rows past the sequence are zero
-  auto load_rows = [&](const uint16_t* src, float* dst) {
-    for (int e = tid; e < kC * (kDk / 8); e += kPrepThreads) {
-      const int r = e / (kDk / 8), c8 = (e % (kDk / 8)) * 8;
-      uint4 w = make_uint4(0, 0, 0, 0);
-      if (r < n) w = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * kDk + c8);
-      float4* d = reinterpret_cast<float4*>(dst + r * kRowF + c8);
-      d[0] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
-      d[1] = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
-    }
-  };
-  load_rows(krow, Ks);
-  load_rows(qrow, QVs);
+  if (tid == 0) {
+    mbar_init(bar_ld, 1);
+    mbar_init(bar_mma, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_addr(tmem_slot), 64);
+    tmem_relinquish();
+  }
   if (tid < kC) {
     const bool ok = tid < n;
-    graw[tid] = ok ? p.g[bh * p.T + t0 + tid] : 0.f;   // padding: no decay, no write
+    graw[tid] = ok ? p.g[bh * p.T + t0 + tid] : 0.f;  // padding: no decay, no write
     bet[tid] = ok ? p.beta[bh * p.T + t0 + tid] : 0.f;
   }
+  tc_fence_before();
   __syncthreads();
-  // cumulative log decay within the chunk (inclusive scan by warp 0, two tokens per lane)
-  if (tid < 32) {
-    const float a = graw[2 * tid], a2 = graw[2 * tid + 1];
-    float s = a + a2;
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_ld, 6 * kC * 128);
+    for (int cb = 0; cb < 2; ++cb) {
+      tma_load_3d(s_base + kPQK + cb * 128 * 128, &tm_q, bar_ld, cb * 64, t0, b * p.Hk + hk);
+      tma_load_3d(s_base + kPQK + cb * 128 * 128 + kC * 128, &tm_k, bar_ld, cb * 64, t0, b * p.Hk + hk);
+      tma_load_3d(s_base + kPV + cb * kC * 128, &tm_v, bar_ld, cb * 64, t0, static_cast<int>(bh));
+    }
+    // [Q; K] K^T: M = 128 (query rows, then key rows), N = 64 key rows, K = 128
+    bool ok = mbar_wait(bar_ld, 0, p.status);
+    if (ok) {
+      tc_fence_after();
+      constexpr uint32_t idesc = idesc_f16(true, 128, kC, false, false);
+#pragma unroll
+      for (int kk = 0; kk < kDk / 16; ++kk) {
+        const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
+        mma_ss(tmem, sdesc_sw128(s_base + kPQK + off, 16, 1024),
+               sdesc_sw128(s_base + kPQK + off + kC * 128, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+      }
+    }
+    tc_commit(bar_mma);  // arrives once the MMAs (if any) are done
+  }
+  // cumulative log decay within the chunk (inclusive scan by warp 4, two tokens per lane)
+  if (warp == 4) {
+    const int l = tid - 128;
+    const float a = graw[2 * l], a2 = graw[2 * l + 1];
+    float sc = a + a2;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, s, o);
-      if (tid >= o) s += y;
+      const float y = __shfl_up_sync(0xffffffffu, sc, o);
+      if (l >= o) sc += y;
     }
-    const float excl = s - (a + a2);
-    gam[2 * tid] = excl + a;
-    gam[2 * tid + 1] = excl + a + a2;
+    const float excl = sc - (a + a2);
+    gam[2 * l] = excl + a;
+    gam[2 * l + 1] = excl + a + a2;
   }
   __syncthreads();
-
-  // Gram products: thread (ti, tj) computes rows ti + 16a and columns tj + 16b (a, b < 4)
-  {
-    const int ti = tid & 15, tj = tid >> 4;
-    float kk[4][4], qk[4][4];
+  bool ok = __syncthreads_and(mbar_wait(bar_mma, 0, p.status));
+  if (warp < 4) {
+    // lane r of the Gram result: r < 64 is row r of Q K^T (-> P), r >= 64 row r - 64 of K K^T
+    tc_fence_after();
+    uint32_t raw[kC];
+    tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16), *reinterpret_cast<uint32_t(*)[32]>(&raw[0]));
+    tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 32,
+              *reinterpret_cast<uint32_t(*)[32]>(&raw[32]));
+    tmem_ld_wait();
+    if (tid < kC) {
+      const int i = tid;
+      uint32_t pk[kC / 2];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int bb = 0; bb < 4; ++bb) kk[a][bb] = qk[a][bb] = 0.f;
-#pragma unroll 2
-    for (int d = 0; d < kDk; d += 4) {
-      float4 ki[4], qi[4], kj[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        ki[a] = *reinterpret_cast<const float4*>(Ks + (ti + 16 * a) * kRowF + d);
-        qi[a] = *reinterpret_cast<const float4*>(QVs + (ti + 16 * a) * kRowF + d);
-        kj[a] = *reinterpret_cast<const float4*>(Ks + (tj + 16 * a) * kRowF + d);
+      for (int j = 0; j < kC; j += 2) {
+        const float p0 = (j <= i && i < n) ? p.scale * expf(gam[i] - gam[j]) * __uint_as_float(raw[j]) : 0.f;
+        const float p1 = (j + 1 <= i && i < n) ? p.scale * expf(gam[i] - gam[j + 1]) * __uint_as_float(raw[j + 1]) : 0.f;
+        pk[j / 2] = pack_bf16x2(p0, p1);
       }
+      uint4* dst = reinterpret_cast<uint4*>(p.p_ws + (bh * p.Tpad + t0 + i) * kC);
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int e = 0; e < kC / 8; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+    } else {
+      const int i = tid - kC;
 #pragma unroll
-        for (int bb = 0; bb < 4; ++bb) {
-          kk[a][bb] += ki[a].x * kj[bb].x + ki[a].y * kj[bb].y + ki[a].z * kj[bb].z + ki[a].w * kj[bb].w;
-          qk[a][bb] += qi[a].x * kj[bb].x + qi[a].y * kj[bb].y + qi[a].z * kj[bb].z + qi[a].w * kj[bb].w;
-        }
-    }
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int bb = 0; bb < 4; ++bb) {
-        const int i = ti + 16 * a, j = tj + 16 * bb;
-        const float r = j <= i ? expf(gam[i] - gam[j]) : 0.f;
-        As[i * kTriF + j] = j < i ? bet[i] * r * kk[a][bb] : 0.f;
-        Ps[i * kTriF + j] = (j <= i && i < n) ? p.scale * r * qk[a][bb] : 0.f;
+      for (int j = 0; j < kC; j += 4) {
+        float4 a;
+        a.x = j < i ? bet[i] * expf(gam[i] - gam[j]) * __uint_as_float(raw[j]) : 0.f;
+        a.y = j + 1 < i ? bet[i] * expf(gam[i] - gam[j + 1]) * __uint_as_float(raw[j + 1]) : 0.f;
+        a.z = j + 2 < i ? bet[i] * expf(gam[i] - gam[j + 2]) * __uint_as_float(raw[j + 2]) : 0.f;
+        a.w = j + 3 < i ? bet[i] * expf(gam[i] - gam[j + 3]) * __uint_as_float(raw[j + 3]) : 0.f;
+        *reinterpret_cast<float4*>(As + i * kTriF + j) = a;
       }
-  }
-  __syncthreads();
-  // P to the workspace as bf16 (row-major, 128 bytes per row), then V over Q
-  {
-    uint16_t* pdst = p.p_ws + (bh * p.Tpad + t0) * kC;
-    for (int e = tid; e < kC * kC / 8; e += kPrepThreads) {
-      const int r = e / (kC / 8), c8 = (e % (kC / 8)) * 8;
-      const float* s = Ps + r * kTriF + c8;
-      *reinterpret_cast<uint4*>(pdst + r * kC + c8) =
-          make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]), pack_bf16x2(s[4], s[5]),
-                     pack_bf16x2(s[6], s[7]));
     }
+  } else if (tid < 128 + 2 * kC) {
+    // decay factors of the chunk: Gamma_i, then Gamma_C / Gamma_i
+    const int e = tid - 128;
+    const float v = e < kC ? expf(gam[e]) : expf(gam[kC - 1] - gam[e - kC]);
+    p.f_ws[(bh * p.n_chunks + c) * (2 * kC) + e] = v;
   }
-  load_rows(vrow, QVs);
+  tc_fence_before();
   __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+  if (!ok) return;
 
   // Triangular solve (I + A) X = R by forward substitution, one right-hand-side column per
   // thread, the column in registers: columns 0..127 give W (R = beta Gamma K), columns
@@ -175,14 +208,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_prep_kernel(const GdnPara
   // above the diagonal are zero, so every row runs over whole groups of four.
   {
     const bool wcol = tid < kDk;
-    const float* rsrc = wcol ? Ks + tid : QVs + (tid - kDk);
+    const int col = wcol ? tid : tid - kDk;
     float x[kC];
 #pragma unroll
     for (int i = 0; i < kC; ++i) x[i] = 0.f;
 #pragma unroll
     for (int i = 0; i < kC; ++i) {
-      float acc = bet[i] * rsrc[i * kRowF];
-      if (wcol) acc *= expf(gam[i]);
+      float acc = wcol ? bet[i] * expf(gam[i]) * swz_at(smem + kPQK, 128, kC + i, col)
+                       : bet[i] * swz_at(smem + kPV, kC, i, col);
 #pragma unroll
       for (int m4 = 0; m4 < (i + 3) / 4; ++m4) {
         const float4 a = *reinterpret_cast<const float4*>(As + i * kTriF + 4 * m4);
@@ -192,46 +225,48 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_prep_kernel(const GdnPara
     }
     const size_t row0 = bh * p.Tpad + t0;
     if (wcol) {
-      uint16_t* wdst = p.w_ws + row0 * kDk + tid;
+      uint16_t* wdst = p.w_ws + row0 * kDk + col;
 #pragma unroll
       for (int i = 0; i < kC; ++i) {
         const __nv_bfloat16 hv = __float2bfloat16_rn(x[i]);
         wdst[static_cast<size_t>(i) * kDk] = *reinterpret_cast<const uint16_t*>(&hv);
       }
     } else {
-      float* udst = p.u_ws + row0 * kDv + (tid - kDk);
+      float* udst = p.u_ws + row0 * kDv + col;
 #pragma unroll
       for (int i = 0; i < kC; ++i) udst[static_cast<size_t>(i) * kDv] = x[i];
     }
-    if (tid < kC) p.gam_ws[row0 + tid] = gam[tid];
   }
 }
 
 // ------------------------------------------------------------------------------------------
-// Kernel 2: the recurrence across chunks.  One CTA per (value head, batch), 192 threads:
-// warps 0-3 own the state rows (thread d = tensor-memory lane d = value dim d), warp 4 loads
-// the chunk operands with TMA, warp 5 issues the MMAs and owns the tensor memory.
+// Kernel 2: the recurrence across chunks.  One CTA per (value head, batch), 320 threads:
+// warps 0-7 own the state rows (thread (d, half): tensor-memory lane d = value dim d, warps
+// 0-3 and 4-7 taking the two halves of every row's columns), warp 8 loads the chunk operands
+// with TMA, warp 9 issues the MMAs and owns the tensor memory.
 // ------------------------------------------------------------------------------------------
-constexpr int kStateThreads = 192;
+constexpr int kStateWarps = 8;
+constexpr int kStateThreads = (kStateWarps + 2) * 32;
+constexpr int kProducerWarp = kStateWarps, kMmaWarp = kStateWarps + 1;
 constexpr int kBlkTok = kC * 128;                // one 64-column block of a 64-row tile
 constexpr int kStageW = 0;
 constexpr int kStageQ = kStageW + 2 * kBlkTok;
 constexpr int kStageK = kStageQ + 2 * kBlkTok;
 constexpr int kStageP = kStageK + 2 * kBlkTok;
-constexpr int kStageBytes = kStageP + kBlkTok;   // 57344: W, Q, K (16 KB each), P (8 KB)
+constexpr int kStageF = kStageP + kBlkTok;       // decay factors: Gamma_i, Gamma_C / Gamma_i
+constexpr int kStageTx = kStageF + 2 * kC * 4;   // bytes landing per chunk
+constexpr int kStageBytes = (kStageTx + 1023) / 1024 * 1024;
 constexpr int kSbfOff = 2 * kStageBytes;         // S as bf16, [128 rows][2 blocks of 128 B]
 constexpr int kSBlk = kDv * 128;                 // 16384: one 64-column block of S
 constexpr int kUtOff = kSbfOff + 2 * kSBlk;      // U^T, [128 rows][128 B]
 constexpr int kUptOff = kUtOff + kSBlk;          // U^T with each token's decay to the chunk end
-constexpr int kGamOff = kUptOff + kSBlk;         // two chunks' decays, fp32
-constexpr int kBarOff = kGamOff + 2 * kC * 4;
+constexpr int kBarOff = kUptOff + kSBlk;
 // full[2], empty[2], s_ready, u_ready, u_done, o_done, mma_done
 constexpr int kNumBars = 9;
 constexpr int kStateSmem = kBarOff + kNumBars * 8 + 16 + 1024;
 static_assert(kStateSmem <= 232448, "shared memory budget");
 constexpr uint32_t kTmS = 0, kTmU = 128, kTmO1 = 192, kTmO2 = 256;
-
-__device__ __forceinline__ void state_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+constexpr uint32_t kStateArrivals = kStateWarps * 32;
 
 __global__ void __launch_bounds__(kStateThreads, 1)
     gdn_state_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
@@ -247,7 +282,6 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   const uint32_t bar_sready = bars + 8u * 4, bar_uready = bars + 8u * 5;
   const uint32_t bar_udone = bars + 8u * 6, bar_odone = bars + 8u * 7, bar_done = bars + 8u * 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + kNumBars * 8);
-  float* gam_s = reinterpret_cast<float*>(smem + kGamOff);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int h = blockIdx.x, b = blockIdx.y;
@@ -258,16 +292,18 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 1);
+      // a stage is free again once its MMAs are done (one commit) and every state thread
+      // has read its decay factors
+      mbar_init(bar_empty(s), 1 + kStateArrivals);
     }
-    mbar_init(bar_sready, 128);
-    mbar_init(bar_uready, 128);
+    mbar_init(bar_sready, kStateArrivals);
+    mbar_init(bar_uready, kStateArrivals);
     mbar_init(bar_udone, 1);
     mbar_init(bar_odone, 1);
     mbar_init(bar_done, 1);
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -276,7 +312,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ---------------------------------- TMA producer ------------------------------------
     if (lane == 0) {
       tma_prefetch_desc(&tm_w);
@@ -289,20 +325,21 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         if (c >= 2 && !mbar_wait(bar_empty(st), ((c >> 1) - 1) & 1, p.status)) break;
         const uint32_t base = s_base + st * kStageBytes;
         const int row = static_cast<int>(bh * p.Tpad) + c * kC;
-        mbar_arrive_expect_tx(bar_full(st), kStageBytes);
+        mbar_arrive_expect_tx(bar_full(st), kStageTx);
         for (int cb = 0; cb < 2; ++cb) {
           tma_load_2d(base + kStageW + cb * kBlkTok, &tm_w, bar_full(st), cb * 64, row);
           tma_load_3d(base + kStageQ + cb * kBlkTok, &tm_q, bar_full(st), cb * 64, c * kC, b * p.Hk + hk);
           tma_load_3d(base + kStageK + cb * kBlkTok, &tm_k, bar_full(st), cb * 64, c * kC, b * p.Hk + hk);
         }
         tma_load_2d(base + kStageP, &tm_p, bar_full(st), 0, row);
+        bulk_load(base + kStageF, p.f_ws + (bh * nc + c) * (2 * kC), 2 * kC * 4, bar_full(st));
         issued = c + 1;
       }
       // a wait ran out: let the copies in flight land before the CTA exits
       for (int c = max(0, issued - 2); c < issued && issued < nc; ++c)
         mbar_wait(bar_full(c & 1), (c >> 1) & 1, nullptr);
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------- MMA issuer --------------------------------------
     if (lane == 0) {
       constexpr uint32_t idesc_n64 = idesc_f16(true, 128, 64, false, false);
@@ -339,7 +376,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         for (int kk = 0; kk < kC / 16; ++kk)
           mma_ss(tmem + kTmO2, sdesc_sw128(ut + kk * 32, 16, 1024),
                  sdesc_sw128(base + kStageP + kk * 32, 16, 1024), idesc_n64, kk > 0 ? 1u : 0u);
-        // D_S += U'^T K (N = 128 key dims, K = 64 tokens; K read MN-major)
+        // D_S (already Gamma_C S) += U'^T K (N = 128 key dims, K = 64 tokens; K read MN-major)
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
           mma_ss(tmem + kTmS, sdesc_sw128(upt + kk * 32, 16, 1024),
@@ -351,13 +388,13 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       mbar_wait(bar_done, 0, nullptr);
     }
   } else {
-    // ------------------------- state rows: thread d = value dim d -----------------------
-    const int d = threadIdx.x;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // ------------------ state rows: thread (d, half), d = value dim d ------------------
+    const int d = (warp & 3) * 32 + lane;
+    const int half = warp >> 2;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint8_t* sbf = smem + kSbfOff;
     uint8_t* utp = smem + kUtOff;
     uint8_t* uptp = smem + kUptOff;
-    const float* gam_g = p.gam_ws + bh * p.Tpad;
     // Row d of a K-major 128-byte-swizzled tile: 16-byte chunk ch sits at chunk ch ^ (d % 8).
     auto put_row32 = [&](uint8_t* blk, int ch0, const float (&v)[32]) {
 #pragma unroll
@@ -366,124 +403,126 @@ __global__ void __launch_bounds__(kStateThreads, 1)
             make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
                        pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
     };
-    // The state entering chunk 0: the initial state (or zero) as the bf16 operand, and in
-    // tensor memory already multiplied by chunk 0's decay to its end (the MMA adds to it).
-    {
-      const float g_end = expf(gam_g[kC - 1]);
+    // This thread's columns: tokens 32 half .. +31 of D_U, D_O1, D_O2 and of U^T; key dims
+    // 64 half .. +63 of the state (block `half` of its bf16 copy).
+    // The state entering chunk 0: the initial state (or zero), as the bf16 operand and in
+    // tensor memory (scaled by the chunk's decay before the chunk's MMA adds to it).
 #pragma unroll 1
-      for (int pc = 0; pc < 4; ++pc) {
-        float s[32];
+    for (int pc = 0; pc < 2; ++pc) {
+      float s[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          s[e] = p.s0 ? p.s0[(bh * kDv + d) * kDk + pc * 32 + e] : 0.f;
-        put_row32(sbf + (pc / 2) * kSBlk, (pc % 2) * 4, s);
-        uint32_t w[32];
+      for (int e = 0; e < 32; ++e)
+        s[e] = p.s0 ? p.s0[(bh * kDv + d) * kDk + half * 64 + pc * 32 + e] : 0.f;
+      put_row32(sbf + half * kSBlk, pc * 4, s);
+      uint32_t w[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(s[e] * g_end);
-        tmem_st32(tmem + kTmS + lane_off + pc * 32, w);
-      }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar_sready);
+      for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(s[e]);
+      tmem_st32(tmem + kTmS + lane_off + half * 64 + pc * 32, w);
     }
+    tmem_st_wait();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(bar_sready);
     bool ok = true;
-    // U~ of the next chunk, loaded ahead into registers (row i, column d)
-    float ut[kC];
+    // U~ of this thread's 32 tokens of the next chunk, loaded ahead (row i, column d)
+    float ut[32];
     {
-      const float* ub = p.u_ws + (bh * p.Tpad) * kDv + d;
+      const float* ub = p.u_ws + (bh * p.Tpad + half * 32) * kDv + d;
 #pragma unroll
-      for (int i = 0; i < kC; ++i) ut[i] = ub[static_cast<size_t>(i) * kDv];
+      for (int e = 0; e < 32; ++e) ut[e] = ub[static_cast<size_t>(e) * kDv];
     }
 #pragma unroll 1
     for (int c = 0; c < nc; ++c) {
-      float* gm = gam_s + (c & 1) * kC;
-      if (d < kC / 4)
-        reinterpret_cast<float4*>(gm)[d] = reinterpret_cast<const float4*>(gam_g + c * kC)[d];
-      state_sync();
-      const float g_end = gm[kC - 1];
+      const int st = c & 1;
+      const float* fct = reinterpret_cast<const float*>(smem + st * kStageBytes + kStageF);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_full(st), (c >> 1) & 1, p.status));
+      // ---- the state in tensor memory times Gamma_C, ready for this chunk's update ----
+      const float g_end = fct[kC - 1];
+#pragma unroll 1
+      for (int pc = 0; pc < 2; ++pc) {
+        uint32_t w[32];
+        tmem_ld32(tmem + kTmS + lane_off + half * 64 + pc * 32, w);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * g_end);
+        tmem_st32(tmem + kTmS + lane_off + half * 64 + pc * 32, w);
+      }
       // ---- U^T = U~^T - S W^T, and U'^T = U^T with token i scaled by Gamma_C / Gamma_i ----
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_udone, c & 1, p.status));
       tc_fence_after();
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      {
         uint32_t du[32];
         tmem_ld32(tmem + kTmU + lane_off + half * 32, du);
         tmem_ld_wait();
         float u[32], up[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const int i = half * 32 + e;
-          u[e] = ut[i] - __uint_as_float(du[e]);
-          up[e] = u[e] * expf(g_end - gm[i]);
+          u[e] = ut[e] - __uint_as_float(du[e]);
+          up[e] = u[e] * fct[kC + half * 32 + e];
         }
         put_row32(utp, half * 4, u);
         put_row32(uptp, half * 4, up);
       }
+      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_uready);
-      // ---- O = Gamma_i scale S q_i + (P U)_i, then the state for the next chunk ----
+      // ---- O = Gamma_i scale S q_i + (P U)_i, then the state's bf16 copy ----
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_odone, c & 1, p.status));
       tc_fence_after();
       const int t0 = c * kC, n = min(kC, p.T - t0);
       if (c + 1 < nc) {  // next chunk's U~, in flight while this chunk finishes
-        const float* ub = p.u_ws + (bh * p.Tpad + (c + 1) * kC) * kDv + d;
+        const float* ub = p.u_ws + (bh * p.Tpad + (c + 1) * kC + half * 32) * kDv + d;
 #pragma unroll
-        for (int i = 0; i < kC; ++i) ut[i] = ub[static_cast<size_t>(i) * kDv];
+        for (int e = 0; e < 32; ++e) ut[e] = ub[static_cast<size_t>(e) * kDv];
       }
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t o1[32], o2[32];
-        tmem_ld32(tmem + kTmO1 + lane_off + half * 32, o1);
-        tmem_ld32(tmem + kTmO2 + lane_off + half * 32, o2);
-        tmem_ld_wait();
-        if (ok) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int i = half * 32 + e;
-            if (i < n) {
-              const float o = expf(gm[i]) * p.scale * __uint_as_float(o1[e]) + __uint_as_float(o2[e]);
-              const __nv_bfloat16 hv = __float2bfloat16_rn(o);
-              p.out[(bh * p.T + t0 + i) * kDv + d] = *reinterpret_cast<const uint16_t*>(&hv);
-            }
-          }
-        }
-      }
+      // D_O1 and D_O2 into registers, then the state's bf16 copy for the next chunk's MMAs;
+      // the outputs are formed and stored after that copy is published
+      uint32_t o1[32], o2[32];
+      tmem_ld32(tmem + kTmO1 + lane_off + half * 32, o1);
+      tmem_ld32(tmem + kTmO2 + lane_off + half * 32, o2);
+      tmem_ld_wait();
       const bool last = c + 1 == nc;
-      const float g_next = last ? 1.f : expf(gam_g[(c + 1) * kC + kC - 1]);
 #pragma unroll 1
-      for (int pc = 0; pc < 4; ++pc) {
+      for (int pc = 0; pc < 2; ++pc) {
         uint32_t w[32];
-        tmem_ld32(tmem + kTmS + lane_off + pc * 32, w);
+        tmem_ld32(tmem + kTmS + lane_off + half * 64 + pc * 32, w);
         tmem_ld_wait();
         float s[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(w[e]);
         if (last) {
           if (ok && p.s_final) {
-            float4* dst = reinterpret_cast<float4*>(p.s_final + (bh * kDv + d) * kDk + pc * 32);
+            float4* dst = reinterpret_cast<float4*>(p.s_final + (bh * kDv + d) * kDk + half * 64 + pc * 32);
 #pragma unroll
             for (int e = 0; e < 8; ++e) dst[e] = make_float4(s[4 * e], s[4 * e + 1], s[4 * e + 2], s[4 * e + 3]);
           }
         } else {
-          put_row32(sbf + (pc / 2) * kSBlk, (pc % 2) * 4, s);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(s[e] * g_next);
-          tmem_st32(tmem + kTmS + lane_off + pc * 32, w);
+          put_row32(sbf + half * kSBlk, pc * 4, s);
         }
       }
       if (!last) {
-        tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar_sready);
       }
+      if (ok) {
+        uint16_t* orow = p.out + (bh * p.T + t0 + half * 32) * kDv + d;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          if (half * 32 + e < n) {
+            const float o = fct[half * 32 + e] * p.scale * __uint_as_float(o1[e]) + __uint_as_float(o2[e]);
+            const __nv_bfloat16 hv = __float2bfloat16_rn(o);
+            orow[static_cast<size_t>(e) * kDv] = *reinterpret_cast<const uint16_t*>(&hv);
+          }
+        }
+      }
+      mbar_arrive(bar_empty(st));  // this thread is done with the stage's decay factors
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -492,7 +531,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 
 struct GdnPlan {
   int n_chunks, Tpad;
-  size_t off_w, off_u, off_p, off_g, total;
+  size_t off_w, off_u, off_p, off_f, total;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -505,8 +544,8 @@ GdnPlan plan_gdn(const gated_delta_args* a) {
   pl.off_w = 0;
   pl.off_u = align256(pl.off_w + rows * kDk * 2);
   pl.off_p = align256(pl.off_u + rows * kDv * 4);
-  pl.off_g = align256(pl.off_p + rows * kC * 2);
-  pl.total = align256(pl.off_g + rows * 4);
+  pl.off_f = align256(pl.off_p + rows * kC * 2);
+  pl.total = align256(pl.off_f + rows * 2 * 4);
   return pl;
 }
 
@@ -598,10 +637,10 @@ int gated_delta_prefill(const gated_delta_args* a, void* stream) {
   p.w_ws = reinterpret_cast<uint16_t*>(ws + pl.off_w);
   p.u_ws = reinterpret_cast<float*>(ws + pl.off_u);
   p.p_ws = reinterpret_cast<uint16_t*>(ws + pl.off_p);
-  p.gam_ws = reinterpret_cast<float*>(ws + pl.off_g);
+  p.f_ws = reinterpret_cast<float*>(ws + pl.off_f);
   p.status = status;
 
-  CUtensorMap tw, tq, tk, tp;
+  CUtensorMap tw, tq, tk, tp, tv;
   const uint64_t rows = static_cast<uint64_t>(a->B) * a->Hv * pl.Tpad;
   {
     const uint64_t dims[2] = {kDk, rows}, str[1] = {kDk * 2};
@@ -627,10 +666,18 @@ int gated_delta_prefill(const gated_delta_args* a, void* stream) {
                       CU_TENSOR_MAP_SWIZZLE_128B))
       return fail_gd(FA_ERR_CUDA, "gated_delta_prefill: tensor map (Q/K) rejected");
   }
+  {
+    const uint64_t dims[3] = {kDv, static_cast<uint64_t>(a->T), static_cast<uint64_t>(a->B) * a->Hv};
+    const uint64_t str[2] = {kDv * 2, static_cast<uint64_t>(a->T) * kDv * 2};
+    const uint32_t box[3] = {64, kC, 1};
+    if (!encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a->v, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail_gd(FA_ERR_CUDA, "gated_delta_prefill: tensor map (V) rejected");
+  }
   cudaError_t e = ensure_smem_limit(gdn_prep_kernel, kPrepSmem);
   if (e == cudaSuccess) e = ensure_smem_limit(gdn_state_kernel, kStateSmem);
   if (e != cudaSuccess) return fail_gd(FA_ERR_CUDA, "gated_delta_prefill: shared memory limit");
-  gdn_prep_kernel<<<dim3(pl.n_chunks, a->Hv, a->B), kPrepThreads, kPrepSmem, st>>>(p);
+  gdn_prep_kernel<<<dim3(pl.n_chunks, a->Hv, a->B), kPrepThreads, kPrepSmem, st>>>(tq, tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail_gd(FA_ERR_CUDA, "gated_delta_prefill: chunk kernel launch failed");
   gdn_state_kernel<<<dim3(a->Hv, a->B), kStateThreads, kStateSmem, st>>>(tw, tq, tk, tp, p);
