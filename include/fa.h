@@ -74,13 +74,15 @@ typedef struct fa_prefill_args {
   int B, Hq, Hkv, Lq, Lkv, D;
   int causal;
   float scale;
-  fa_dtype dtype;        /* FA_BF16, FA_FP16, or FA_FP32 (fp32 inputs are rounded to fp16
-                            for the tensor cores, accumulation stays fp32; needs workspace) */
+  fa_dtype dtype;        /* FA_BF16, FA_FP16 (tensor cores, fp32 accumulation), or FA_FP32:
+                            fp32 inputs are computed in fp32 on the CUDA cores, keeping fp32
+                            range and precision (no split, no workspace; for small problems) */
   const void* mask;      /* optional additive mask [mask_batches, Lq, Lkv]; -inf removes a
                             key; shared by all heads; NULL = none */
   fa_dtype mask_dtype;   /* FA_FP32 or FA_BF16 */
   int mask_batches;      /* 1 (broadcast over the batch) or B */
-  int num_splits;        /* 0: the library picks; >= 1: split the KV loop this many ways */
+  int num_splits;        /* 0: the library picks; >= 1: split the KV loop this many ways
+                            (16-bit inputs; fp32 inputs are never split) */
   void* workspace;       /* device scratch, >= fa_prefill_workspace_size(args) bytes */
   size_t workspace_bytes;
   /* Paged K/V (page_size = 0: dense k and v as above).  With page_size > 0, k and v are

@@ -12,7 +12,7 @@ ROOT = os.path.dirname(HERE)
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libfa.so")
 SOURCES = ["abi.cu", "prefill.cu", "decode.cu", "decode_noalloc.cu", "mla.cu", "merge.cu",
-           "selftest.cu", "gated_delta.cu"]
+           "selftest.cu", "gated_delta.cu", "prefill_f32.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("internal.h", "sm103.cuh", "prefill_common.cuh")] + [
     os.path.join(ROOT, "include", "fa.h")]
 

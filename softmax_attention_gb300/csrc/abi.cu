@@ -133,8 +133,8 @@ namespace {
 // ---------------------------------------------------------------------------------------
 struct PrefillPlan {
   int G, q_per_tile, n_qtiles, n_splits;
-  size_t part_bytes, cast_bytes, total_bytes;
-  size_t off_o, off_lse, off_q, off_k, off_v;
+  size_t part_bytes, total_bytes;
+  size_t off_o, off_lse;
 };
 
 int validate_prefill(const fa_prefill_args* a, bool check_pointers = true) {
@@ -202,7 +202,9 @@ PrefillPlan plan_prefill(const fa_prefill_args* a) {
   const int bn = prefill_block_n(a->D);
   const int kv_tiles = a->Lkv > 0 ? (a->Lkv + bn - 1) / bn : 0;
   int s = 1;
-  if (a->num_splits > 0) {
+  if (a->dtype == FA_FP32) {
+    // fp32 inputs run on the fp32 kernel, one warp per query row over all its keys
+  } else if (a->num_splits > 0) {
     s = a->num_splits;
   } else if (kv_tiles > 0) {
     const long tiles = (long)pl.n_qtiles * a->Hkv * a->B;
@@ -218,7 +220,7 @@ PrefillPlan plan_prefill(const fa_prefill_args* a) {
     }
   }
   if (kv_tiles > 0 && s > kv_tiles) s = kv_tiles;
-  if (s < 1) s = 1;
+  if (s < 1 || a->dtype == FA_FP32) s = 1;
   pl.n_splits = s;
   const size_t rows = (size_t)a->B * a->Hq * a->Lq;
   size_t off = 0;
@@ -229,15 +231,6 @@ PrefillPlan plan_prefill(const fa_prefill_args* a) {
     off = align_up(off + rows * s * sizeof(float), 256);
   }
   pl.part_bytes = off;
-  if (a->dtype == FA_FP32) {
-    pl.off_q = off;
-    off = align_up(off + (size_t)a->B * a->Hq * a->Lq * a->D * 2, 256);
-    pl.off_k = off;
-    off = align_up(off + (size_t)a->B * a->Hkv * a->Lkv * a->D * 2, 256);
-    pl.off_v = off;
-    off = align_up(off + (size_t)a->B * a->Hkv * a->Lkv * a->D * 2, 256);
-  }
-  pl.cast_bytes = off - pl.part_bytes;
   pl.total_bytes = off;
   return pl;
 }
@@ -261,19 +254,7 @@ int run_prefill(const fa_prefill_args* a, cudaStream_t stream) {
   p.q = a->q;
   p.k = a->k;
   p.v = a->v;
-  Dtype operand = static_cast<Dtype>(a->dtype);
-  if (a->dtype == FA_FP32) {
-    const size_t nq = (size_t)a->B * a->Hq * a->Lq * a->D;
-    const size_t nk = (size_t)a->B * a->Hkv * a->Lkv * a->D;
-    cudaError_t e = launch_f32_to_f16(static_cast<const float*>(a->q), ws + pl.off_q, nq, stream);
-    if (e == cudaSuccess) e = launch_f32_to_f16(static_cast<const float*>(a->k), ws + pl.off_k, nk, stream);
-    if (e == cudaSuccess) e = launch_f32_to_f16(static_cast<const float*>(a->v), ws + pl.off_v, nk, stream);
-    if (e != cudaSuccess) return cuda_fail("fa_prefill (fp32 staging)", e);
-    p.q = ws + pl.off_q;
-    p.k = ws + pl.off_k;
-    p.v = ws + pl.off_v;
-    operand = Dtype::FP16;
-  }
+  const Dtype operand = static_cast<Dtype>(a->dtype);
   if (a->Lkv == 0 && a->page_size == 0) {  // keep the tensor maps valid; no key is read
     p.k = p.q;
     p.v = p.q;
@@ -306,6 +287,11 @@ int run_prefill(const fa_prefill_args* a, cudaStream_t stream) {
   p.lse_part = pl.n_splits > 1 ? reinterpret_cast<float*>(ws + pl.off_lse) : nullptr;
   p.out_dtype = static_cast<Dtype>(a->dtype);
   p.status = status;
+  if (operand == Dtype::FP32) {
+    cudaError_t e = launch_prefill_f32(p, stream);
+    if (e != cudaSuccess) return cuda_fail("fa_prefill (fp32 kernel)", e);
+    return FA_OK;
+  }
   cudaError_t e = launch_prefill(p, operand, stream);
   if (e != cudaSuccess) return cuda_fail("fa_prefill (attention kernel)", e);
   if (pl.n_splits > 1) {

@@ -128,8 +128,8 @@ struct MergeParams {
 };
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 
-// fp32 -> fp16 element conversion (used for fp32 prefill inputs).
-cudaError_t launch_f32_to_f16(const float* src, void* dst, size_t n, cudaStream_t stream);
+// Attention for fp32 inputs in fp32 on the CUDA cores (prefill_f32.cu): dense K/V, no split.
+cudaError_t launch_prefill_f32(const PrefillParams& p, cudaStream_t stream);
 
 // Checks a decode call's arguments (sizes, dtype, pointers, alignment of q, pages and out)
 // as fa_decode_paged_ex does; sets the error text and returns the fa_status code.

@@ -115,11 +115,6 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
   if (lane == 0 && p.lse) p.lse[row] = lse;
 }
 
-__global__ void f32_to_f16_kernel(const float* __restrict__ src, __half* __restrict__ dst, size_t n) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-    dst[i] = __float2half_rn(src[i]);
-}
-
 }  // namespace
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
@@ -136,15 +131,6 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
     case 3: merge_kernel<3><<<grid, kMergeWarps * 32, smem, stream>>>(p, W); break;
     default: merge_kernel<4><<<grid, kMergeWarps * 32, smem, stream>>>(p, W); break;
   }
-  return cudaGetLastError();
-}
-
-cudaError_t launch_f32_to_f16(const float* src, void* dst, size_t n, cudaStream_t stream) {
-  if (n == 0) return cudaSuccess;
-  const int threads = 256;
-  size_t blocks = (n + threads - 1) / threads;
-  if (blocks > 4096) blocks = 4096;
-  f32_to_f16_kernel<<<(unsigned)blocks, threads, 0, stream>>>(src, static_cast<__half*>(dst), n);
   return cudaGetLastError();
 }
 

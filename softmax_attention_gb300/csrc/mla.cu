@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t t_last = global_timer_ns();
       while (ok && next_pv < n_tiles) {
         bool progress = false;
-        if (next_s < n_tiles && next_s <= next_pv + 1 && stage_landed(2 * next_s) &&
+        if (next_s < n_tiles && next_s <= next_pv && stage_landed(2 * next_s) &&
             stage_landed(2 * next_s + 1)) {
           tc_fence_after();
           issue_s(next_s++);

@@ -83,9 +83,11 @@ def test_empty_work_is_ok_without_device(lib):
 
 
 def test_workspace_sizes_are_consistent(lib):
-    # fp32 inputs need fp16 staging; forced splits need partial states
-    a = _args(dtype=fa.FA_FP32)
-    assert lib.fa_prefill_workspace_size(ctypes.byref(a)) >= (1 * 4 * 8 + 2 * 1 * 2 * 8) * 128 * 2
+    # fp32 inputs run unsplit in fp32 (no workspace, even when a split is asked for); forced
+    # splits of 16-bit inputs need partial states
+    a = _args(dtype=fa.FA_FP32, num_splits=4, Lkv=4096)
+    assert lib.fa_prefill_workspace_size(ctypes.byref(a)) == 0
+    assert lib.fa_prefill_num_splits(ctypes.byref(a)) == 1
     a = _args(num_splits=4, Lkv=4096)
     assert lib.fa_prefill_num_splits(ctypes.byref(a)) == 4
     assert lib.fa_prefill_workspace_size(ctypes.byref(a)) >= 1 * 4 * 8 * 4 * (128 + 1) * 4
@@ -133,9 +135,8 @@ def test_merge_rejects_bad_arguments(lib):
 
 
 def test_size_queries_ignore_pointers(lib):
-    a = _args(dtype=fa.FA_FP32, q=None, k=None, v=None, out=None)
+    a = _args(num_splits=3, Lkv=4096, q=None, k=None, v=None, out=None)
     assert lib.fa_prefill_workspace_size(ctypes.byref(a)) > 0
-    a = _args(num_splits=3, Lkv=4096, q=None, out=None)
     assert lib.fa_prefill_num_splits(ctypes.byref(a)) == 3
 
 

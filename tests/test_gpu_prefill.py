@@ -58,6 +58,34 @@ def test_tiny_fp32(causal):
     check(out, lse, ro, rl, what=f"tiny causal={causal}")
 
 
+def _fp32_range_case(q_mag, k_mag, v_mag, seed):
+    c = workloads.DenseCase(B=1, Hq=4, Hkv=2, Lq=70, Lkv=300, D=64, causal=True,
+                            dtype=torch.float32, sigma=1.0, seed=seed)
+    q, k, v = workloads.dense_inputs(c)
+    return c, q * q_mag, k * k_mag, v * v_mag
+
+
+@pytest.mark.parametrize("q_mag,k_mag,v_mag", [(1e5, 1e-5, 1e5), (1e-20, 1e20, 1e-30),
+                                               (1.0, 1.0, 3e37)])
+def test_fp32_keeps_range_and_precision(q_mag, k_mag, v_mag):
+    # magnitudes fp16 cannot hold (above 65504, below its subnormals): fp32 inputs are not
+    # narrowed, so the result matches the oracle to fp32 precision relative to its scale
+    c, q, k, v = _fp32_range_case(q_mag, k_mag, v_mag, seed=17)
+    dev = torch.device("cuda")
+    og, lg = Guarded(q.shape, torch.float32), Guarded(q.shape[:-1], torch.float32)
+    out, lse = fa.fa_prefill_ex(q.to(dev), k.to(dev), v.to(dev), causal=True, scale=c.sm_scale,
+                                out=og.view, lse=lg.view)
+    torch.cuda.synchronize()
+    og.assert_intact("fp32 out")
+    lg.assert_intact("fp32 lse")
+    ro, rl = oracle.attention(q, k, v, causal=True, scale=c.sm_scale)
+    o64 = out.double().cpu()
+    assert torch.isfinite(o64).all()
+    rel = ((o64 - ro).abs().max() / ro.abs().max()).item()
+    assert rel <= 1e-5, f"relative max error {rel:.3e}"
+    assert (lse.double().cpu() - rl).abs().max().item() <= 1e-4
+
+
 CASES = [
     # B, Hq, Hkv, Lq, Lkv, D, causal
     (1, 4, 4, 200, 333, 64, False),
