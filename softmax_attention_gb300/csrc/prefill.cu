@@ -33,7 +33,7 @@ namespace {
 
 using prefill::kRows;
 constexpr int kThreads = 224;
-constexpr int kLptMaxSeqs = 64;  // paged: order sequences by length when there are at most this many
+constexpr int kLptMaxSeqs = kThreads;  // paged: order sequences by length (one ranking thread each)
 
 // 5-D tiled TMA load (the paged K/V boxes below).
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
