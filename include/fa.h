@@ -236,7 +236,9 @@ int fa_decode_paged_states(const void* q, const void* k_pages, const void* v_pag
  *   ckv_pages [num_pages, page_size, Dc] bf16, kpe_pages [num_pages, page_size, Dr] bf16
  *   page_table [B, max_pages_per_seq] int32, seq_lens [B] int32
  *   out [B, H, Dc] bf16 (latent space), lse [B, H] fp32 or NULL
- *   Dc == 512, Dr == 64, H == 64 (one tensor-core tile of heads).  Any page_size >= 1;
+ *   Dc == 512, Dr == 64, 1 <= H <= 1024: each CTA takes one group of up to 64 heads (one
+ *   tensor-core tile of heads), so 128 heads read a sequence's cache twice (the second read
+ *   mostly from L2) and fewer than 64 heads leave part of the tile idle.  Any page_size >= 1;
  *   pages of a multiple of 64 tokens are copied a 64-token tile at a time with TMA.
  *   workspace >= mla_decode_workspace_size(B, H, Dc, max_seq_len) bytes.
  */

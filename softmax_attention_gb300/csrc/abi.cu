@@ -621,9 +621,10 @@ int check_mla(const void* q_nope, const void* q_pe, const void* ckv_pages, const
               int page_size, int max_pages_per_seq, int num_pages, int max_seq_len, float scale) {
   if (B < 0 || H <= 0 || Dc <= 0 || Dr < 0)
     return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: need B >= 0, H, Dc > 0, Dr >= 0");
-  if (Dc != 512 || Dr != 64 || H != 64)
-    return fail(FA_ERR_UNSUPPORTED, "mla_decode_paged: supports Dc=512, Dr=64, H=64 (got %d, %d, %d)",
-                Dc, Dr, H);
+  if (Dc != 512 || Dr != 64)
+    return fail(FA_ERR_UNSUPPORTED, "mla_decode_paged: supports Dc=512, Dr=64 (got %d, %d)", Dc, Dr);
+  if (H > 1024)
+    return fail(FA_ERR_UNSUPPORTED, "mla_decode_paged: H must be <= 1024 (got %d)", H);
   if (page_size <= 0) return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: page_size must be > 0");
   if (max_pages_per_seq < 0 || num_pages < 0 || max_seq_len < 0)
     return fail(FA_ERR_INVALID_ARG, "mla_decode_paged: negative size");

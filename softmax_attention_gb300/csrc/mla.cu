@@ -117,8 +117,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* stat_s = alpha_s + 64;  // [0..63]: l per head (epilogue)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // whole sequences first, then the chunks of the split ones
-  const int bx = blockIdx.x;
+  // Each CTA takes one group of up to 64 heads (hb .. hb + hv - 1) of one work item; items
+  // are whole sequences first, then the chunks of the split ones.  Head rows past H read as
+  // zero and are not written.
+  const int n_groups = (p.H + kH - 1) / kH;
+  const int bx = blockIdx.x / n_groups;
+  const int hb = (blockIdx.x % n_groups) * kH, hv = min(kH, p.H - hb);
   const bool direct = bx < p.n_whole;
   const int b = direct ? bx : p.n_whole + (bx - p.n_whole) / p.n_chunks;
   const int c = direct ? 0 : (bx - p.n_whole) % p.n_chunks;
@@ -132,10 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (t_start >= len) {
     // an empty sequence still owns its final output when this launch writes it directly
     if (direct) {
-      for (int i = threadIdx.x; i < kH * kDc / 8; i += kThreads)
-        reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + static_cast<size_t>(b) * kH * kDc)[i] =
-            make_uint4(0, 0, 0, 0);
-      if (threadIdx.x < kH && p.lse) p.lse[static_cast<size_t>(b) * kH + threadIdx.x] = -INFINITY;
+      const size_t r0 = static_cast<size_t>(b) * p.H + hb;
+      for (int i = threadIdx.x; i < hv * kDc / 8; i += kThreads)
+        reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + r0 * kDc)[i] = make_uint4(0, 0, 0, 0);
+      if (threadIdx.x < hv && p.lse) p.lse[r0 + threadIdx.x] = -INFINITY;
     }
     return;
   }
@@ -182,8 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mbar_arrive_expect_tx(bar_q, kQBytes);
       for (int kb = 0; kb < kDc / 64; ++kb)
-        tma_load_2d(sQ + kb * (kH * 128), &tm_qn, bar_q, kb * 64, b * kH);
-      tma_load_2d(sQ + (kDc / 64) * (kH * 128), &tm_qp, bar_q, 0, b * kH);
+        tma_load_3d(sQ + kb * (kH * 128), &tm_qn, bar_q, kb * 64, hb, b);
+      tma_load_3d(sQ + (kDc / 64) * (kH * 128), &tm_qp, bar_q, 0, hb, b);
     }
     // Row ids: a group is four 32-token stages; lane l holds the row of token
     // 32 * (4g + (l >> 3)) + 8pw + (l & 7) of the current group g, and the page id of the
@@ -498,11 +502,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     softmax_sync();
     if (ok) {
-      const size_t row0 = static_cast<size_t>(b) * kH;                 // output rows
-      const size_t prow0 = static_cast<size_t>(b - p.n_whole) * kH;    // partial-state rows
+      const size_t row0 = static_cast<size_t>(b) * p.H + hb;               // output rows
+      const size_t prow0 = static_cast<size_t>(b - p.n_whole) * p.H + hb;  // partial-state rows
 #pragma unroll 1
       for (int r = 0; r < 16; ++r) {
         const int hh = warp * 16 + r;
+        if (hh >= hv) break;
         const float4* src = reinterpret_cast<const float4*>(ostage + hh * kDc);
         if (direct) {
           // the whole sequence was this CTA's chunk: write the final bf16 row
@@ -522,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kDc / 4 / 32; ++k) dst[lane + 32 * k] = src[lane + 32 * k];
         }
       }
-      if (lead) {
+      if (lead && h < hv) {
         const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
         if (!direct) p.lse_part[(prow0 + h) * p.n_chunks + c] = lse_v;
         else if (p.lse) p.lse[row0 + h] = lse_v;
@@ -542,8 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Tokens per CTA: each CTA pays a fixed cost (pipeline start, epilogue) worth a few hundred
 // tokens of streaming, so prefer long chunks, but keep the waves of CTAs balanced.
-int mla_chunk_tokens(int B, int, int max_seq_len) {
+int mla_chunk_tokens(int B, int H, int max_seq_len) {
   const int sms = num_sms() > 0 ? num_sms() : 148;
+  B *= (H + kH - 1) / kH;  // CTAs per chunk of the batch: one per group of 64 heads
   const int len = ((max_seq_len + kTile - 1) / kTile) * kTile;
   int best = 512;
   long best_cost = -1;
@@ -578,6 +584,7 @@ MlaPlan mla_plan(int B, int H, int max_seq_len) {
   pl.whole_chunk = chunk;
   pl.chunk = chunk;
   pl.n_chunks = 1;
+  if (H > kH) return pl;  // several head groups per sequence: no short-wave split
   const int sms = num_sms() > 0 ? num_sms() : 148;
   const int waves = (B + sms - 1) / sms;
   const int tail = B - (waves - 1) * sms;  // sequences in the last wave
@@ -596,7 +603,7 @@ MlaPlan mla_plan(int B, int H, int max_seq_len) {
 
 cudaError_t launch_mla(const MlaParams& params, cudaStream_t stream) {
   MlaParams p = params;
-  if (p.H != kH || p.Dc != kDc || p.Dr != kDr || p.n_whole < 0 || p.n_whole > p.B)
+  if (p.H < 1 || p.Dc != kDc || p.Dr != kDr || p.n_whole < 0 || p.n_whole > p.B)
     return cudaErrorInvalidValue;
   if (p.n_whole > 0 && (p.whole_chunk % kTile != 0 || p.whole_chunk > kMaxChunk))
     return cudaErrorInvalidValue;
@@ -604,22 +611,20 @@ cudaError_t launch_mla(const MlaParams& params, cudaStream_t stream) {
       (p.n_chunks < 1 || p.chunk % kTile != 0 || p.chunk > kMaxChunk || !p.o_part || !p.lse_part))
     return cudaErrorInvalidValue;
   CUtensorMap tqn, tqp;
-  const uint64_t qrows = static_cast<uint64_t>(p.B) * kH;
   const CUtensorMapDataType dt = p.f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   {
-    const uint64_t dims[2] = {kDc, qrows};
-    const uint64_t str[1] = {kDc * 2};
-    const uint32_t box[2] = {64, kH};
-    if (!encode_tiled(&tqn, dt, 2, p.q_nope, dims, str, box,
-                      CU_TENSOR_MAP_SWIZZLE_128B))
+    // (latent column, head, sequence): a box of 64 columns x 64 heads, heads past H zero
+    const uint64_t dims[3] = {kDc, static_cast<uint64_t>(p.H), static_cast<uint64_t>(p.B)};
+    const uint64_t str[2] = {kDc * 2, static_cast<uint64_t>(p.H) * kDc * 2};
+    const uint32_t box[3] = {64, kH, 1};
+    if (!encode_tiled(&tqn, dt, 3, p.q_nope, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   {
-    const uint64_t dims[2] = {kDr, qrows};
-    const uint64_t str[1] = {kDr * 2};
-    const uint32_t box[2] = {64, kH};
-    if (!encode_tiled(&tqp, dt, 2, p.q_pe, dims, str, box,
-                      CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint64_t dims[3] = {kDr, static_cast<uint64_t>(p.H), static_cast<uint64_t>(p.B)};
+    const uint64_t str[2] = {kDr * 2, static_cast<uint64_t>(p.H) * kDr * 2};
+    const uint32_t box[3] = {64, kH, 1};
+    if (!encode_tiled(&tqp, dt, 3, p.q_pe, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   // Tile-sized TMA copies (see the producer) when a page holds whole 64-token tiles.  The
@@ -641,7 +646,8 @@ cudaError_t launch_mla(const MlaParams& params, cudaStream_t stream) {
   auto kern = p.f16 ? mla_kernel<false> : mla_kernel<true>;
   cudaError_t e = ensure_smem_limit(kern, kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long ctas = p.n_whole + static_cast<long>(p.B - p.n_whole) * (p.n_whole < p.B ? p.n_chunks : 0);
+  const long ctas = static_cast<long>((p.H + kH - 1) / kH) *
+                    (p.n_whole + static_cast<long>(p.B - p.n_whole) * (p.n_whole < p.B ? p.n_chunks : 0));
   if (ctas <= 0) return cudaSuccess;
   if (ctas > 0x7fffffffL) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(ctas));

@@ -122,9 +122,10 @@ def test_decode_rejects_bad_arguments(lib, args, code):
 
 
 def test_mla_rejects_unsupported_shapes(lib):
-    rc = lib.mla_decode_paged(*([4096] * 7), None, 2, 128, 512, 64, 1, 16, 32, 16, 0.1, 4096,
-                              1 << 30, None)
-    assert rc == fa.FA_ERR_UNSUPPORTED
+    for H, Dc, Dr in ((2048, 512, 64), (64, 256, 64), (64, 512, 32)):
+        rc = lib.mla_decode_paged(*([4096] * 7), None, 2, H, Dc, Dr, 1, 16, 32, 16, 0.1, 4096,
+                                  1 << 30, None)
+        assert rc == fa.FA_ERR_UNSUPPORTED, (H, Dc, Dr)
 
 
 def test_merge_rejects_bad_arguments(lib):

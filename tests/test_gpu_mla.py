@@ -55,6 +55,21 @@ def test_parity_shapes(lens, ps):
     check(out, lse, ro, rl, what=f"mla {lens} ps={ps}")
 
 
+@pytest.mark.parametrize("H,lens,ps", [
+    (16, [100, 700, 0], 1),      # one tensor-parallel shard's heads: a partial head group
+    (32, [513, 64], 16),
+    (128, [300, 1500, 65], 1),   # two head groups per sequence
+    (96, [200, 129], 64),        # a full and a partial group
+    (128, [4000, 100], 1),       # several chunks per sequence, merged
+    (1, [77], 1),
+])
+def test_head_counts(H, lens, ps):
+    c = workloads.MlaCase(B=len(lens), H=H, seq_len=None, seq_lens=lens, page_size=ps,
+                          seed=H + len(lens))
+    out, lse, ro, rl = _run(c)
+    check(out, lse, ro, rl, what=f"mla H={H} {lens} ps={ps}")
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 def test_short_last_wave_is_split(dtype):
     """More sequences than SMs, one chunk each: the sequences of the short last wave are cut
