@@ -77,6 +77,7 @@ KERNEL_SOURCES = {
     "prefill": ("prefill.cu", "prefill_common.cuh", "sm103.cuh", "internal.h"),
     "decode": ("decode.cu", "sm103.cuh", "internal.h"),
     "mla": ("mla.cu", "sm103.cuh", "internal.h"),
+    "gated_delta": ("gated_delta.cu", "sm103.cuh", "internal.h"),
 }
 
 
@@ -437,7 +438,8 @@ def bench_gated_delta(fa, c, steps, warmup, flush, dist, pk):
     res = {"value": round(nbytes / (f_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms": round(f_ms, 4),
            "tokens_per_s": round(c.B * c.T / (f_ms * 1e-3), 1), "bytes": nbytes,
            "launches_per_step": 2, "mode": mode,
-           "roofline": roofline("hbm", nbytes / (f_ms * 1e-3) / 1e9, pk["hbm"], "GB/s", None, pk)}
+           "roofline": roofline("hbm", nbytes / (f_ms * 1e-3) / 1e9, pk["hbm"], "GB/s",
+                                profiled_traffic("gated_delta_prefill.md", "gated_delta"), pk)}
     del q, k, v, g, beta, out, st, ws
     torch.cuda.empty_cache()
     return res
@@ -619,7 +621,8 @@ def mqa_point(r, mc, pk):
     return {"value": round(r["tflops"], 2), "unit": "TFLOP/s", "ms": round(r["ms"], 4),
             "splits": r["splits"], "launches_per_step": r["launches_per_step"],
             "roofline": roofline(bound, ach, pk["hbm"] if bound == "hbm" else pk["bf16"],
-                                 "GB/s" if bound == "hbm" else "TFLOP/s", None, pk)}
+                                 "GB/s" if bound == "hbm" else "TFLOP/s",
+                                 profiled_traffic(f"prefill_mqa_lq{mc.Lq}.md", "prefill"), pk)}
 
 
 def main():
