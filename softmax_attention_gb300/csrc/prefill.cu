@@ -14,14 +14,14 @@
 // one 5-D TMA box, and each sequence has its own length.
 //
 // Warp roles (224 threads): warps 0-3 softmax + epilogue (thread t owns row t), warp 4 TMA
-// producer, warp 5 MMA issuer (one elected thread) and tensor-memory owner, warp 6 the
-// landing watcher.  Once a thread has committed MMAs, its next shared-memory access (an
-// mbarrier wait included) is held until those MMAs finish, so every wait the issuer makes
-// drains the tensor pipe.  The issuer therefore waits once per KV tile, on ready[j % STAGES],
-// whose phase completes when the softmax has written P_j (128 arrivals) and the watcher has
-// seen V_j and K_{j+2} land (1 arrival); it then issues P_j V_j and S_{j+2} back to back.
-// With two stages K_{j+2} can only load once S_j is done, too late to gate P_j V_j, so there
-// the watcher covers V_j alone and the issuer waits for K_{j+2} itself.
+// producer, warp 5 the P V issuer (one elected thread) and tensor-memory owner, warp 6 the
+// S issuer (one elected thread).  Once a thread has committed MMAs, its next shared-memory
+// access (an mbarrier wait included) is held until those MMAs finish, so a single issuer that
+// waits for P_j drains the tensor pipe every tile.  With two issuers each wait holds only
+// its own thread's MMAs: while the P V issuer waits for the softmax, the S issuer's next
+// products keep the tensor pipe busy, and the other way round.  S/P has three buffers in
+// tensor memory (S_j in buffer j % 3), so S can run up to two tiles ahead of the softmax;
+// S_{j+3} is issued into P_j's buffer once P_j V_j has finished.
 #include <math.h>
 
 #include "internal.h"
@@ -47,6 +47,8 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+constexpr int kNumS = 3;  // S/P buffers in tensor memory
+
 template <int D, int BN, int STAGES>
 struct Layout {
   static constexpr int kQBytes = kRows * D * 2;
@@ -55,12 +57,15 @@ struct Layout {
   static constexpr int kKOff = kQBytes;
   static constexpr int kVOff = kKOff + STAGES * kKVBytes;
   static constexpr int kBarOff = kVOff + STAGES * kKVBytes;
-  // q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], ready[S], o_full,
-  // mma_done, q_in_tmem
-  static constexpr int kNumBars = 1 + 5 * STAGES + 2 + 3;
+  // Q, the A operand of S, also goes into tensor memory when it fits beside O and the S/P
+  // buffers (D/2 columns): S then reads only K from shared memory.
+  static constexpr bool kQInTmem = D + kNumS * BN + D / 2 <= 512;
+  // q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[3], p_full[3], pv_done[3],
+  // pv_issuer_done, s_issuer_done, q_in_tmem
+  static constexpr int kNumBars = 1 + 4 * STAGES + 3 * kNumS + 3;
   static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 bytes
-  static_assert(D + 2 * BN + D / 2 <= 512, "tensor memory budget (O, two S/P buffers, Q)");
+  static_assert(D + kNumS * BN <= 512, "tensor memory budget (O and the S/P buffers)");
   static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
@@ -70,7 +75,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using L = Layout<D, BN, STAGES>;
-  constexpr bool kWatchK = STAGES >= 3;  // ready[j] also covers K_{j+2}
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -82,12 +86,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_v = [&](int s) { return bars + 8u * (1 + STAGES + s); };
   auto bar_ke = [&](int s) { return bars + 8u * (1 + 2 * STAGES + s); };
   auto bar_ve = [&](int s) { return bars + 8u * (1 + 3 * STAGES + s); };
+  // per S/P buffer b (tile j with j % 3 == b): S_j computed, P_j written, P_j V_j finished
   auto bar_s = [&](int b) { return bars + 8u * (1 + 4 * STAGES + b); };
-  // ready[s]: P_j written, V_j landed and K_{j+2} landed, for the tile j with j % S == s
-  auto bar_r = [&](int s) { return bars + 8u * (3 + 4 * STAGES + s); };
-  const uint32_t bar_o = bars + 8u * (3 + 5 * STAGES);
-  const uint32_t bar_done = bars + 8u * (4 + 5 * STAGES);
-  const uint32_t bar_qt = bars + 8u * (5 + 5 * STAGES);  // Q copied into tensor memory
+  auto bar_p = [&](int b) { return bars + 8u * (1 + 4 * STAGES + kNumS + b); };
+  auto bar_pv = [&](int b) { return bars + 8u * (1 + 4 * STAGES + 2 * kNumS + b); };
+  const uint32_t bar_done = bars + 8u * (1 + 4 * STAGES + 3 * kNumS);
+  const uint32_t bar_sdone = bar_done + 8u;
+  const uint32_t bar_qt = bar_done + 16u;  // Q copied into tensor memory (kQInTmem)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBarOff + L::kNumBars * 8);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -144,12 +149,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_v(s), 1);
       mbar_init(bar_ke(s), 1);
       mbar_init(bar_ve(s), 1);
-      mbar_init(bar_r(s), 4 * 32 + 1);
     }
-    mbar_init(bar_s(0), 1);
-    mbar_init(bar_s(1), 1);
-    mbar_init(bar_o, 1);
+    for (int b = 0; b < kNumS; ++b) {
+      mbar_init(bar_s(b), 1);
+      mbar_init(bar_p(b), 4 * 32);
+      mbar_init(bar_pv(b), 1);
+    }
     mbar_init(bar_done, 1);
+    mbar_init(bar_sdone, 1);
     mbar_init(bar_qt, 4 * 32);
     fence_barrier_init();
   }
@@ -163,9 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tm_o = tmem;           // O: columns [0, D)
   const uint32_t tm_s0 = tmem + D;      // S/P buffer b: columns [D + b*BN, D + (b+1)*BN)
-  // Q, the A operand of S: row r in lane r, element pairs packed per column (D/2 columns).
-  // Taking A from tensor memory leaves only K to be read from shared memory per S MMA.
-  const uint32_t tq_tmem = tmem + D + 2 * BN;
+  // Q (kQInTmem): row r in lane r, element pairs packed per column (D/2 columns)
+  const uint32_t tq_tmem = tmem + D + kNumS * BN;
 
   if (warp == 4) {
     // ------------------------------- TMA producer ---------------------------------------
@@ -265,78 +271,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 5) {
-    // ------------------------------- MMA issuer -----------------------------------------
+    // ------------------------------- P V issuer -----------------------------------------
     if (lane == 0 && n > 0) {
-      constexpr uint32_t idesc_s = idesc_f16(BF16, kRows, BN, false, false);
       constexpr uint32_t idesc_o = idesc_f16(BF16, kRows, D, false, true);
-      auto issue_s = [&](int jj) {
-        const uint32_t kbase = sK + (jj % STAGES) * L::kKVBytes;
-        const uint32_t d_s = tm_s0 + (jj & 1) * BN;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk % 4) * 32;
-          const uint64_t bd = sdesc_sw128(kbase + (kk / 4) * kCB + off, 16, kRG);
-          mma_ts(d_s, tq_tmem + kk * 8, bd, idesc_s, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(bar_s(jj & 1));
-        tc_commit(bar_ke(jj % STAGES));
-      };
-      // S_0 and S_1 up front; afterwards one wait per tile (ready[j]) and no other shared-
-      // memory access, since each would be held until the committed MMAs finish.
-      bool ok = mbar_wait(bar_qt, 0, p.status) && mbar_wait(bar_k(0), 0, p.status);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-      }
-      if (ok && n > 1 && (ok = mbar_wait(bar_k(1), 0, p.status))) {
-        tc_fence_after();
-        issue_s(1);
-      }
+      // descriptors are built once; per tile and K step only their start address moves
+      const uint64_t v_desc = sdesc_sw128(sV, kCB, kRG);
+      bool ok = true;
       for (int jj = 0; ok && jj < n; ++jj) {
-        const int stage = jj % STAGES;
-        if (!(ok = mbar_wait(bar_r(stage), (jj / STAGES) & 1, p.status))) break;
+        const int stage = jj % STAGES, buf = jj % kNumS;
+        // the first wait is held until P_{j-1} V_j-1 finishes; the second then finds V_j
+        if (!(ok = mbar_wait(bar_p(buf), (jj / kNumS) & 1, p.status))) break;
+        if (!(ok = mbar_wait(bar_v(stage), (jj / STAGES) & 1, p.status))) break;
         tc_fence_after();
-        const uint32_t vbase = sV + stage * L::kKVBytes;
-        const uint32_t a_p = tm_s0 + (jj & 1) * BN;
+        const uint64_t vd = sdesc_add(v_desc, stage * L::kKVBytes);
+        const uint32_t a_p = tm_s0 + buf * BN;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(vbase + kk * (2 * kRG), kCB, kRG);
-          mma_ts(tm_o, a_p + kk * 8, bd, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(bar_o);
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tm_o, a_p + kk * 8, sdesc_add(vd, kk * (2 * kRG)), idesc_o,
+                 (jj > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar_pv(buf));
         tc_commit(bar_ve(stage));
-        // S_{j+2} goes into the buffer that holds P_j: the tensor pipe runs one thread's MMAs
-        // in order, so P_j V_j has read P_j before S_{j+2} overwrites it.
-        if (jj + 2 < n) {
-          if constexpr (!kWatchK) {
-            if (!(ok = mbar_wait(bar_k((jj + 2) % STAGES), ((jj + 2) / STAGES) & 1, p.status))) break;
-            tc_fence_after();
-          }
-          issue_s(jj + 2);
-        }
       }
       // Every MMA this thread issued must finish before tensor memory is released.
       tc_commit(bar_done);
       mbar_wait(bar_done, 0, nullptr);
     }
   } else if (warp == 6) {
-    // ------------------------------ landing watcher -------------------------------------
-    // One arrival on ready[j] once V_j and K_{j+2} have landed.  It can run ahead of the
-    // softmax by at most STAGES tiles: V_{j+STAGES} is only loaded after P_j V_j is done.
+    // --------------------------------- S issuer -----------------------------------------
+    // S_j = Q K_j^T into buffer j % 3 once K_j has landed and, from j = 3 on, P_{j-3} V_{j-3}
+    // (the last reader of that buffer) has finished.  It runs at most two tiles ahead of the
+    // softmax, and the K ring bounds it by STAGES.
     if (lane == 0 && n > 0) {
-      // K_0 and K_1 are otherwise waited for only by the issuer.  Their stages later hold
-      // K_STAGES and K_{STAGES+1}, which this warp does wait for; observing phase 0 first keeps
-      // those parity waits exact whatever order the loads complete in.
-      bool okw = !kWatchK ||
-                 (mbar_wait(bar_k(0), 0, p.status) && (n < 2 || mbar_wait(bar_k(1), 0, p.status)));
-      for (int jj = 0; okw && jj < n; ++jj) {
-        const int stage = jj % STAGES;
-        if (!mbar_wait(bar_v(stage), (jj / STAGES) & 1, p.status)) break;
-        if (kWatchK && jj + 2 < n &&
-            !mbar_wait(bar_k((jj + 2) % STAGES), ((jj + 2) / STAGES) & 1, p.status))
-          break;
-        mbar_arrive(bar_r(stage));
+      constexpr uint32_t idesc_s = idesc_f16(BF16, kRows, BN, false, false);
+      const uint64_t k_desc = sdesc_sw128(sK, 16, kRG);
+      const uint64_t q_desc = sdesc_sw128(sQ, 16, 1024);
+      bool ok = L::kQInTmem ? mbar_wait(bar_qt, 0, p.status) : mbar_wait(bar_q, 0, p.status);
+      for (int jj = 0; ok && jj < n; ++jj) {
+        const int stage = jj % STAGES, buf = jj % kNumS;
+        if (!(ok = mbar_wait(bar_k(stage), (jj / STAGES) & 1, p.status))) break;
+        if (jj >= kNumS && !(ok = mbar_wait(bar_pv(buf), ((jj - kNumS) / kNumS) & 1, p.status))) break;
+        tc_fence_after();
+        const uint64_t kd = sdesc_add(k_desc, stage * L::kKVBytes);
+        const uint32_t d_s = tm_s0 + buf * BN;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk % 4) * 32;
+          const uint64_t bd = sdesc_add(kd, (kk / 4) * kCB + off);
+          if constexpr (L::kQInTmem) {
+            mma_ts(d_s, tq_tmem + kk * 8, bd, idesc_s, kk > 0 ? 1u : 0u);
+          } else {
+            mma_ss(d_s, sdesc_add(q_desc, (kk / 4) * (kRows * 128) + off), bd, idesc_s,
+                   kk > 0 ? 1u : 0u);
+          }
+        }
+        tc_commit(bar_s(buf));
+        tc_commit(bar_ke(stage));
       }
+      tc_commit(bar_sdone);
+      mbar_wait(bar_sdone, 0, nullptr);
     }
   } else {
     // ------------------------- softmax + epilogue (row per thread) ----------------------
@@ -344,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    if (n > 0) {
+    if (L::kQInTmem && n > 0) {
       // Copy this thread's Q row from the swizzled shared-memory tile into its tensor-memory
       // lane: 64-column block kb, 16-byte chunk ch of row r sits at chunk ch ^ (r & 7).
       ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, p.status));
@@ -370,8 +362,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     for (int jj = 0; ok && jj < n; ++jj) {
-      const uint32_t t_s = tm_s0 + lane_off + (jj & 1) * BN;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_s(jj & 1), (jj >> 1) & 1, p.status));
+      const int buf = jj % kNumS;
+      const uint32_t t_s = tm_s0 + lane_off + buf * BN;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_s(buf), (jj / kNumS) & 1, p.status));
       if (!ok) break;
       tc_fence_after();
       uint32_t raw[BN];
@@ -381,13 +374,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the exponentials overlap the previous tile's P V on the tensor cores
       const bool need = prefill::softmax_tile<BN, BF16>(p, row, (t_begin + jj) * BN, raw, m_run,
                                                         l_run, alpha, pk);
-      // O must hold every earlier P V product before it is rescaled or fed P_j; waiting on
-      // each phase in turn also keeps this warp at most one tile ahead of the MMA issuer.
-      if (jj > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (jj - 1) & 1, p.status));
+      // O is rescaled only once every earlier P V product is in it (the P V issuer runs its
+      // products in order, so P_{j-1} V_{j-1} finishing means all have).  A tile with no
+      // rescale does not wait: P_j V_j is issued after P_j anyway, and this warp cannot get
+      // two phases ahead on a P V barrier, since S_j itself needed P_{j-3} V_{j-3} finished.
+      const bool rescale = jj > 0 && __any_sync(0xffffffffu, need);
+      if (rescale) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_pv((jj - 1) % kNumS), ((jj - 1) / kNumS) & 1, p.status));
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) prefill::rescale_o<D>(tm_o + lane_off, alpha);
+        prefill::rescale_o<D>(tm_o + lane_off, alpha);
       }
       prefill::store_p<BN>(t_s, pk);
       tmem_st_wait();
@@ -395,7 +391,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (PAGED && key0 + BN > Lkv) {
         // Rows past the sequence's end hold whatever the pool has there; P is 0 for them,
         // but 0 times a non-finite V would still poison O, so clear them once V has landed.
+        // The parity wait for V_j is exact only once the stage's previous tile V_{j-STAGES}
+        // has landed: waiting first for P_{j-1} V_{j-1} (in order, so V_{j-STAGES} was read)
+        // makes sure of it.
         const int stage = jj % STAGES;
+        if (jj > 0 && !rescale) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar_pv((jj - 1) % kNumS), ((jj - 1) / kNumS) & 1, p.status));
+          if (!ok) break;
+        }
         ok = __all_sync(0xffffffffu, mbar_wait(bar_v(stage), (jj / STAGES) & 1, p.status));
         if (!ok) break;
         const int r0 = Lkv - key0;
@@ -409,10 +412,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
       }
       tc_fence_before();
-      mbar_arrive(bar_r(jj % STAGES));
+      mbar_arrive(bar_p(buf));
     }
     if (ok && n > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (n - 1) & 1, p.status));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_pv((n - 1) % kNumS), ((n - 1) / kNumS) & 1, p.status));
       tc_fence_after();
     }
     if (ok) {

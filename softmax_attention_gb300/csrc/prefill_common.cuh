@@ -43,6 +43,13 @@ __device__ __forceinline__ Row make_row(const PrefillParams& p, int b, int hk, i
   return row;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // One KV tile of the online softmax for one row: raw = the tile's S row (fp32 bits, keys
 // key0..key0+BN-1).  Updates the running max m (log2 units) and sum l, writes P (16-bit
 // pairs, even key in the low half) to pk, and returns whether O must be rescaled by alpha.
@@ -57,6 +64,9 @@ __device__ __forceinline__ bool softmax_tile(const PrefillParams& p, const Row& 
   // Masked keys hold -inf either way.  Eight independent max accumulators keep the
   // reduction's dependency chain short.
   const bool fast = !row.mask && p.scale_log2 > 0.f;
+  // 64-key tiles reduce the max after x is built, with three-input max instructions (measured
+  // faster there); 128-key tiles fold a two-input max into the loops that build x.
+  constexpr bool kMax3 = BN <= 64;
   float x[BN];
   float mx[8];
 #pragma unroll
@@ -66,13 +76,13 @@ __device__ __forceinline__ bool softmax_tile(const PrefillParams& p, const Row& 
 #pragma unroll
       for (int c = 0; c < BN; ++c) {
         x[c] = __uint_as_float(raw[c]);
-        mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+        if constexpr (!kMax3) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
       }
     } else {
 #pragma unroll
       for (int c = 0; c < BN; ++c) {
         x[c] = (key0 + c < row.key_lim) ? __uint_as_float(raw[c]) : -INFINITY;
-        mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+        if constexpr (!kMax3) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
       }
     }
   } else if (row.mask) {
@@ -87,17 +97,29 @@ __device__ __forceinline__ bool softmax_tile(const PrefillParams& p, const Row& 
         v = fmaf(__uint_as_float(raw[c]), p.scale_log2, mv * kLog2e);
       }
       x[c] = v;
-      mx[c & 7] = fmaxf(mx[c & 7], v);
+      if constexpr (!kMax3) mx[c & 7] = fmaxf(mx[c & 7], v);
     }
   } else {
 #pragma unroll
     for (int c = 0; c < BN; ++c) {
       x[c] = (key0 + c < row.key_lim) ? __uint_as_float(raw[c]) * p.scale_log2 : -INFINITY;
-      mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+      if constexpr (!kMax3) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
     }
   }
-  float row_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                        fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+  float row_max;
+  if constexpr (kMax3) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mx[e] = fmax3(x[e], x[e + 8], -INFINITY);
+#pragma unroll
+    for (int c = 16; c < BN; c += 16) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx[e] = fmax3(mx[e], x[c + e], x[c + 8 + e]);
+    }
+    row_max = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+  } else {
+    row_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                    fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+  }
   if (fast) row_max *= p.scale_log2;
   const float m_new = fmaxf(m, row_max);
   const bool need = m_new > m + kRescaleLog2;

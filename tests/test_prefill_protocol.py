@@ -1,21 +1,24 @@
 """A discrete-event model of the prefill kernel's barrier protocol, checked on CPU.
 
 prefill_kernel (softmax_attention_gb300/csrc/prefill.cu) runs seven warps that only meet
-through mbarriers: a TMA producer, a landing watcher, one MMA-issuing thread and four softmax
-warps.  A mistake there hangs or races on the GPU, where it cannot be tried safely, so this
-module restates the protocol as agents over modelled barriers and runs it under random
-latencies.  For every run it checks that
+through mbarriers: a TMA producer, two MMA-issuing threads (one for S = Q K^T, one for
+O += P V) and four softmax warps, with three S/P buffers in tensor memory.  A mistake there
+hangs or races on the GPU, where it cannot be tried safely, so this module restates the
+protocol as agents over modelled barriers and runs it under random latencies.  For every run
+it checks that
 
 * every agent finishes (no deadlock);
 * every parity wait is unambiguous whenever it polls: the barrier has completed exactly the
   awaited phase's predecessors or one more, never two phases past nor one short (either would
   make the hardware's parity test answer wrongly);
 * no shared-memory stage or tensor-memory S/P buffer is read before its data is there, or
-  overwritten while a reader still needs it.
+  overwritten while a reader still needs it, and O is not rescaled under a running P V.
 
-The model follows the kernel's structure (one agent per role, the same barriers and phase
-arithmetic); the mutation tests at the end plant known protocol mistakes and check that the
-model reports them.
+Each issuing thread's MMAs run in order on a pipe of their own, and the two pipes run
+independently, so the model allows any interleaving of the two threads' MMAs (the hardware
+orders them at least that strictly).  The model follows the kernel's structure (one agent
+per role, the same barriers and phase arithmetic); the mutation tests at the end plant known
+protocol mistakes and check that the model reports them.
 """
 import random
 
@@ -23,33 +26,34 @@ import pytest
 
 from tests._protomodel import Hazard, Sim, TensorPipe, Bar
 
+NS = 3  # S/P buffers
 
-def run_protocol(n, stages, seed, *, paged_tail=False, mutate=None, fault=None):
+
+def run_protocol(n, stages, seed, *, paged_tail=False, q_tmem=False, mutate=None, fault=None):
     """Runs one CTA's KV loop of n tiles with `stages` K/V stages; raises Hazard on a fault.
 
-    fault = (agent, tile) stops that agent at that tile, as if one of its waits had run out
-    ("softmax1", "mma" or "watcher"); every wait is then bounded and the others take the
+    q_tmem: Q is copied into tensor memory by the softmax warps and the S issuer waits for
+    that copy.  fault = (agent, tile) stops that agent at that tile, as if one of its waits
+    had run out ("softmax1", "pv" or "s"); every wait is then bounded and the others take the
     kernel's error paths.  Returns the agents that recorded an error.
     """
     rng = random.Random(seed)
     sim = Sim(rng)
-    pipe = TensorPipe(sim)
+    pipe_s, pipe_pv = TensorPipe(sim), TensorPipe(sim)
     limit = 50.0 if fault else 1e9   # latencies below are at most a few units
-    watch_k = stages >= 3                                 # ready[j] also covers K_{j+2}
-    watcher_k = watch_k and mutate != "watcher_skips_k"
-    watcher_v = mutate != "watcher_skips_v"
     B = lambda name, c=1: Bar(name, c)
-    bar_q, bar_qt, bar_done = B("q"), B("q_in_tmem", 128), B("mma_done")
+    bar_q, bar_qt = B("q"), B("q_in_tmem", 128)
+    bar_done, bar_sdone = B("pv_issuer_done"), B("s_issuer_done")
     bar_k = [B(f"k_full{s}") for s in range(stages)]
     bar_v = [B(f"v_full{s}") for s in range(stages)]
     bar_ke = [B(f"k_empty{s}") for s in range(stages)]
     bar_ve = [B(f"v_empty{s}") for s in range(stages)]
-    bar_s = [B("s_full0"), B("s_full1")]
-    bar_r = [B(f"ready{s}", 128 + (0 if mutate == "ready_count_128" else 1)) for s in range(stages)]
-    bar_o = B("o_full")
+    bar_s = [B(f"s_full{b}") for b in range(NS)]
+    bar_p = [B(f"p_full{b}", 96 if mutate == "p_count_96" else 128) for b in range(NS)]
+    bar_pv = [B(f"pv_done{b}") for b in range(NS)]
 
     kstage, vstage = [None] * stages, [None] * stages   # (tile, landed)
-    sbuf = [[None] * 4 for _ in range(2)]               # per buffer, per warp quarter
+    sbuf = [[None] * 4 for _ in range(NS)]              # per buffer, per warp quarter
     s_done, pv_done = set(), set()
     errors = set()
     last_landing = [0.0]
@@ -116,127 +120,114 @@ def run_protocol(n, stages, seed, *, paged_tail=False, mutate=None, fault=None):
                 if not (yield wait(lambda bar=bar, phase=phase: bar.passed(phase))):
                     errors.add("drain ran out")
 
-    def watcher():
-        if watcher_k and mutate != "watcher_skips_k01":
-            # K_0 and K_1 share barriers with K_S and K_{S+1}, which the watcher waits for
-            if not (yield wait(lambda: bar_k[0].passed(0))):
-                errors.add("watcher")
-                return
-            if n > 1 and not (yield wait(lambda: bar_k[1].passed(0))):
-                errors.add("watcher")
-                return
-        for j in range(n):
-            s = j % stages
-            if stops("watcher", j):
-                errors.add("watcher")
-                return
-            if watcher_v and not (yield wait(lambda s=s, j=j: bar_v[s].passed(j // stages))):
-                errors.add("watcher")
-                return
-            if watcher_k and j + 2 < n:
-                s2 = (j + 2) % stages
-                if not (yield wait(lambda s2=s2, j=j: bar_k[s2].passed((j + 2) // stages))):
-                    errors.add("watcher")
-                    return
-            bar_r[s].arrive()
-
-    def issue_s(j):
-        b, s = j & 1, j % stages
-
-        def start():
-            check(kstage[s] == (j, True), f"S_{j} reads K stage {s} holding {kstage[s]}")
-            if j >= 2:
-                check(j - 2 in pv_done, f"S_{j} overwrites P_{j - 2} before P V read it")
-
-        def end():
-            s_done.add(j)
-            for w in range(4):
-                sbuf[b][w] = ("S", j)
-        pipe.mma(lat(0.2, 0.6), start, end)
-        pipe.commit(bar_s[b])
-        pipe.commit(bar_ke[s])
-
-    def issue_pv(j):
-        b, s = j & 1, j % stages
-
-        def start():
-            check(all(q == ("P", j) for q in sbuf[b]), f"P_{j} V_{j} reads {sbuf[b]}")
-            check(vstage[s] == (j, True), f"P_{j} V_{j} reads V stage {s} holding {vstage[s]}")
-
-        pipe.mma(lat(0.2, 0.6), start, lambda: pv_done.add(j))
-        pipe.commit(bar_o)
-        pipe.commit(bar_ve[s])
-
-    def mma():
-        ok = yield wait(lambda: bar_qt.passed(0))
-        ok = ok and (yield wait(lambda: bar_k[0].passed(0)))
-        if ok:
-            issue_s(0)
-        if ok and n > 1:
-            ok = yield wait(lambda: bar_k[1].passed(0))
-            if ok:
-                issue_s(1)
+    def s_issuer():
+        q_bar = bar_qt if q_tmem else bar_q
+        ok = yield wait(lambda: q_bar.passed(0))
         for j in range(n):
             if not ok:
                 break
-            s = j % stages
-            if stops("mma", j):
+            b, s = j % NS, j % stages
+            if stops("s", j):
                 ok = False
                 break
-            if mutate == "s_before_pv" and j + 2 < n:
-                if not watch_k:
-                    yield ("wait", lambda j=j: bar_k[(j + 2) % stages].passed((j + 2) // stages))
-                yield ("wait", lambda s=s, j=j: bar_r[s].passed(j // stages))
-                issue_s(j + 2)
-                issue_pv(j)
-                continue
-            if not (ok := (yield wait(lambda s=s, j=j: bar_r[s].passed(j // stages)))):
-                break
-            issue_pv(j)
-            if j + 2 < n:
-                if not watch_k:
-                    s2 = (j + 2) % stages
-                    if not (ok := (yield wait(lambda s2=s2, j=j: bar_k[s2].passed((j + 2) // stages)))):
-                        break
-                issue_s(j + 2)
+            if mutate != "s_skips_k":
+                if not (ok := (yield wait(lambda s=s, j=j: bar_k[s].passed(j // stages)))):
+                    break
+            if j >= NS and mutate != "s_skips_buffer_wait":
+                if not (ok := (yield wait(lambda b=b, j=j: bar_pv[b].passed((j - NS) // NS)))):
+                    break
+
+            def start(j=j, b=b, s=s):
+                check(kstage[s] == (j, True), f"S_{j} reads K stage {s} holding {kstage[s]}")
+                if j >= NS:
+                    check(j - NS in pv_done, f"S_{j} overwrites P_{j - NS} before P V read it")
+
+            def end(j=j, b=b):
+                s_done.add(j)
+                for w in range(4):
+                    sbuf[b][w] = ("S", j)
+            pipe_s.mma(lat(0.2, 0.6), start, end)
+            pipe_s.commit(bar_s[b])
+            pipe_s.commit(bar_ke[s])
         if not ok:
-            errors.add("mma")
-        # every MMA issued must finish before tensor memory is released
-        pipe.commit(bar_done)
+            errors.add("s")
+        pipe_s.commit(bar_sdone)
+        yield wait(lambda: bar_sdone.passed(0))
+
+    def pv_issuer():
+        ok = True
+        for j in range(n):
+            b, s = j % NS, j % stages
+            if stops("pv", j):
+                ok = False
+                break
+            if mutate != "pv_skips_p":
+                if not (ok := (yield wait(lambda b=b, j=j: bar_p[b].passed(j // NS)))):
+                    break
+            if mutate != "pv_skips_v":
+                if not (ok := (yield wait(lambda s=s, j=j: bar_v[s].passed(j // stages)))):
+                    break
+
+            def start(j=j, b=b, s=s):
+                check(all(q == ("P", j) for q in sbuf[b]), f"P_{j} V_{j} reads {sbuf[b]}")
+                check(vstage[s] == (j, True), f"P_{j} V_{j} reads V stage {s} holding {vstage[s]}")
+                o_busy[0] = True
+
+            def end(j=j):
+                o_busy[0] = False
+                pv_done.add(j)
+            pipe_pv.mma(lat(0.2, 0.6), start, end)
+            pipe_pv.commit(bar_pv[b])
+            pipe_pv.commit(bar_ve[s])
+        if not ok:
+            errors.add("pv")
+        # every MMA this thread issued must finish before tensor memory is released
+        pipe_pv.commit(bar_done)
         yield wait(lambda: bar_done.passed(0))
 
+    o_busy = [False]
+
     def softmax(w):
-        ok = yield wait(lambda: bar_q.passed(0))
-        if ok:
-            yield ("delay", lat(0.05, 0.2))
-            for _ in range(32):
-                bar_qt.arrive()
+        ok = True
+        if q_tmem:
+            ok = yield wait(lambda: bar_q.passed(0))
+            if ok:
+                yield ("delay", lat(0.05, 0.2))
+                for _ in range(32):
+                    bar_qt.arrive()
         for j in range(n):
             if not ok:
                 break
-            b, s = j & 1, j % stages
+            b, s = j % NS, j % stages
             if stops(f"softmax{w}", j):
                 ok = False
                 break
-            if not (ok := (yield wait(lambda b=b, j=j: bar_s[b].passed(j >> 1)))):
+            if not (ok := (yield wait(lambda b=b, j=j: bar_s[b].passed(j // NS)))):
                 break
             check(sbuf[b][w] == ("S", j), f"softmax {w} reads S_{j} from {sbuf[b][w]}")
             yield ("delay", lat(0.3, 1.0))
-            # The kernel waits every tile.  Skipping the wait on tiles with no rescale is unsafe
-            # with a single barrier: the epilogue's wait for the last P V could then pass on
-            # the phase before it (the skip_o_waits mutation).
-            if j > 0 and not (mutate == "skip_o_waits" and rng.random() < 0.8):
-                if not (ok := (yield wait(lambda j=j: bar_o.passed(j - 1)))):
-                    break
-                check(j - 1 in pv_done, f"softmax {w} rescales O before P_{j - 1} V_{j - 1}")
+            # A warp rescales O (some of its rows' max moved) only after waiting for
+            # P_{j-1} V_{j-1}; other tiles do not wait (the rescale_without_wait mutation
+            # skips the wait on rescale tiles too).
+            rescale = rng.random() < 0.3
+            if j > 0 and rescale:
+                if mutate != "rescale_without_wait":
+                    if not (ok := (yield wait(lambda j=j: bar_pv[(j - 1) % NS].passed((j - 1) // NS)))):
+                        break
+                check(j - 1 in pv_done and not o_busy[0],
+                      f"softmax {w} rescales O before P_{j - 1} V_{j - 1} finished")
             sbuf[b][w] = ("P", j)
             if paged_tail and j == n - 1:
+                # the V wait is exact once P_{j-1} V_{j-1} (hence V_{j-stages}) is done
+                if j > 0 and not rescale and mutate != "tail_skips_pv_wait":
+                    if not (ok := (yield wait(lambda j=j: bar_pv[(j - 1) % NS].passed((j - 1) // NS)))):
+                        break
                 if not (ok := (yield wait(lambda s=s, j=j: bar_v[s].passed(j // stages)))):
                     break
             for _ in range(32):
-                bar_r[s].arrive()
+                bar_p[b].arrive()
         if ok and n > 0:
-            ok = yield wait(lambda: bar_o.passed(n - 1))
+            ok = yield wait(lambda: bar_pv[(n - 1) % NS].passed((n - 1) // NS))
             if ok:
                 check(n - 1 in pv_done, "epilogue reads O before the last P V")
         if not ok:
@@ -244,17 +235,18 @@ def run_protocol(n, stages, seed, *, paged_tail=False, mutate=None, fault=None):
 
     if n > 0:
         sim.start("producer", producer())
-        sim.start("watcher", watcher())
-        sim.start("mma", mma())
+        sim.start("s", s_issuer())
+        sim.start("pv", pv_issuer())
         for w in range(4):
             sim.start(f"softmax{w}", softmax(w))
     sim.run()
-    expected = {"producer", "watcher", "mma"} | {f"softmax{w}" for w in range(4)} if n else set()
+    expected = {"producer", "s", "pv"} | {f"softmax{w}" for w in range(4)} if n else set()
     check(sim.finished == expected, f"unfinished: {expected - sim.finished}")
     if n:
         exit_time = max(sim.finish_time.values())
         check(last_landing[0] <= exit_time, "a copy lands after every warp has finished")
-        check(pipe.free_at <= exit_time, "an MMA runs after every warp has finished")
+        check(max(pipe_s.free_at, pipe_pv.free_at) <= exit_time,
+              "an MMA runs after every warp has finished")
     return errors
 
 
@@ -262,52 +254,56 @@ def run_protocol(n, stages, seed, *, paged_tail=False, mutate=None, fault=None):
 @pytest.mark.parametrize("n", [0, 1, 2, 3, 4, 5, 7, 10])
 def test_protocol_is_safe(stages, n):
     for seed in range(40):
-        run_protocol(n, stages, seed)
+        run_protocol(n, stages, seed, q_tmem=(seed % 2 == 1))
         run_protocol(n, stages, seed + 1000, paged_tail=True)
 
 
-def _fails(n, stages, mutate):
+def _fails(n, stages, mutate, **kw):
     for seed in range(200):
         try:
-            run_protocol(n, stages, seed, mutate=mutate)
+            run_protocol(n, stages, seed, mutate=mutate, **kw)
         except Hazard:
             return True
     return False
 
 
-def test_model_catches_missing_k_landing_wait():
-    # ready[j] must cover K_{j+2} when the issuer does not wait for it itself
-    assert _fails(8, 3, "watcher_skips_k")
+def test_model_catches_s_over_an_unread_p():
+    # S_j goes into P_{j-3}'s buffer; without waiting for P_{j-3} V_{j-3} it can overwrite it
+    assert _fails(8, 3, "s_skips_buffer_wait")
 
 
-def test_model_catches_s_issued_over_unread_p():
-    # S_{j+2} shares P_j's buffer, so it has to follow P_j V_j in the tensor pipe
-    assert _fails(8, 3, "s_before_pv")
+def test_model_catches_s_before_its_k_lands():
+    assert _fails(8, 3, "s_skips_k")
 
 
-def test_model_catches_watcher_not_observing_k0_k1():
-    # without it, the wait for K_S can pass on K_0's phase when loads complete out of order
-    assert _fails(8, 3, "watcher_skips_k01")
+def test_model_catches_pv_before_p():
+    assert _fails(8, 3, "pv_skips_p")
 
 
-def test_model_catches_watcher_not_waiting_for_v():
-    assert _fails(8, 3, "watcher_skips_v")
+def test_model_catches_pv_before_its_v_lands():
+    assert _fails(8, 3, "pv_skips_v")
 
 
-def test_model_catches_ready_count_without_the_watcher():
-    # 128 + 1 arrivals per phase; with a count of 128 a phase can close before every P row
-    assert _fails(8, 3, "ready_count_128")
+def test_model_catches_p_count_short_of_the_rows():
+    # 128 arrivals (4 warps x 32 rows) per phase; with fewer a phase closes before every row
+    assert _fails(8, 3, "p_count_96")
 
 
-def test_model_catches_skipped_o_waits_on_one_barrier():
-    assert _fails(9, 3, "skip_o_waits")
+def test_model_catches_a_paged_tail_v_wait_without_the_pv_wait():
+    # without P_{j-1} V_{j-1} done, V_{j-stages} may not have landed and the parity wait for
+    # V_j can pass on its phase
+    assert _fails(5, 2, "tail_skips_pv_wait", paged_tail=True)
 
 
-@pytest.mark.parametrize("agent", ["softmax1", "mma", "watcher"])
+def test_model_catches_a_rescale_without_the_o_wait():
+    assert _fails(9, 3, "rescale_without_wait")
+
+
+@pytest.mark.parametrize("agent", ["softmax1", "pv", "s"])
 @pytest.mark.parametrize("stages", [2, 3])
 def test_error_paths_end_with_nothing_in_flight(agent, stages):
     # a warp stopping mid-loop (as after a wait that ran out): every other wait is bounded,
-    # the producer lets its copies in flight land and the issuer's MMAs finish before exit
+    # the producer lets its copies in flight land and the issuers' MMAs finish before exit
     for seed in range(30):
         n = 7
         errors = run_protocol(n, stages, seed, fault=(agent, seed % n))
@@ -319,7 +315,7 @@ def test_model_catches_drain_waiting_for_a_reused_k_stage():
     # the drain's wait for the K whose stage the last K reused reads a barrier two phases on
     def fails():
         for seed in range(200):
-            for agent in ("softmax1", "mma", "watcher"):
+            for agent in ("softmax1", "pv", "s"):
                 try:
                     run_protocol(7, 3, seed, mutate="drain_waits_stale_k", fault=(agent, seed % 7))
                 except Hazard:
