@@ -372,8 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       float alpha;
       uint32_t pk[BN / 2];
       // the exponentials overlap the previous tile's P V on the tensor cores
-      const bool need = prefill::softmax_tile<BN, BF16>(p, row, (t_begin + jj) * BN, raw, m_run,
-                                                        l_run, alpha, pk);
+      // three-input max: faster for 64-key tiles and the paged instantiations, slower for
+      // the dense 128-key one (measured)
+      const bool need = prefill::softmax_tile<BN, BF16, (BN <= 64 || PAGED)>(
+          p, row, (t_begin + jj) * BN, raw, m_run, l_run, alpha, pk);
       // O is rescaled only once every earlier P V product is in it (the P V issuer runs its
       // products in order, so P_{j-1} V_{j-1} finishing means all have).  A tile with no
       // rescale does not wait: P_j V_j is issued after P_j anyway, and this warp cannot get

@@ -55,7 +55,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // pairs, even key in the low half) to pk, and returns whether O must be rescaled by alpha.
 // Lazy rescale: m moves only when the tile's max exceeds it by more than 2^8, so P may be
 // computed against a stale max; the final division by l makes that exact.
-template <int BN, bool BF16>
+template <int BN, bool BF16, bool kMax3>
 __device__ __forceinline__ bool softmax_tile(const PrefillParams& p, const Row& row, int key0,
                                              const uint32_t (&raw)[BN], float& m, float& l,
                                              float& alpha, uint32_t (&pk)[BN / 2]) {
@@ -64,9 +64,9 @@ __device__ __forceinline__ bool softmax_tile(const PrefillParams& p, const Row& 
   // Masked keys hold -inf either way.  Eight independent max accumulators keep the
   // reduction's dependency chain short.
   const bool fast = !row.mask && p.scale_log2 > 0.f;
-  // 64-key tiles reduce the max after x is built, with three-input max instructions (measured
-  // faster there); 128-key tiles fold a two-input max into the loops that build x.
-  constexpr bool kMax3 = BN <= 64;
+  // kMax3: reduce the max after x is built, with three-input max instructions; otherwise a
+  // two-input max is folded into the loops that build x.  Which is faster depends on the
+  // instantiation (measured; the caller chooses).
   float x[BN];
   float mx[8];
 #pragma unroll
