@@ -8,7 +8,7 @@
 // overlapping the next tile's Q K^T (the FA3 software pipeline described in flashinfer PR
 // "perf: FlashAttention-3 style MLA PageAttention", change list items 1-3), rebuilt for
 // Blackwell: TMA loads into a multi-stage shared-memory ring, tcgen05.mma accumulating in
-// tensor memory, S/P double-buffered in tensor memory with P (16-bit) written over S, and O
+// tensor memory, three S/P buffers in tensor memory with P (16-bit) written over S, and O
 // resident in tensor memory for the whole KV loop.  The paged instantiation reads K/V
 // through a page table (chunked prefill against a paged cache): each page of a KV tile is
 // one 5-D TMA box, and each sequence has its own length.
