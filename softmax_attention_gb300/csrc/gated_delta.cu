@@ -15,10 +15,13 @@
 // Two kernels:
 //   1. chunk preparation (every chunk of every head in parallel): the Gram products Q K^T
 //      and K K^T in one tensor-core MMA (the chunk's Q and K rows stacked as a 128-row A
-//      operand against its K rows), the triangular solve for W and U~ on the CUDA cores in
-//      fp32 (each thread one right-hand-side column, held in registers), P, and the per-token
-//      decay factors Gamma_i and Gamma_C / Gamma_i; written to a workspace (W and P in bf16
-//      as tensor-core operands, U~ and the factors in fp32);
+//      operand against its K rows), T = (I + A)^-1 on the CUDA cores in fp32 (blocked: the
+//      four 16x16 diagonal blocks by substitution, then the off-diagonal blocks one block
+//      diagonal at a time), then W = T diag(beta Gamma) K and U~ = T diag(beta) V on the
+//      tensor cores (T's scaled columns split into bf16 high and low parts, so the products
+//      keep ~16 bits; K and V exact in bf16), P, and the per-token decay factors Gamma_i and
+//      Gamma_C / Gamma_i; written to a workspace (W and P in bf16 as tensor-core operands,
+//      U~ and the factors in fp32);
 //   2. the recurrence across chunks (one CTA per (batch, value head), tensor cores): the state
 //      lives in tensor memory in fp32 (dv lanes x dk columns), with a bf16 copy in shared
 //      memory as the A operand; per chunk  U^T = U~^T - S W^T,  O^T = S Q^T (scaled per token)
@@ -61,25 +64,24 @@ struct GdnParams {
 // ------------------------------------------------------------------------------------------
 // Kernel 1: chunk preparation.  One CTA per (chunk, value head, batch), 256 threads.  Thread
 // 0 loads the chunk's Q, K and V rows with TMA (128-byte swizzled, rows past the sequence
-// read as zero) and issues the Gram MMA; warps 0-3 read its rows back; all threads solve.
+// read as zero) and issues the MMAs; warps 0-3 read the Gram rows back; all threads form T.
 // ------------------------------------------------------------------------------------------
 constexpr int kPrepThreads = 256;
-constexpr int kTriF = kC + 4;                  // padded fp32 row of A (float4-aligned)
+constexpr int kTriF = kC + 4;                  // padded fp32 row of A and T (float4-aligned)
 constexpr int kPQK = 0;                        // [Q rows; K rows]: 2 column blocks of 128 x 128 B
 constexpr int kPV = kPQK + 2 * 128 * 128;      // V rows: 2 column blocks of 64 x 128 B
 constexpr int kPA = kPV + 2 * kC * 128;        // A, fp32 [C][kTriF]
-constexpr int kPSmall = kPA + kC * kTriF * 4;  // gamma, beta, raw g: 3 x C fp32
-constexpr int kPBar = kPSmall + 3 * kC * 4;    // two mbarriers + the tensor-memory slot
+constexpr int kPT = kPA + kC * kTriF * 4;      // T = (I + A)^-1, fp32 [C][kTriF]
+constexpr int kPM = kPT + kC * kTriF * 4;      // off-diagonal block sums, 3 x 16 x 16 fp32
+constexpr int kPSmall = kPM + 3 * 256 * 4;     // gamma, beta, raw g, Gamma: 4 x C fp32
+constexpr int kPBar = kPSmall + 4 * kC * 4;    // three mbarriers + the tensor-memory slot
 constexpr int kPrepSmem = kPBar + 32 + 1024;
-
-// Element (row r, column col) of a K-major 128-byte-swizzled bf16 tile made of 64-column
-// blocks of `rows` rows each (the layout TMA writes and the MMA reads).
-__device__ __forceinline__ float swz_at(const uint8_t* tile, int rows, int r, int col) {
-  const int cb = col >> 6, ch = (col >> 3) & 7;
-  const uint16_t bits = *reinterpret_cast<const uint16_t*>(
-      tile + cb * rows * 128 + r * 128 + ((ch ^ (r & 7)) * 16) + (col & 7) * 2);
-  return __uint_as_float(static_cast<uint32_t>(bits) << 16);
-}
+// The MMA operands T diag(beta Gamma) and T diag(beta) (64 x 64 bf16, K-major, 128-byte
+// swizzled, high and low parts) reuse dead space once T is formed: the Q rows of the [Q; K]
+// tile (read only by the Gram MMA) and the A matrix.
+constexpr int kOpWHi = kPQK, kOpWLo = kPQK + 128 * 128, kOpUHi = kPA, kOpULo = kPA + kC * 128;
+static_assert(kPA % 1024 == 0 && kC * kTriF * 4 >= 2 * kC * 128, "operand tiles over A");
+static_assert(2 * kPrepSmem <= 232448, "two CTAs per SM");
 
 __global__ void __launch_bounds__(kPrepThreads, 2)
     gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -89,14 +91,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t s_base = smem_addr(smem);
   float* As = reinterpret_cast<float*>(smem + kPA);
+  float* Ts = reinterpret_cast<float*>(smem + kPT);
+  float* Ms = reinterpret_cast<float*>(smem + kPM);
   float* gam = reinterpret_cast<float*>(smem + kPSmall);
   float* bet = gam + kC;
-  float* graw = bet + kC;
+  float* graw = bet + kC;  // raw g, then gamma_i in log2 units (after the scan)
+  float* Gam = graw + kC;  // Gamma_i = e^gamma_i
   const uint32_t bar_ld = s_base + kPBar, bar_mma = s_base + kPBar + 8;
+  const uint32_t bar_mma2 = s_base + kPBar + 24;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPBar + 16);
 
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
-  const int warp = tid / 32;
+  const int warp = tid / 32, lane = tid % 32;
   const int hk = h / (p.Hv / p.Hk);
   const int t0 = c * kC, n = min(kC, p.T - t0);
   const size_t bh = static_cast<size_t>(b) * p.Hv + h;
@@ -104,10 +110,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   if (tid == 0) {
     mbar_init(bar_ld, 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_mma2, 1);
     fence_barrier_init();
   }
   if (warp == 0) {
-    tmem_alloc(smem_addr(tmem_slot), 64);
+    // Gram result (M = 128, 64 columns), later W and U~ (M = 64, 2 x 128 columns)
+    tmem_alloc(smem_addr(tmem_slot), 256);
     tmem_relinquish();
   }
   if (tid < kC) {
@@ -153,6 +161,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     const float excl = sc - (a + a2);
     gam[2 * l] = excl + a;
     gam[2 * l + 1] = excl + a + a2;
+    constexpr float kLog2e = 1.44269504088896340736f;
+    graw[2 * l] = (excl + a) * kLog2e;
+    graw[2 * l + 1] = (excl + a + a2) * kLog2e;
   }
   __syncthreads();
   bool ok = __syncthreads_and(mbar_wait(bar_mma, 0, p.status));
@@ -164,13 +175,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 32,
               *reinterpret_cast<uint32_t(*)[32]>(&raw[32]));
     tmem_ld_wait();
+    // Gamma_i / Gamma_j = 2^(gl_i - gl_j) <= 1 for j <= i (gl = gamma in log2 units)
+    const float* gl = graw;
     if (tid < kC) {
       const int i = tid;
+      const float gi = gl[i];
       uint32_t pk[kC / 2];
 #pragma unroll
       for (int j = 0; j < kC; j += 2) {
-        const float p0 = (j <= i && i < n) ? p.scale * expf(gam[i] - gam[j]) * __uint_as_float(raw[j]) : 0.f;
-        const float p1 = (j + 1 <= i && i < n) ? p.scale * expf(gam[i] - gam[j + 1]) * __uint_as_float(raw[j + 1]) : 0.f;
+        const float p0 = (j <= i && i < n) ? p.scale * exp2_approx(gi - gl[j]) * __uint_as_float(raw[j]) : 0.f;
+        const float p1 = (j + 1 <= i && i < n) ? p.scale * exp2_approx(gi - gl[j + 1]) * __uint_as_float(raw[j + 1]) : 0.f;
         pk[j / 2] = pack_bf16x2(p0, p1);
       }
       uint4* dst = reinterpret_cast<uint4*>(p.p_ws + (bh * p.Tpad + t0 + i) * kC);
@@ -178,13 +192,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       for (int e = 0; e < kC / 8; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
     } else {
       const int i = tid - kC;
+      const float gi = gl[i], bi = bet[i];
 #pragma unroll
       for (int j = 0; j < kC; j += 4) {
         float4 a;
-        a.x = j < i ? bet[i] * expf(gam[i] - gam[j]) * __uint_as_float(raw[j]) : 0.f;
-        a.y = j + 1 < i ? bet[i] * expf(gam[i] - gam[j + 1]) * __uint_as_float(raw[j + 1]) : 0.f;
-        a.z = j + 2 < i ? bet[i] * expf(gam[i] - gam[j + 2]) * __uint_as_float(raw[j + 2]) : 0.f;
-        a.w = j + 3 < i ? bet[i] * expf(gam[i] - gam[j + 3]) * __uint_as_float(raw[j + 3]) : 0.f;
+        a.x = j < i ? bi * exp2_approx(gi - gl[j]) * __uint_as_float(raw[j]) : 0.f;
+        a.y = j + 1 < i ? bi * exp2_approx(gi - gl[j + 1]) * __uint_as_float(raw[j + 1]) : 0.f;
+        a.z = j + 2 < i ? bi * exp2_approx(gi - gl[j + 2]) * __uint_as_float(raw[j + 2]) : 0.f;
+        a.w = j + 3 < i ? bi * exp2_approx(gi - gl[j + 3]) * __uint_as_float(raw[j + 3]) : 0.f;
         *reinterpret_cast<float4*>(As + i * kTriF + j) = a;
       }
     }
@@ -193,49 +208,159 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     const int e = tid - 128;
     const float v = e < kC ? expf(gam[e]) : expf(gam[kC - 1] - gam[e - kC]);
     p.f_ws[(bh * p.n_chunks + c) * (2 * kC) + e] = v;
+    if (e < kC) Gam[e] = v;
+  }
+  if (!ok) {
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      tc_fence_after();
+      tmem_dealloc(tmem, 256);
+    }
+    return;
+  }
+  // T = (I + A)^-1 (A strictly lower triangular, 16 x 16 blocks A_ik): T_ii = (I + A_ii)^-1
+  // by substitution, then for i > j, one block diagonal at a time,
+  //   T_ij = -T_ii M_ij,   M_ij = sum_{k=j}^{i-1} A_ik T_kj.
+  for (int e = tid; e < kC * kC; e += kPrepThreads) Ts[(e / kC) * kTriF + e % kC] = 0.f;
+  __syncthreads();
+  if (tid < kC) {
+    const int blk = tid / 16, cj = tid % 16, o = 16 * blk;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float acc = r == cj ? 1.f : 0.f;
+#pragma unroll
+      for (int q = 0; q < r; ++q) acc -= As[(o + r) * kTriF + o + q] * x[q];
+      x[r] = acc;
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) Ts[(o + r) * kTriF + o + cj] = x[r];
+  }
+  __syncthreads();
+  // (the loops have constant trip counts so they unroll, with four partial sums each)
+#pragma unroll
+  for (int d = 1; d < 4; ++d) {
+    // M for the 4 - d blocks (i = j + d): one entry (r, cc) of one block per thread and pass
+#pragma unroll
+    for (int pass = 0; pass < 4 - d; ++pass) {
+      const int e = tid + pass * kPrepThreads;
+      const int jb = e / 256, r = (e / 16) % 16, cc = e % 16, ib = jb + d;
+      const float* arow = As + (16 * ib + r) * kTriF + 16 * jb;
+      const float* tcol = Ts + 16 * jb * kTriF + 16 * jb + cc;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < 16 * d; ++k) acc[k & 3] += arow[k] * tcol[k * kTriF];
+      Ms[e] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    }
+    __syncthreads();
+    // T_ij = -T_ii M_ij (T_ii is zero above its diagonal, so every row sums all 16 terms)
+#pragma unroll
+    for (int pass = 0; pass < 4 - d; ++pass) {
+      const int e = tid + pass * kPrepThreads;
+      const int jb = e / 256, r = (e / 16) % 16, cc = e % 16, ib = jb + d;
+      const float* trow = Ts + (16 * ib + r) * kTriF + 16 * ib;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < 16; ++q) acc[q & 3] += trow[q] * Ms[jb * 256 + q * 16 + cc];
+      Ts[(16 * ib + r) * kTriF + 16 * jb + cc] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
+    }
+    __syncthreads();
+  }
+
+  // The MMA operands: T diag(beta Gamma) for W and T diag(beta) for U~, each as a bf16 high
+  // part and the bf16 rounding of the remainder, written K-major in the 128-byte swizzle
+  // (row i, 16-byte chunk ch at chunk ch ^ (i & 7)).  A is no longer read.
+  {
+    const int i = tid / 4, g = tid % 4;
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int ch = 2 * g + h2;
+      uint32_t whi[4], wlo[4], uhi[4], ulo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j0 = 8 * ch + 2 * e;
+        float w2[2], u2[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const float tv = Ts[i * kTriF + j0 + t];
+          u2[t] = tv * bet[j0 + t];
+          w2[t] = u2[t] * Gam[j0 + t];
+        }
+        whi[e] = pack_bf16x2(w2[0], w2[1]);
+        uhi[e] = pack_bf16x2(u2[0], u2[1]);
+        const float wh0 = __uint_as_float(whi[e] << 16), wh1 = __uint_as_float(whi[e] & 0xFFFF0000u);
+        const float uh0 = __uint_as_float(uhi[e] << 16), uh1 = __uint_as_float(uhi[e] & 0xFFFF0000u);
+        wlo[e] = pack_bf16x2(w2[0] - wh0, w2[1] - wh1);
+        ulo[e] = pack_bf16x2(u2[0] - uh0, u2[1] - uh1);
+      }
+      const int off = i * 128 + ((ch ^ (i & 7)) * 16);
+      *reinterpret_cast<uint4*>(smem + kOpWHi + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
+      *reinterpret_cast<uint4*>(smem + kOpWLo + off) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+      *reinterpret_cast<uint4*>(smem + kOpUHi + off) = make_uint4(uhi[0], uhi[1], uhi[2], uhi[3]);
+      *reinterpret_cast<uint4*>(smem + kOpULo + off) = make_uint4(ulo[0], ulo[1], ulo[2], ulo[3]);
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    tc_fence_after();
+    // W (columns 0-127) and U~ (columns 128-255): M = 64 chunk rows, N = 128, K = 64 tokens;
+    // A = the operand tiles (K-major), B = the chunk's K or V rows read MN-major.
+    constexpr uint32_t idesc = idesc_f16(true, kC, 128, false, true);
+    const uint32_t kb = s_base + kPQK + kC * 128, vb = s_base + kPV;
+#pragma unroll
+    for (int part = 0; part < 4; ++part) {
+      const uint32_t a_tile = s_base + (part == 0 ? kOpWHi : part == 1 ? kOpWLo : part == 2 ? kOpUHi : kOpULo);
+      const uint32_t d = tmem + (part < 2 ? 0u : 128u);
+#pragma unroll
+      for (int kk = 0; kk < kC / 16; ++kk) {
+        const uint64_t ad = sdesc_sw128(a_tile + kk * 32, 16, 1024);
+        const uint64_t bd = part < 2 ? sdesc_sw128(kb + kk * 2048, 128 * 128, 1024)
+                                     : sdesc_sw128(vb + kk * 2048, kC * 128, 1024);
+        mma_ss(d, ad, bd, idesc, ((part & 1) || kk > 0) ? 1u : 0u);
+      }
+    }
+    tc_commit(bar_mma2);
+  }
+  ok = __syncthreads_and(mbar_wait(bar_mma2, 0, p.status));
+  if (ok) {
+    // M = 64 result: row 16 q + l (l < 16) sits in lane 32 q + l; warps q and q + 4 share the
+    // sub-partition's lanes, the first writing W (columns 0-127), the second U~ (128-255)
+    tc_fence_after();
+    const int quad = warp % 4, half = warp / 4;
+    const int i = 16 * quad + lane % 16;
+    const size_t row = bh * p.Tpad + t0 + i;
+#pragma unroll 1
+    for (int cb = 4 * half; cb < 4 * half + 4; ++cb) {
+      uint32_t r32[32];
+      tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + cb * 32, r32);
+      tmem_ld_wait();
+      if (lane < 16) {
+        if (cb < 4) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(r32[2 * e]), __uint_as_float(r32[2 * e + 1]));
+          uint4* dst = reinterpret_cast<uint4*>(p.w_ws + row * kDk + cb * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(p.u_ws + row * kDv + (cb - 4) * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(r32[4 * e]), __uint_as_float(r32[4 * e + 1]),
+                                 __uint_as_float(r32[4 * e + 2]), __uint_as_float(r32[4 * e + 3]));
+        }
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 64);
-  }
-  if (!ok) return;
-
-  // Triangular solve (I + A) X = R by forward substitution, one right-hand-side column per
-  // thread, the column in registers: columns 0..127 give W (R = beta Gamma K), columns
-  // 128..255 give U~ (R = beta V).  A's rows are read as broadcast float4s; entries at and
-  // above the diagonal are zero, so every row runs over whole groups of four.
-  {
-    const bool wcol = tid < kDk;
-    const int col = wcol ? tid : tid - kDk;
-    float x[kC];
-#pragma unroll
-    for (int i = 0; i < kC; ++i) x[i] = 0.f;
-#pragma unroll
-    for (int i = 0; i < kC; ++i) {
-      float acc = wcol ? bet[i] * expf(gam[i]) * swz_at(smem + kPQK, 128, kC + i, col)
-                       : bet[i] * swz_at(smem + kPV, kC, i, col);
-#pragma unroll
-      for (int m4 = 0; m4 < (i + 3) / 4; ++m4) {
-        const float4 a = *reinterpret_cast<const float4*>(As + i * kTriF + 4 * m4);
-        acc -= a.x * x[4 * m4] + a.y * x[4 * m4 + 1] + a.z * x[4 * m4 + 2] + a.w * x[4 * m4 + 3];
-      }
-      x[i] = acc;
-    }
-    const size_t row0 = bh * p.Tpad + t0;
-    if (wcol) {
-      uint16_t* wdst = p.w_ws + row0 * kDk + col;
-#pragma unroll
-      for (int i = 0; i < kC; ++i) {
-        const __nv_bfloat16 hv = __float2bfloat16_rn(x[i]);
-        wdst[static_cast<size_t>(i) * kDk] = *reinterpret_cast<const uint16_t*>(&hv);
-      }
-    } else {
-      float* udst = p.u_ws + row0 * kDv + col;
-#pragma unroll
-      for (int i = 0; i < kC; ++i) udst[static_cast<size_t>(i) * kDv] = x[i];
-    }
+    tmem_dealloc(tmem, 256);
   }
 }
 
@@ -261,11 +386,13 @@ constexpr int kSBlk = kDv * 128;                 // 16384: one 64-column block o
 constexpr int kUtOff = kSbfOff + 2 * kSBlk;      // U^T, [128 rows][128 B]
 constexpr int kUptOff = kUtOff + kSBlk;          // U^T with each token's decay to the chunk end
 constexpr int kBarOff = kUptOff + kSBlk;
-// full[2], empty[2], s_ready, u_ready, u_done, o_done, mma_done
-constexpr int kNumBars = 9;
+// full[2], empty[2], s_ready, u_ready, u_done, o_done, mma_done, s_done
+constexpr int kNumBars = 10;
 constexpr int kStateSmem = kBarOff + kNumBars * 8 + 16 + 1024;
 static_assert(kStateSmem <= 232448, "shared memory budget");
-constexpr uint32_t kTmS = 0, kTmU = 128, kTmO1 = 192, kTmO2 = 256;
+// tensor memory: the state (128 columns), D_U (64), and two sets of output accumulators D_O1,
+// D_O2 (64 each), used by alternate chunks
+constexpr uint32_t kTmS = 0, kTmU = 128, kTmO1 = 192, kTmO2 = 256, kTmOSet = 128;
 constexpr uint32_t kStateArrivals = kStateWarps * 32;
 
 __global__ void __launch_bounds__(kStateThreads, 1)
@@ -281,6 +408,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   auto bar_empty = [&](int s) { return bars + 8u * (2 + s); };
   const uint32_t bar_sready = bars + 8u * 4, bar_uready = bars + 8u * 5;
   const uint32_t bar_udone = bars + 8u * 6, bar_odone = bars + 8u * 7, bar_done = bars + 8u * 8;
+  const uint32_t bar_sdone = bars + 8u * 9;  // the state update of the chunk has finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + kNumBars * 8);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -301,6 +429,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     mbar_init(bar_udone, 1);
     mbar_init(bar_odone, 1);
     mbar_init(bar_done, 1);
+    mbar_init(bar_sdone, 1);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -361,26 +490,29 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                  idesc_n64, kk > 0 ? 1u : 0u);
         }
         tc_commit(bar_udone);
-        // S Q^T -> D_O1
+        // S Q^T -> D_O1 of this chunk's output set
+        const uint32_t oset = (c & 1) * kTmOSet;
 #pragma unroll
         for (int kk = 0; kk < kDk / 16; ++kk) {
           const uint32_t off = (kk / 4) * kSBlk + (kk % 4) * 32;
-          mma_ss(tmem + kTmO1, sdesc_sw128(sbf + off, 16, 1024),
+          mma_ss(tmem + kTmO1 + oset, sdesc_sw128(sbf + off, 16, 1024),
                  sdesc_sw128(base + kStageQ + (kk / 4) * kBlkTok + (kk % 4) * 32, 16, 1024),
                  idesc_n64, kk > 0 ? 1u : 0u);
         }
         if (!(ok = mbar_wait(bar_uready, c & 1, p.status))) break;
         tc_fence_after();
-        // U^T P^T -> D_O2 (N = 64 query tokens, K = 64 key tokens)
-#pragma unroll
-        for (int kk = 0; kk < kC / 16; ++kk)
-          mma_ss(tmem + kTmO2, sdesc_sw128(ut + kk * 32, 16, 1024),
-                 sdesc_sw128(base + kStageP + kk * 32, 16, 1024), idesc_n64, kk > 0 ? 1u : 0u);
-        // D_S (already Gamma_C S) += U'^T K (N = 128 key dims, K = 64 tokens; K read MN-major)
+        // D_S (already Gamma_C S) += U'^T K (N = 128 key dims, K = 64 tokens; K read MN-major),
+        // first: the next chunk's state copy waits only for this
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
           mma_ss(tmem + kTmS, sdesc_sw128(upt + kk * 32, 16, 1024),
                  sdesc_sw128(base + kStageK + kk * 2048, kBlkTok, 1024), idesc_s, 1u);
+        tc_commit(bar_sdone);
+        // U^T P^T -> D_O2 (N = 64 query tokens, K = 64 key tokens)
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk)
+          mma_ss(tmem + kTmO2 + oset, sdesc_sw128(ut + kk * 32, 16, 1024),
+                 sdesc_sw128(base + kStageP + kk * 32, 16, 1024), idesc_n64, kk > 0 ? 1u : 0u);
         tc_commit(bar_odone);
         tc_commit(bar_empty(st));
       }
@@ -405,25 +537,33 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     };
     // This thread's columns: tokens 32 half .. +31 of D_U, D_O1, D_O2 and of U^T; key dims
     // 64 half .. +63 of the state (block `half` of its bf16 copy).
-    // The state entering chunk 0: the initial state (or zero), as the bf16 operand and in
-    // tensor memory (scaled by the chunk's decay before the chunk's MMA adds to it).
+    // Per chunk c the state in tensor memory enters already scaled by Gamma_C of chunk c (the
+    // chunk's MMA adds U'^T K to it), while the bf16 copy holds the unscaled state S.  Chunk
+    // c's outputs are formed as soon as its products land but stored only after chunk c+1's
+    // U has been published, so the stores overlap the next chunk's MMAs.
+    auto fct_of = [&](int cc) {
+      return reinterpret_cast<const float*>(smem + (cc & 1) * kStageBytes + kStageF);
+    };
+    bool ok = __all_sync(0xffffffffu, mbar_wait(bar_full(0), 0, p.status));
+    {
+      const float g0 = ok ? fct_of(0)[kC - 1] : 1.f;
 #pragma unroll 1
-    for (int pc = 0; pc < 2; ++pc) {
-      float s[32];
+      for (int pc = 0; pc < 2; ++pc) {
+        float s[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
-        s[e] = p.s0 ? p.s0[(bh * kDv + d) * kDk + half * 64 + pc * 32 + e] : 0.f;
-      put_row32(sbf + half * kSBlk, pc * 4, s);
-      uint32_t w[32];
+        for (int e = 0; e < 32; ++e)
+          s[e] = p.s0 ? p.s0[(bh * kDv + d) * kDk + half * 64 + pc * 32 + e] : 0.f;
+        put_row32(sbf + half * kSBlk, pc * 4, s);
+        uint32_t w[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(s[e]);
-      tmem_st32(tmem + kTmS + lane_off + half * 64 + pc * 32, w);
+        for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(s[e] * g0);
+        tmem_st32(tmem + kTmS + lane_off + half * 64 + pc * 32, w);
+      }
     }
     tmem_st_wait();
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(bar_sready);
-    bool ok = true;
     // U~ of this thread's 32 tokens of the next chunk, loaded ahead (row i, column d)
     float ut[32];
     {
@@ -431,22 +571,21 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 #pragma unroll
       for (int e = 0; e < 32; ++e) ut[e] = ub[static_cast<size_t>(e) * kDv];
     }
+    // outputs of the previous chunk, bf16 pairs, waiting to be stored
+    uint32_t opk[16];
+    int out_t0 = -1, out_n = 0;
+    auto store_out = [&]() {
+      if (out_t0 < 0 || !ok) return;
+      uint16_t* orow = p.out + (bh * p.T + out_t0 + half * 32) * kDv + d;
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (half * 32 + e < out_n)
+          orow[static_cast<size_t>(e) * kDv] = static_cast<uint16_t>((e & 1) ? (opk[e / 2] >> 16) : (opk[e / 2] & 0xFFFFu));
+    };
 #pragma unroll 1
     for (int c = 0; c < nc; ++c) {
       const int st = c & 1;
-      const float* fct = reinterpret_cast<const float*>(smem + st * kStageBytes + kStageF);
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_full(st), (c >> 1) & 1, p.status));
-      // ---- the state in tensor memory times Gamma_C, ready for this chunk's update ----
-      const float g_end = fct[kC - 1];
-#pragma unroll 1
-      for (int pc = 0; pc < 2; ++pc) {
-        uint32_t w[32];
-        tmem_ld32(tmem + kTmS + lane_off + half * 64 + pc * 32, w);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(__uint_as_float(w[e]) * g_end);
-        tmem_st32(tmem + kTmS + lane_off + half * 64 + pc * 32, w);
-      }
+      const float* fct = fct_of(c);
       // ---- U^T = U~^T - S W^T, and U'^T = U^T with token i scaled by Gamma_C / Gamma_i ----
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_udone, c & 1, p.status));
       tc_fence_after();
@@ -463,26 +602,25 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         put_row32(utp, half * 4, u);
         put_row32(uptp, half * 4, up);
       }
-      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_uready);
-      // ---- O = Gamma_i scale S q_i + (P U)_i, then the state's bf16 copy ----
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_odone, c & 1, p.status));
+      store_out();  // the previous chunk's outputs, while this chunk's last MMAs run
+      // ---- the state's bf16 copy (and the next chunk's scaled state) once D_S is final ----
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_sdone, c & 1, p.status));
       tc_fence_after();
-      const int t0 = c * kC, n = min(kC, p.T - t0);
-      if (c + 1 < nc) {  // next chunk's U~, in flight while this chunk finishes
+      const bool last = c + 1 == nc;
+      if (!last) {  // next chunk's U~, in flight while this chunk finishes
         const float* ub = p.u_ws + (bh * p.Tpad + (c + 1) * kC + half * 32) * kDv + d;
 #pragma unroll
         for (int e = 0; e < 32; ++e) ut[e] = ub[static_cast<size_t>(e) * kDv];
       }
-      // D_O1 and D_O2 into registers, then the state's bf16 copy for the next chunk's MMAs;
-      // the outputs are formed and stored after that copy is published
-      uint32_t o1[32], o2[32];
-      tmem_ld32(tmem + kTmO1 + lane_off + half * 32, o1);
-      tmem_ld32(tmem + kTmO2 + lane_off + half * 32, o2);
-      tmem_ld_wait();
-      const bool last = c + 1 == nc;
+      // the next chunk's Gamma_C (its stage was loaded ahead)
+      float g_next = 1.f;
+      if (!last) {
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_full((c + 1) & 1), ((c + 1) >> 1) & 1, p.status));
+        g_next = ok ? fct_of(c + 1)[kC - 1] : 1.f;
+      }
 #pragma unroll 1
       for (int pc = 0; pc < 2; ++pc) {
         uint32_t w[32];
@@ -499,26 +637,41 @@ __global__ void __launch_bounds__(kStateThreads, 1)
           }
         } else {
           put_row32(sbf + half * kSBlk, pc * 4, s);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(s[e] * g_next);
+          tmem_st32(tmem + kTmS + lane_off + half * 64 + pc * 32, w);
         }
       }
       if (!last) {
+        tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar_sready);
       }
-      if (ok) {
-        uint16_t* orow = p.out + (bh * p.T + t0 + half * 32) * kDv + d;
+      // ---- O = Gamma_i scale S q_i + (P U)_i from this chunk's output set: the next chunk's
+      // products go to the other set, so this read may follow the state's publication ----
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_odone, c & 1, p.status));
+      tc_fence_after();
+      {
+        const uint32_t oset = (c & 1) * kTmOSet;
+        uint32_t o1[32], o2[32];
+        tmem_ld32(tmem + kTmO1 + oset + lane_off + half * 32, o1);
+        tmem_ld32(tmem + kTmO2 + oset + lane_off + half * 32, o2);
+        tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          if (half * 32 + e < n) {
-            const float o = fct[half * 32 + e] * p.scale * __uint_as_float(o1[e]) + __uint_as_float(o2[e]);
-            const __nv_bfloat16 hv = __float2bfloat16_rn(o);
-            orow[static_cast<size_t>(e) * kDv] = *reinterpret_cast<const uint16_t*>(&hv);
-          }
+        for (int e = 0; e < 16; ++e) {
+          const float a0 = fct[half * 32 + 2 * e] * p.scale * __uint_as_float(o1[2 * e]) + __uint_as_float(o2[2 * e]);
+          const float a1 = fct[half * 32 + 2 * e + 1] * p.scale * __uint_as_float(o1[2 * e + 1]) +
+                           __uint_as_float(o2[2 * e + 1]);
+          opk[e] = pack_bf16x2(a0, a1);
         }
+        out_t0 = c * kC;
+        out_n = min(kC, p.T - out_t0);
       }
+      tc_fence_before();
       mbar_arrive(bar_empty(st));  // this thread is done with the stage's decay factors
     }
+    store_out();
   }
   tc_fence_before();
   __syncthreads();
