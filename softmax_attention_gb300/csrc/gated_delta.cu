@@ -385,9 +385,11 @@ constexpr int kSbfOff = 2 * kStageBytes;         // S as bf16, [128 rows][2 bloc
 constexpr int kSBlk = kDv * 128;                 // 16384: one 64-column block of S
 constexpr int kUtOff = kSbfOff + 2 * kSBlk;      // U^T, [128 rows][128 B]
 constexpr int kUptOff = kUtOff + kSBlk;          // U^T with each token's decay to the chunk end
-constexpr int kBarOff = kUptOff + kSBlk;
-// full[2], empty[2], s_ready, u_ready, u_done, o_done, mma_done, s_done
-constexpr int kNumBars = 10;
+constexpr int kUtlOff = kUptOff + kSBlk;         // U~ of the chunk, fp32 [64 tokens][128 dv]
+constexpr int kUtlBytes = kC * kDv * 4;
+constexpr int kBarOff = kUtlOff + kUtlBytes;
+// full[2], empty[2], s_ready, u_ready, u_done, o_done, mma_done, s_done, utl_full, utl_empty
+constexpr int kNumBars = 12;
 constexpr int kStateSmem = kBarOff + kNumBars * 8 + 16 + 1024;
 static_assert(kStateSmem <= 232448, "shared memory budget");
 // tensor memory: the state (128 columns), D_U (64), and two sets of output accumulators D_O1,
@@ -409,6 +411,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   const uint32_t bar_sready = bars + 8u * 4, bar_uready = bars + 8u * 5;
   const uint32_t bar_udone = bars + 8u * 6, bar_odone = bars + 8u * 7, bar_done = bars + 8u * 8;
   const uint32_t bar_sdone = bars + 8u * 9;  // the state update of the chunk has finished
+  const uint32_t bar_utl_full = bars + 8u * 10, bar_utl_empty = bars + 8u * 11;  // U~ tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + kNumBars * 8);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -430,6 +433,8 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     mbar_init(bar_odone, 1);
     mbar_init(bar_done, 1);
     mbar_init(bar_sdone, 1);
+    mbar_init(bar_utl_full, 1);
+    mbar_init(bar_utl_empty, kStateArrivals);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -448,7 +453,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_p);
-      int issued = 0;
+      int issued = 0, u_issued = 0;
       for (int c = 0; c < nc; ++c) {
         const int st = c & 1;
         if (c >= 2 && !mbar_wait(bar_empty(st), ((c >> 1) - 1) & 1, p.status)) break;
@@ -463,10 +468,16 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         tma_load_2d(base + kStageP, &tm_p, bar_full(st), 0, row);
         bulk_load(base + kStageF, p.f_ws + (bh * nc + c) * (2 * kC), 2 * kC * 4, bar_full(st));
         issued = c + 1;
+        // the chunk's U~ (64 contiguous rows), once the state warps have read the previous one
+        if (c >= 1 && !mbar_wait(bar_utl_empty, (c - 1) & 1, p.status)) break;
+        mbar_arrive_expect_tx(bar_utl_full, kUtlBytes);
+        bulk_load(s_base + kUtlOff, p.u_ws + (bh * p.Tpad + c * kC) * kDv, kUtlBytes, bar_utl_full);
+        u_issued = c + 1;
       }
       // a wait ran out: let the copies in flight land before the CTA exits
       for (int c = max(0, issued - 2); c < issued && issued < nc; ++c)
         mbar_wait(bar_full(c & 1), (c >> 1) & 1, nullptr);
+      if (u_issued > 0 && u_issued < nc) mbar_wait(bar_utl_full, (u_issued - 1) & 1, nullptr);
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------- MMA issuer --------------------------------------
@@ -564,13 +575,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(bar_sready);
-    // U~ of this thread's 32 tokens of the next chunk, loaded ahead (row i, column d)
-    float ut[32];
-    {
-      const float* ub = p.u_ws + (bh * p.Tpad + half * 32) * kDv + d;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) ut[e] = ub[static_cast<size_t>(e) * kDv];
-    }
+    const float* utl = reinterpret_cast<const float*>(smem + kUtlOff);  // U~ [token][dv]
     // outputs of the previous chunk, bf16 pairs, waiting to be stored
     uint32_t opk[16];
     int out_t0 = -1, out_n = 0;
@@ -592,13 +597,15 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       {
         uint32_t du[32];
         tmem_ld32(tmem + kTmU + lane_off + half * 32, du);
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_utl_full, c & 1, p.status));
         tmem_ld_wait();
         float u[32], up[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          u[e] = ut[e] - __uint_as_float(du[e]);
+          u[e] = utl[(half * 32 + e) * kDv + d] - __uint_as_float(du[e]);
           up[e] = u[e] * fct[kC + half * 32 + e];
         }
+        mbar_arrive(bar_utl_empty);  // this thread has read the chunk's U~
         put_row32(utp, half * 4, u);
         put_row32(uptp, half * 4, up);
       }
@@ -610,11 +617,6 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_sdone, c & 1, p.status));
       tc_fence_after();
       const bool last = c + 1 == nc;
-      if (!last) {  // next chunk's U~, in flight while this chunk finishes
-        const float* ub = p.u_ws + (bh * p.Tpad + (c + 1) * kC + half * 32) * kDv + d;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) ut[e] = ub[static_cast<size_t>(e) * kDv];
-      }
       // the next chunk's Gamma_C (its stage was loaded ahead)
       float g_next = 1.f;
       if (!last) {
