@@ -167,45 +167,49 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   }
   __syncthreads();
   bool ok = __syncthreads_and(mbar_wait(bar_mma, 0, p.status));
-  if (warp < 4) {
-    // lane r of the Gram result: r < 64 is row r of Q K^T (-> P), r >= 64 row r - 64 of K K^T
+  {
+    // lane r of the Gram result: r < 64 is row r of Q K^T (-> P), r >= 64 row r - 64 of K K^T;
+    // warps q and q + 4 share the sub-partition's lanes and take columns 0-31 and 32-63
     tc_fence_after();
-    uint32_t raw[kC];
-    tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16), *reinterpret_cast<uint32_t(*)[32]>(&raw[0]));
-    tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 32,
-              *reinterpret_cast<uint32_t(*)[32]>(&raw[32]));
+    const int quad = warp % 4, j0 = 32 * (warp / 4);
+    uint32_t raw[32];
+    tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + j0, raw);
     tmem_ld_wait();
     // Gamma_i / Gamma_j = 2^(gl_i - gl_j) <= 1 for j <= i (gl = gamma in log2 units)
     const float* gl = graw;
-    if (tid < kC) {
-      const int i = tid;
+    const int r = quad * 32 + lane;
+    if (r < kC) {
+      const int i = r;
       const float gi = gl[i];
-      uint32_t pk[kC / 2];
+      uint32_t pk[16];
 #pragma unroll
-      for (int j = 0; j < kC; j += 2) {
-        const float p0 = (j <= i && i < n) ? p.scale * exp2_approx(gi - gl[j]) * __uint_as_float(raw[j]) : 0.f;
-        const float p1 = (j + 1 <= i && i < n) ? p.scale * exp2_approx(gi - gl[j + 1]) * __uint_as_float(raw[j + 1]) : 0.f;
-        pk[j / 2] = pack_bf16x2(p0, p1);
+      for (int e = 0; e < 32; e += 2) {
+        const int j = j0 + e;
+        const float p0 = (j <= i && i < n) ? p.scale * exp2_approx(gi - gl[j]) * __uint_as_float(raw[e]) : 0.f;
+        const float p1 = (j + 1 <= i && i < n) ? p.scale * exp2_approx(gi - gl[j + 1]) * __uint_as_float(raw[e + 1]) : 0.f;
+        pk[e / 2] = pack_bf16x2(p0, p1);
       }
-      uint4* dst = reinterpret_cast<uint4*>(p.p_ws + (bh * p.Tpad + t0 + i) * kC);
+      uint4* dst = reinterpret_cast<uint4*>(p.p_ws + (bh * p.Tpad + t0 + i) * kC + j0);
 #pragma unroll
-      for (int e = 0; e < kC / 8; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+      for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
     } else {
-      const int i = tid - kC;
+      const int i = r - kC;
       const float gi = gl[i], bi = bet[i];
 #pragma unroll
-      for (int j = 0; j < kC; j += 4) {
+      for (int e = 0; e < 32; e += 4) {
+        const int j = j0 + e;
         float4 a;
-        a.x = j < i ? bi * exp2_approx(gi - gl[j]) * __uint_as_float(raw[j]) : 0.f;
-        a.y = j + 1 < i ? bi * exp2_approx(gi - gl[j + 1]) * __uint_as_float(raw[j + 1]) : 0.f;
-        a.z = j + 2 < i ? bi * exp2_approx(gi - gl[j + 2]) * __uint_as_float(raw[j + 2]) : 0.f;
-        a.w = j + 3 < i ? bi * exp2_approx(gi - gl[j + 3]) * __uint_as_float(raw[j + 3]) : 0.f;
+        a.x = j < i ? bi * exp2_approx(gi - gl[j]) * __uint_as_float(raw[e]) : 0.f;
+        a.y = j + 1 < i ? bi * exp2_approx(gi - gl[j + 1]) * __uint_as_float(raw[e + 1]) : 0.f;
+        a.z = j + 2 < i ? bi * exp2_approx(gi - gl[j + 2]) * __uint_as_float(raw[e + 2]) : 0.f;
+        a.w = j + 3 < i ? bi * exp2_approx(gi - gl[j + 3]) * __uint_as_float(raw[e + 3]) : 0.f;
         *reinterpret_cast<float4*>(As + i * kTriF + j) = a;
       }
     }
-  } else if (tid < 128 + 2 * kC) {
+  }
+  if (tid < 2 * kC) {
     // decay factors of the chunk: Gamma_i, then Gamma_C / Gamma_i
-    const int e = tid - 128;
+    const int e = tid;
     const float v = e < kC ? expf(gam[e]) : expf(gam[kC - 1] - gam[e - kC]);
     p.f_ws[(bh * p.n_chunks + c) * (2 * kC) + e] = v;
     if (e < kC) Gam[e] = v;
