@@ -30,15 +30,17 @@ __device__ __forceinline__ void store4(void* out, Dtype t, size_t idx, float4 v)
 // kMergeWarps warps per CTA; W of them (1, 2, 4 or 8, from the largest part count) share one
 // row, so a CTA merges kMergeWarps / W rows.  Every warp of a row reduces the row's
 // log-sum-exps (a few loads, L1-resident), then accumulates the parts s = k, k + W, ... of
-// the row over all D columns: lane l holds the 16-byte vectors l, l + 32, ... (VPL of them),
-// and the part loop is unrolled so that several parts' loads are in flight at once.  With
-// W > 1 the warps' sums are combined through shared memory.  Few parts: one warp per row
-// and eight rows per CTA; many parts: eight warps on one row.
+// the row over all D columns: lane l holds the 16-byte vectors l, l + 32, ... (VPL of them).
+// Parts are taken in batches of kBatch whose loads are all issued before their
+// multiply-adds, and the first batch is issued before the log-sum-exp reduction, so that its
+// latency overlaps it.  With W > 1 the warps' sums are combined through shared memory.  Few
+// parts: one warp per row and eight rows per CTA; many parts: eight warps on one row.
 constexpr int kMergeWarps = 8;
 
 template <int VPL>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p, int W) {
   extern __shared__ float4 part[];  // [kMergeWarps][VPL * 32] when W > 1
+  constexpr int kBatch = 8 / VPL;   // parts per batch: 8 float4 per lane in flight
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int rows_per_cta = kMergeWarps / W;
   const int row = blockIdx.x * rows_per_cta + warp / W;
@@ -59,6 +61,20 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
     }
     n = max(0, min(n, p.max_splits));
     const float* lrow = p.lse_part + static_cast<size_t>(row) * p.max_splits;
+    const float4* orow = reinterpret_cast<const float4*>(p.o_part + static_cast<size_t>(row) * p.max_splits * p.D);
+    auto load_batch = [&](int s0, float4 (&xv)[kBatch][VPL]) {
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int s = s0 + u * W;
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+          const int v = lane + 32 * j;
+          xv[u][j] = (s < n && v < nv) ? orow[static_cast<size_t>(s) * nv + v] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    };
+    float4 xv[kBatch][VPL];
+    load_batch(k, xv);
     float m = -INFINITY;
     for (int s = lane; s < n; s += 32) m = fmaxf(m, lrow[s]);
 #pragma unroll
@@ -70,23 +86,23 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
     for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     lse = (m == -INFINITY) ? -INFINITY : m + logf(sum);
     if (m != -INFINITY) {
-      const float4* orow = reinterpret_cast<const float4*>(p.o_part + static_cast<size_t>(row) * p.max_splits * p.D);
-#pragma unroll 4
-      for (int s = k; s < n; s += W) {
-        const float ls = lrow[s];
-        const float w = (ls == -INFINITY) ? 0.f : exp2_approx((ls - lse) * kLog2e);
-        const float4* src = orow + static_cast<size_t>(s) * nv;
+      for (int s0 = k;; ) {
 #pragma unroll
-        for (int j = 0; j < VPL; ++j) {
-          const int v = lane + 32 * j;
-          if (v < nv) {
-            const float4 x = src[v];
-            acc[j].x = fmaf(w, x.x, acc[j].x);
-            acc[j].y = fmaf(w, x.y, acc[j].y);
-            acc[j].z = fmaf(w, x.z, acc[j].z);
-            acc[j].w = fmaf(w, x.w, acc[j].w);
+        for (int u = 0; u < kBatch; ++u) {
+          const int s = s0 + u * W;
+          const float ls = s < n ? lrow[s] : -INFINITY;
+          const float w = (ls == -INFINITY) ? 0.f : exp2_approx((ls - lse) * kLog2e);
+#pragma unroll
+          for (int j = 0; j < VPL; ++j) {
+            acc[j].x = fmaf(w, xv[u][j].x, acc[j].x);
+            acc[j].y = fmaf(w, xv[u][j].y, acc[j].y);
+            acc[j].z = fmaf(w, xv[u][j].z, acc[j].z);
+            acc[j].w = fmaf(w, xv[u][j].w, acc[j].w);
           }
         }
+        s0 += kBatch * W;
+        if (s0 >= n) break;
+        load_batch(s0, xv);
       }
     }
   }
