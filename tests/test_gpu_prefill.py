@@ -131,6 +131,27 @@ def test_additive_mask(mask_dtype, mask_b):
     check(out, lse, ro, rl, what="mask")
 
 
+@pytest.mark.parametrize("D,causal,splits", [(64, False, 0), (128, False, 0), (128, True, 3),
+                                              (256, False, 0), (256, True, 2)])
+def test_running_max_rises_every_tile(D, causal, splits):
+    """Scores that grow along the keys by ~12 (log2 units) per key tile: every tile moves the
+    running max past the lazy-rescale threshold, so O and the row sum are rescaled each time;
+    with splits, the parts' log-sum-exps differ by hundreds."""
+    c = workloads.DenseCase(B=1, Hq=4, Hkv=2, Lq=96, Lkv=1100, D=D, causal=causal, sigma=0.5,
+                            seed=D + 5)
+    q, k, v = workloads.dense_inputs(c)
+    bn = 64 if D == 256 else 128
+    ramp = 12.0 / (bn * 2.0 * c.sm_scale * 1.4426950408889634)  # per key, in raw score units
+    q[..., 0] = 2.0
+    k[..., 0] = (k[..., 0].float() + ramp * torch.arange(c.Lkv, dtype=torch.float32)).to(k.dtype)
+    dev = torch.device("cuda")
+    out, lse = fa.fa_prefill_ex(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=c.sm_scale,
+                                num_splits=splits)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(q, k, v, causal=causal, scale=c.sm_scale)
+    check(out, lse, ro, rl, what=f"rising scores D={D} causal={causal} splits={splits}")
+
+
 def test_fp16_inputs():
     c = workloads.DenseCase(B=1, Hq=4, Hkv=1, Lq=150, Lkv=400, D=128, causal=True,
                             dtype=torch.float16, sigma=0.5)

@@ -70,6 +70,32 @@ def test_parity_shapes(B, Hq, Hkv, Lq, lens, D, ps, causal):
     check(out, lse, ro, rl, what=f"paged prefill {lens} D={D} ps={ps}")
 
 
+@pytest.mark.parametrize("D,ps", [(128, 16), (256, 64)])
+def test_running_max_rises_every_tile(D, ps):
+    """Scores that grow along each sequence's keys by ~12 (log2 units) per key tile, so every
+    tile moves the running max past the lazy-rescale threshold (the paged instantiations
+    reduce the tile max differently from the dense one)."""
+    c = workloads.PagedPrefillCase(B=2, Hq=8, Hkv=2, Lq=40, D=D, page_size=ps, num_pages=120,
+                                   min_len=0, max_len=1100, seq_lens=[1100, 700], causal=True,
+                                   seed=D + ps)
+    q, kp, vp, table, lens = workloads.paged_prefill_inputs(c)
+    bn = 64 if D == 256 else 128
+    ramp = 12.0 / (bn * 2.0 * c.sm_scale * 1.4426950408889634)  # per key, in raw score units
+    q[..., 0] = 2.0
+    for b in range(c.B):
+        n = int(lens[b])
+        for pi in range(-(-n // ps)):
+            keys = pi * ps + torch.arange(ps, dtype=torch.float32)
+            page = int(table[b, pi])
+            kp[page, :, :, 0] = (kp[page, :, :, 0].float() + ramp * keys).to(kp.dtype)
+    qd, kd, vd, td, ld = (t.cuda() for t in (q, kp, vp, table, lens))
+    out, lse = fa.fa_prefill_paged(qd, kd, vd, td, ld, int(lens.max()), causal=True,
+                                   scale=c.sm_scale)
+    torch.cuda.synchronize()
+    ro, rl = oracle.prefill_paged(q, kp, vp, table, lens, causal=True, scale=c.sm_scale)
+    check(out, lse, ro, rl, what=f"paged rising scores D={D} page={ps}")
+
+
 def test_full_size_sampled():
     c = workloads.paged_gqa_prefill()
     rows = list(range(0, c.B * c.Hq * c.Lq, 613))
