@@ -94,6 +94,28 @@ def test_parity_shapes(B, Hq, Hkv, D, ps, lens, path):
 
 
 @pytest.mark.parametrize("path", [CC, TC], ids=["cuda_cores", "tensor_cores"])
+def test_running_max_rises_every_tile(path):
+    """Scores that grow along each sequence by ~0.2 (log2 units) per token: every key tile
+    (and every CUDA-core chunk) moves the running max past the lazy-rescale threshold."""
+    c = workloads.PagedCase(B=3, Hq=32, Hkv=8, D=128, page_size=16, num_pages=200, min_len=1,
+                            max_len=1500, seq_lens=[1500, 900, 40], seed=17)
+    q, kp, vp, table, lens = workloads.paged_inputs(c)
+    ramp = 0.2 / (2.0 * c.sm_scale * 1.4426950408889634)  # per token, in raw score units
+    q[..., 0] = 2.0
+    for b in range(c.B):
+        n = int(lens[b])
+        for pi in range(-(-n // c.page_size)):
+            toks = pi * c.page_size + torch.arange(c.page_size, dtype=torch.float32)
+            page = int(table[b, pi])
+            kp[page, :, :, 0] = (kp[page, :, :, 0].float() + ramp * toks).to(kp.dtype)
+    out, lse = fa.fa_decode_paged(*_gpu(q, kp, vp, table, lens), int(lens.max()), c.sm_scale,
+                                  path=path)
+    torch.cuda.synchronize()
+    ro, rl = oracle.decode_paged(q, kp, vp, table, lens, scale=c.sm_scale)
+    check(out, lse, ro, rl, what=f"decode rising scores path {path}")
+
+
+@pytest.mark.parametrize("path", [CC, TC], ids=["cuda_cores", "tensor_cores"])
 def test_paged_equals_dense_gathered_bit_exact(path):
     c = workloads.PagedCase(B=6, Hq=32, Hkv=8, D=128, page_size=16, num_pages=2000, min_len=1,
                             max_len=3000, seed=5)

@@ -55,6 +55,28 @@ def test_parity_shapes(lens, ps):
     check(out, lse, ro, rl, what=f"mla {lens} ps={ps}")
 
 
+@pytest.mark.parametrize("ps", [1, 64])
+def test_running_max_rises_every_tile(ps):
+    """Scores that grow along each sequence by ~0.2 (log2 units) per token, ~13 per 64-token
+    tile: every tile moves the running max past the lazy-rescale threshold.  The ramp is put
+    on the rope part (kpe, q_pe), which enters the scores but not the values."""
+    c = workloads.MlaCase(B=2, H=64, seq_len=None, seq_lens=[2000, 900], page_size=ps, seed=ps + 3)
+    qn, qp, ckv, kpe, table, lens = workloads.mla_inputs(c)
+    ramp = 0.2 / (2.0 * c.scale * 1.4426950408889634)  # per token, in raw score units
+    qp[..., 0] = 2.0
+    for b in range(c.B):
+        n = int(lens[b])
+        for pi in range(-(-n // ps)):
+            toks = pi * ps + torch.arange(ps, dtype=torch.float32)
+            page = int(table[b, pi])
+            kpe[page, :, 0] = (kpe[page, :, 0].float() + ramp * toks).to(kpe.dtype)
+    dev = [t.cuda() for t in (qn, qp, ckv, kpe, table, lens)]
+    out, lse = fa.mla_decode_paged(*dev, c.max_len, c.scale)
+    torch.cuda.synchronize()
+    ro, rl = oracle.mla_decode_paged(qn, qp, ckv, kpe, table, lens, scale=c.scale)
+    check(out, lse, ro, rl, what=f"mla rising scores ps={ps}")
+
+
 @pytest.mark.parametrize("H,lens,ps", [
     (16, [100, 700, 0], 1),      # one tensor-parallel shard's heads: a partial head group
     (32, [513, 64], 16),
