@@ -49,6 +49,11 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map
 
 constexpr int kNumS = 3;  // S/P buffers in tensor memory
 
+// Named barrier `id` over `nthreads` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 template <int D, int BN, int STAGES>
 struct Layout {
   static constexpr int kQBytes = kRows * D * 2;
@@ -70,10 +75,13 @@ struct Layout {
 };
 
 // One CTA per (query tile, split) x kv head x batch.  PAGED: K/V through a page table.
-template <int D, int BN, int STAGES, bool BF16, bool PAGED>
+// SPLIT: the KV loop is split across CTAs and each writes a partial state (a separate
+// instantiation, so that the unsplit kernel carries none of its epilogue).
+template <int D, int BN, int STAGES, bool BF16, bool PAGED, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_po,
+                   const PrefillParams p) {
   using L = Layout<D, BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -420,15 +428,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar_pv((n - 1) % kNumS), ((n - 1) / kNumS) & 1, p.status));
       tc_fence_after();
     }
-    if (ok) {
-      float* part_o = nullptr;
-      float* part_lse = nullptr;
-      if (p.n_splits > 1 && row.valid) {
-        const size_t r = row.flat * p.n_splits + split;
-        part_o = p.o_part + r * D;
-        part_lse = p.lse_part + r;
+    if constexpr (SPLIT) {
+      // A split's partial state (O / l in fp32, a row per thread) is staged in the K/V rings,
+      // free once the loop is done, and written by TMA stores of whole 32-column tiles: rows
+      // are 1 KB apart in the partial buffer, so per-thread stores would not coalesce.  Every
+      // softmax thread reaches the barrier; a warp whose waits ran out flags the tile so that
+      // nothing half-written is stored.
+      volatile uint32_t& stage_bad = tmem_slot[1];  // spare word beside the tensor-memory slot
+      if (threadIdx.x == 0) stage_bad = 0;
+      named_barrier_sync(1, 4 * 32);
+      uint8_t* stage = smem + L::kKOff;
+      if (ok) {
+        prefill::epilogue_stage<D>(tm_o + lane_off, n > 0, m_run, l_run, stage, threadIdx.x,
+                                   row.valid ? p.lse_part + row.flat * p.n_splits + split : nullptr);
+      } else if (lane == 0) {
+        stage_bad = 1;
       }
-      prefill::epilogue<D>(p, row, tm_o + lane_off, n > 0, m_run, l_run, part_o, part_lse);
+      fence_proxy_async_smem();
+      named_barrier_sync(1, 4 * 32);
+      if (threadIdx.x == 0 && !stage_bad) {
+        // box: 32 columns x 1 split x q_per_tile queries x G heads; rows past Lq are clipped
+        for (int c = 0; c < D / 32; ++c)
+          prefill::tma_store_4d(&tm_po, sK + c * (kRows * 128), c * 32, split, q0, b * p.Hq + hk * p.G);
+        prefill::bulk_commit_group();
+        prefill::bulk_wait_read_all();
+      }
+    } else if (ok) {
+      prefill::epilogue<D>(p, row, tm_o + lane_off, n > 0, m_run, l_run, nullptr, nullptr);
     }
   }
   tc_fence_before();
@@ -472,11 +498,24 @@ cudaError_t launch_impl(const PrefillParams& p, cudaStream_t stream) {
         !encode_tiled(&tv, dt, 3, p.v, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  auto kern = prefill_kernel<D, BN, STAGES, BF16, PAGED>;
+  // the partial states [B*Hq rows: (b, h, i)][n_splits][D] fp32, as (column, split, query,
+  // b*Hq + h); one store box = 32 columns x 1 split x q_per_tile queries x G heads
+  CUtensorMap tpo = tq;  // not read unless the KV loop is split
+  if (p.n_splits > 1) {
+    const uint64_t ns = (uint64_t)p.n_splits;
+    const uint64_t dims[4] = {(uint64_t)D, ns, (uint64_t)p.Lq, (uint64_t)p.Hq * p.B};
+    const uint64_t str[3] = {(uint64_t)D * 4, ns * D * 4, (uint64_t)p.Lq * ns * D * 4};
+    const uint32_t box[4] = {32, 1, (uint32_t)p.q_per_tile, (uint32_t)p.G};
+    if (!encode_tiled(&tpo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.o_part, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  auto kern = p.n_splits > 1 ? prefill_kernel<D, BN, STAGES, BF16, PAGED, true>
+                             : prefill_kernel<D, BN, STAGES, BF16, PAGED, false>;
   cudaError_t e = ensure_smem_limit(kern, L::kAlloc);
   if (e != cudaSuccess) return e;
   const dim3 grid(p.n_qtiles * p.n_splits, p.Hkv, p.B);
-  kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, p);
+  kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, tpo, p);
   return cudaGetLastError();
 }
 

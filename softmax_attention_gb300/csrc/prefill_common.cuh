@@ -229,6 +229,52 @@ __device__ __forceinline__ void epilogue(const PrefillParams& p, const Row& row,
   }
 }
 
+// 4-D tiled TMA store from shared to global memory, completed through the bulk group
+// (coordinates non-negative; the innermost one a multiple of 16 bytes).
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int32_t c0,
+                                             int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until the committed bulk stores have read their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Partial-state epilogue of one row, staged for TMA stores: O / l (fp32) of row r goes into
+// the D/32 staging tiles (tile c holds columns 32c .. 32c+31 of the 128 rows, 128-byte rows,
+// 128-byte swizzle: 16-byte chunk ch of row r at chunk ch ^ (r & 7)); the lse goes to
+// part_lse when set.  Warp-collective (every lane reads its TMEM lane).
+template <int D>
+__device__ __forceinline__ void epilogue_stage(uint32_t t_o, bool have_o, float m, float l,
+                                               uint8_t* stage, int r, float* part_lse) {
+  const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    if (have_o) {
+      tmem_ld32(t_o + c * 32, o);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = 0u;
+    }
+    uint8_t* tile = stage + c * (kRows * 128) + r * 128;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+      *reinterpret_cast<float4*>(tile + ((ch ^ (r & 7)) * 16)) =
+          make_float4(__uint_as_float(o[4 * ch]) * inv_l, __uint_as_float(o[4 * ch + 1]) * inv_l,
+                      __uint_as_float(o[4 * ch + 2]) * inv_l, __uint_as_float(o[4 * ch + 3]) * inv_l);
+  }
+  if (part_lse) *part_lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+}
+
 // KV tiles [t_begin, t_end) of one split for a tile set whose last query is q_last, in a
 // sequence of Lkv keys.
 __device__ __forceinline__ void kv_range(const PrefillParams& p, int q_last, int bn, int split,
