@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_po,
                    const PrefillParams p) {
   using L = Layout<D, BN, STAGES>;
+  constexpr bool kStagedOut = D <= 128;  // final 16-bit output through TMA stores
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -453,6 +454,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefill::bulk_commit_group();
         prefill::bulk_wait_read_all();
       }
+    } else if (kStagedOut && p.Lq > 1 && p.out_dtype != Dtype::FP32) {
+      // The 16-bit output is staged the same way and written by TMA stores through a map
+      // shaped like Q's (64 columns x q_per_tile queries x G heads per box).  Measured: a
+      // gain for D <= 128 with a query tile of several queries; one query per tile (decode)
+      // and the D = 256 kernels keep the per-thread stores.
+      volatile uint32_t& stage_bad = tmem_slot[1];
+      if (threadIdx.x == 0) stage_bad = 0;
+      named_barrier_sync(1, 4 * 32);
+      uint8_t* stage = smem + L::kKOff;
+      if (ok) {
+        prefill::epilogue_stage16<D, BF16>(tm_o + lane_off, n > 0, m_run, l_run, stage, threadIdx.x,
+                                           row.valid && p.lse ? p.lse + row.flat : nullptr);
+      } else if (lane == 0) {
+        stage_bad = 1;
+      }
+      fence_proxy_async_smem();
+      named_barrier_sync(1, 4 * 32);
+      if (threadIdx.x == 0 && !stage_bad) {
+        for (int t = 0; t < D / 64; ++t)
+          prefill::tma_store_4d(&tm_po, sK + t * (kRows * 128), t * 64, q0, hk * p.G, b);
+        prefill::bulk_commit_group();
+        prefill::bulk_wait_read_all();
+      }
     } else if (ok) {
       prefill::epilogue<D>(p, row, tm_o + lane_off, n > 0, m_run, l_run, nullptr, nullptr);
     }
@@ -500,7 +524,16 @@ cudaError_t launch_impl(const PrefillParams& p, cudaStream_t stream) {
   }
   // the partial states [B*Hq rows: (b, h, i)][n_splits][D] fp32, as (column, split, query,
   // b*Hq + h); one store box = 32 columns x 1 split x q_per_tile queries x G heads
-  CUtensorMap tpo = tq;  // not read unless the KV loop is split
+  CUtensorMap tpo = tq;
+  if (D <= 128 && p.Lq > 1 && p.n_splits <= 1 && p.out_dtype != Dtype::FP32) {
+    // the 16-bit output [B, Hq, Lq, D], as Q: one store box = 64 columns x q_per_tile queries
+    // x G heads
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)p.Lq, (uint64_t)p.Hq, (uint64_t)p.B};
+    const uint64_t str[3] = {(uint64_t)D * 2, (uint64_t)p.Lq * D * 2, (uint64_t)p.Hq * p.Lq * D * 2};
+    const uint32_t box[4] = {64, (uint32_t)p.q_per_tile, (uint32_t)p.G, 1};
+    if (!encode_tiled(&tpo, dt, 4, p.out, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   if (p.n_splits > 1) {
     const uint64_t ns = (uint64_t)p.n_splits;
     const uint64_t dims[4] = {(uint64_t)D, ns, (uint64_t)p.Lq, (uint64_t)p.Hq * p.B};

@@ -275,6 +275,41 @@ __device__ __forceinline__ void epilogue_stage(uint32_t t_o, bool have_o, float 
   if (part_lse) *part_lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
+// Final-output epilogue of one row, staged for TMA stores: O / l in 16 bits (BF16 selects
+// bf16, else fp16) goes into the D/64 staging tiles (tile t holds columns 64t .. 64t+63 of
+// the 128 rows, 128-byte rows, 128-byte swizzle); the lse goes to lse_out when set.
+template <int D, bool BF16>
+__device__ __forceinline__ void epilogue_stage16(uint32_t t_o, bool have_o, float m, float l,
+                                                 uint8_t* stage, int r, float* lse_out) {
+  const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    if (have_o) {
+      tmem_ld32(t_o + c * 32, o);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = 0u;
+    }
+    // columns 32c .. 32c+31 are 16-byte chunks 4(c % 2) .. 4(c % 2) + 3 of tile c / 2
+    uint8_t* tile = stage + (c / 2) * (kRows * 128) + r * 128;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float a = __uint_as_float(o[8 * q + 2 * e]) * inv_l;
+        const float b = __uint_as_float(o[8 * q + 2 * e + 1]) * inv_l;
+        w[e] = BF16 ? pack_bf16x2(a, b) : pack_f16x2(a, b);
+      }
+      const int ch = 4 * (c % 2) + q;
+      *reinterpret_cast<uint4*>(tile + ((ch ^ (r & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  if (lse_out) *lse_out = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+}
+
 // KV tiles [t_begin, t_end) of one split for a tile set whose last query is q_last, in a
 // sequence of Lkv keys.
 __device__ __forceinline__ void kv_range(const PrefillParams& p, int q_last, int bn, int split,
