@@ -159,10 +159,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_ke(s), 1);
       mbar_init(bar_ve(s), 1);
     }
-    for (int b = 0; b < kNumS; ++b) {
-      mbar_init(bar_s(b), 1);
-      mbar_init(bar_p(b), 4 * 32);
-      mbar_init(bar_pv(b), 1);
+    for (int i = 0; i < kNumS; ++i) {
+      mbar_init(bar_s(i), 1);
+      mbar_init(bar_p(i), 4 * 32);
+      mbar_init(bar_pv(i), 1);
     }
     mbar_init(bar_done, 1);
     mbar_init(bar_sdone, 1);
@@ -429,53 +429,67 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar_pv((n - 1) % kNumS), ((n - 1) / kNumS) & 1, p.status));
       tc_fence_after();
     }
-    if constexpr (SPLIT) {
-      // A split's partial state (O / l in fp32, a row per thread) is staged in the K/V rings,
-      // free once the loop is done, and written by TMA stores of whole 32-column tiles: rows
-      // are 1 KB apart in the partial buffer, so per-thread stores would not coalesce.  Every
-      // softmax thread reaches the barrier; a warp whose waits ran out flags the tile so that
-      // nothing half-written is stored.
-      volatile uint32_t& stage_bad = tmem_slot[1];  // spare word beside the tensor-memory slot
-      if (threadIdx.x == 0) stage_bad = 0;
-      named_barrier_sync(1, 4 * 32);
-      uint8_t* stage = smem + L::kKOff;
-      if (ok) {
-        prefill::epilogue_stage<D>(tm_o + lane_off, n > 0, m_run, l_run, stage, threadIdx.x,
-                                   row.valid ? p.lse_part + row.flat * p.n_splits + split : nullptr);
-      } else if (lane == 0) {
-        stage_bad = 1;
-      }
-      fence_proxy_async_smem();
-      named_barrier_sync(1, 4 * 32);
-      if (threadIdx.x == 0 && !stage_bad) {
-        // box: 32 columns x 1 split x q_per_tile queries x G heads; rows past Lq are clipped
-        for (int c = 0; c < D / 32; ++c)
-          prefill::tma_store_4d(&tm_po, sK + c * (kRows * 128), c * 32, split, q0, b * p.Hq + hk * p.G);
-        prefill::bulk_commit_group();
-        prefill::bulk_wait_read_all();
-      }
-    } else if (kStagedOut && p.Lq > 1 && p.out_dtype != Dtype::FP32) {
-      // The 16-bit output is staged the same way and written by TMA stores through a map
-      // shaped like Q's (64 columns x q_per_tile queries x G heads per box).  Measured: a
-      // gain for D <= 128 with a query tile of several queries; one query per tile (decode)
-      // and the D = 256 kernels keep the per-thread stores.
-      volatile uint32_t& stage_bad = tmem_slot[1];
-      if (threadIdx.x == 0) stage_bad = 0;
-      named_barrier_sync(1, 4 * 32);
-      uint8_t* stage = smem + L::kKOff;
-      if (ok) {
-        prefill::epilogue_stage16<D, BF16>(tm_o + lane_off, n > 0, m_run, l_run, stage, threadIdx.x,
-                                           row.valid && p.lse ? p.lse + row.flat : nullptr);
-      } else if (lane == 0) {
-        stage_bad = 1;
-      }
-      fence_proxy_async_smem();
-      named_barrier_sync(1, 4 * 32);
-      if (threadIdx.x == 0 && !stage_bad) {
-        for (int t = 0; t < D / 64; ++t)
-          prefill::tma_store_4d(&tm_po, sK + t * (kRows * 128), t * 64, q0, hk * p.G, b);
-        prefill::bulk_commit_group();
-        prefill::bulk_wait_read_all();
+    if constexpr (SPLIT || kStagedOut) {
+      if (SPLIT || (p.Lq > 1 && p.out_dtype != Dtype::FP32)) {
+        // The row's output is staged in the K ring (free once the loop is done) one
+        // 32-column slab at a time and written by TMA stores: a split's fp32 partial state
+        // through 32-column boxes over the [rows, n_splits, D] buffer (rows are 1 KB apart
+        // there, so per-thread stores would not coalesce), the 16-bit output of D <= 128
+        // through 64-column boxes of a Q-shaped map.  Thread 0 starts each box as soon as the
+        // four softmax warps have staged it, so the copy-out overlaps the staging that
+        // follows, and the next slab's tensor-memory load is in flight while one is staged.
+        // Every softmax thread reaches every barrier; a warp whose waits ran out flags the
+        // tile so that nothing half-written is stored.
+        volatile uint32_t& stage_bad = tmem_slot[1];  // spare word beside the tensor-memory slot
+        if (threadIdx.x == 0) stage_bad = 0;
+        named_barrier_sync(1, 4 * 32);
+        if (!ok && lane == 0) stage_bad = 1;
+        const bool have_o = ok && n > 0;
+        const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+        uint8_t* stage = smem + L::kKOff;
+        uint32_t oa[32], ob[32];
+        if (have_o) tmem_ld32(tm_o + lane_off, oa);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t(&cur)[32] = (c & 1) ? ob : oa;
+          uint32_t(&nxt)[32] = (c & 1) ? oa : ob;
+          if (have_o) {
+            tmem_ld_wait_tied(cur);
+            if (c + 1 < D / 32) tmem_ld32(tm_o + lane_off + (c + 1) * 32, nxt);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) cur[e] = 0u;
+          }
+          if constexpr (SPLIT) {
+            if (ok) prefill::stage_slab_f32(cur, inv_l, stage + c * (kRows * 128), threadIdx.x);
+            fence_proxy_async_smem();
+            named_barrier_sync(1, 4 * 32);
+            if (threadIdx.x == 0 && !stage_bad) {
+              // box: 32 columns x 1 split x q_per_tile queries x G heads; rows past Lq clipped
+              prefill::tma_store_4d(&tm_po, sK + c * (kRows * 128), c * 32, split, q0,
+                                    b * p.Hq + hk * p.G);
+              prefill::bulk_commit_group();
+            }
+          } else {
+            if (ok) prefill::stage_slab16<BF16>(cur, inv_l, stage + (c / 2) * (kRows * 128), threadIdx.x, c);
+            if (c & 1) {
+              fence_proxy_async_smem();
+              named_barrier_sync(1, 4 * 32);
+              if (threadIdx.x == 0 && !stage_bad) {
+                prefill::tma_store_4d(&tm_po, sK + (c / 2) * (kRows * 128), (c / 2) * 64, q0,
+                                      hk * p.G, b);
+                prefill::bulk_commit_group();
+              }
+            }
+          }
+        }
+        if (ok && row.valid) {
+          if constexpr (SPLIT) p.lse_part[row.flat * p.n_splits + split] = prefill::row_lse(m_run, l_run);
+          else if (p.lse) p.lse[row.flat] = prefill::row_lse(m_run, l_run);
+        }
+        if (threadIdx.x == 0 && !stage_bad) prefill::bulk_wait_read_all();
+      } else if (ok) {
+        prefill::epilogue<D>(p, row, tm_o + lane_off, n > 0, m_run, l_run, nullptr, nullptr);
       }
     } else if (ok) {
       prefill::epilogue<D>(p, row, tm_o + lane_off, n > 0, m_run, l_run, nullptr, nullptr);

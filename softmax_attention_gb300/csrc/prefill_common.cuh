@@ -247,67 +247,44 @@ __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-// Partial-state epilogue of one row, staged for TMA stores: O / l (fp32) of row r goes into
-// the D/32 staging tiles (tile c holds columns 32c .. 32c+31 of the 128 rows, 128-byte rows,
-// 128-byte swizzle: 16-byte chunk ch of row r at chunk ch ^ (r & 7)); the lse goes to
-// part_lse when set.  Warp-collective (every lane reads its TMEM lane).
-template <int D>
-__device__ __forceinline__ void epilogue_stage(uint32_t t_o, bool have_o, float m, float l,
-                                               uint8_t* stage, int r, float* part_lse) {
-  const float inv_l = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll 1
-  for (int c = 0; c < D / 32; ++c) {
-    uint32_t o[32];
-    if (have_o) {
-      tmem_ld32(t_o + c * 32, o);
-      tmem_ld_wait();
-    } else {
+// Staging of one row's output for TMA stores, 32 columns (one tcgen05.ld) at a time.  A slab
+// of fp32 partial state holds columns 32c .. 32c+31 of the 128 rows as 128-byte rows; a
+// 16-bit tile holds columns 64t .. 64t+63, two slabs' worth.  Both use the 128-byte swizzle:
+// 16-byte chunk ch of row r sits at chunk ch ^ (r & 7), so the 32 rows of a warp write
+// whole 128-byte bank lines.
+__device__ __forceinline__ void stage_slab_f32(const uint32_t (&o)[32], float inv_l, uint8_t* slab,
+                                               int r) {
+  uint8_t* row = slab + r * 128;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) o[e] = 0u;
-    }
-    uint8_t* tile = stage + c * (kRows * 128) + r * 128;
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch)
-      *reinterpret_cast<float4*>(tile + ((ch ^ (r & 7)) * 16)) =
-          make_float4(__uint_as_float(o[4 * ch]) * inv_l, __uint_as_float(o[4 * ch + 1]) * inv_l,
-                      __uint_as_float(o[4 * ch + 2]) * inv_l, __uint_as_float(o[4 * ch + 3]) * inv_l);
-  }
-  if (part_lse) *part_lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+  for (int ch = 0; ch < 8; ++ch)
+    *reinterpret_cast<float4*>(row + ((ch ^ (r & 7)) * 16)) =
+        make_float4(__uint_as_float(o[4 * ch]) * inv_l, __uint_as_float(o[4 * ch + 1]) * inv_l,
+                    __uint_as_float(o[4 * ch + 2]) * inv_l, __uint_as_float(o[4 * ch + 3]) * inv_l);
 }
 
-// Final-output epilogue of one row, staged for TMA stores: O / l in 16 bits (BF16 selects
-// bf16, else fp16) goes into the D/64 staging tiles (tile t holds columns 64t .. 64t+63 of
-// the 128 rows, 128-byte rows, 128-byte swizzle); the lse goes to lse_out when set.
-template <int D, bool BF16>
-__device__ __forceinline__ void epilogue_stage16(uint32_t t_o, bool have_o, float m, float l,
-                                                 uint8_t* stage, int r, float* lse_out) {
-  const float inv_l = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll 1
-  for (int c = 0; c < D / 32; ++c) {
-    uint32_t o[32];
-    if (have_o) {
-      tmem_ld32(t_o + c * 32, o);
-      tmem_ld_wait();
-    } else {
+// Columns 32c .. 32c+31 in 16 bits (BF16 selects bf16, else fp16): chunks 4(c % 2) .. +3 of
+// the row in its 64-column tile.
+template <bool BF16>
+__device__ __forceinline__ void stage_slab16(const uint32_t (&o)[32], float inv_l, uint8_t* tile,
+                                             int r, int c) {
+  uint8_t* row = tile + r * 128;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) o[e] = 0u;
+  for (int q = 0; q < 4; ++q) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float a = __uint_as_float(o[8 * q + 2 * e]) * inv_l;
+      const float b = __uint_as_float(o[8 * q + 2 * e + 1]) * inv_l;
+      w[e] = BF16 ? pack_bf16x2(a, b) : pack_f16x2(a, b);
     }
-    // columns 32c .. 32c+31 are 16-byte chunks 4(c % 2) .. 4(c % 2) + 3 of tile c / 2
-    uint8_t* tile = stage + (c / 2) * (kRows * 128) + r * 128;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float a = __uint_as_float(o[8 * q + 2 * e]) * inv_l;
-        const float b = __uint_as_float(o[8 * q + 2 * e + 1]) * inv_l;
-        w[e] = BF16 ? pack_bf16x2(a, b) : pack_f16x2(a, b);
-      }
-      const int ch = 4 * (c % 2) + q;
-      *reinterpret_cast<uint4*>(tile + ((ch ^ (r & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+    const int ch = 4 * (c % 2) + q;
+    *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
-  if (lse_out) *lse_out = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+}
+
+// log-sum-exp (natural log) of a row from its running max (log2 units) and sum
+__device__ __forceinline__ float row_lse(float m, float l) {
+  return l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
 // KV tiles [t_begin, t_end) of one split for a tile set whose last query is q_last, in a
