@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t(&cur)[32] = (c & 1) ? ob : oa;
           uint32_t(&nxt)[32] = (c & 1) ? oa : ob;
           if (have_o) {
-            tmem_ld_wait_tied(cur);
+            prefill::tmem_ld_wait_tied(cur);
             if (c + 1 < D / 32) tmem_ld32(tm_o + lane_off + (c + 1) * 32, nxt);
           } else {
 #pragma unroll

@@ -247,6 +247,22 @@ __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// tcgen05.wait::ld tied to the 32 registers of one earlier tmem_ld32: the compiler cannot move
+// a use of them above it (a plain wait orders memory only), so a second load may be in
+// flight while these are used.
+__device__ __forceinline__ void tmem_ld_wait_tied(uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+        "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]),
+        "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),
+        "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),
+        "+r"(r[31])
+      :
+      : "memory");
+}
+
 // Staging of one row's output for TMA stores, 32 columns (one tcgen05.ld) at a time.  A slab
 // of fp32 partial state holds columns 32c .. 32c+31 of the 128 rows as 128-byte rows; a
 // 16-bit tile holds columns 64t .. 64t+63, two slabs' worth.  Both use the 128-byte swizzle:

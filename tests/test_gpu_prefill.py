@@ -116,6 +116,21 @@ def test_forced_splits(splits):
     check(out, lse, ro, rl, what=f"splits={splits}")
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lkv,D,causal,splits", [
+    (1, 12, 4, 50, 700, 64, False, 5),    # G=3: 42 queries x 3 heads per tile; last split empty
+    (2, 16, 1, 33, 515, 128, True, 4),    # G=16: 8 queries per tile, ragged last query tile
+    (1, 8, 1, 37, 900, 256, True, 9),     # MQA, D=256: 16 queries x 8 heads, ragged tail
+    (1, 6, 6, 300, 300, 128, True, 3),    # square causal: the early query tiles' later splits are empty
+])
+def test_forced_splits_shapes(B, Hq, Hkv, Lq, Lkv, D, causal, splits):
+    """Split partial states of tiles whose rows are not a power of two of queries per head,
+    ragged query tiles and empty splits (O = 0, lse = -inf), through the merge."""
+    c = workloads.DenseCase(B=B, Hq=Hq, Hkv=Hkv, Lq=Lq, Lkv=Lkv, D=D, causal=causal, sigma=0.5,
+                            seed=11 * splits + D)
+    out, lse, ro, rl = _run(c, num_splits=splits)
+    check(out, lse, ro, rl, what=f"{c} splits={splits}")
+
+
 def test_short_form_matches_oracle():
     c = workloads.DenseCase(B=1, Hq=8, Hkv=2, Lq=256, Lkv=1024, D=128, causal=True, sigma=0.5)
     out, lse, ro, rl = _run(c, short_form=True)
