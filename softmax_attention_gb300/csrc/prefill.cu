@@ -489,10 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (threadIdx.x == 0 && !stage_bad) prefill::bulk_wait_read_all();
       } else if (ok) {
-        prefill::epilogue<D>(p, row, tm_o + lane_off, n > 0, m_run, l_run, nullptr, nullptr);
+        prefill::epilogue<D>(p, row, tm_o + lane_off, n > 0, m_run, l_run);
       }
     } else if (ok) {
-      prefill::epilogue<D>(p, row, tm_o + lane_off, n > 0, m_run, l_run, nullptr, nullptr);
+      prefill::epilogue<D>(p, row, tm_o + lane_off, n > 0, m_run, l_run);
     }
   }
   tc_fence_before();

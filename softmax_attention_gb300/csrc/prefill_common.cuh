@@ -180,16 +180,19 @@ __device__ __forceinline__ void store_p(uint32_t t_s, const uint32_t (&pk)[BN / 
     tmem_st16(t_s + c, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c]));
 }
 
-// Epilogue of one row: O / l to the output, or to a partial state (part_o [D] fp32 and
-// part_lse, natural log) when part_o is set; lse to p.lse.  Warp-collective: every lane reads
-// its TMEM lane; rows that are not valid store nothing.  have_o is false when no P V product
-// was issued (no KV tile in this part): the row is then empty.
+// log-sum-exp (natural log) of a row from its running max (log2 units) and sum
+__device__ __forceinline__ float row_lse(float m, float l) {
+  return l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+}
+
+// Epilogue of one row with per-thread stores: O / l to the output in out_dtype, lse to p.lse.
+// Warp-collective: every lane reads its TMEM lane; rows that are not valid store nothing.
+// have_o is false when no P V product was issued (no KV tile in this part): the row is then
+// empty.
 template <int D>
 __device__ __forceinline__ void epilogue(const PrefillParams& p, const Row& row, uint32_t t_o,
-                                         bool have_o, float m, float l, float* part_o,
-                                         float* part_lse) {
+                                         bool have_o, float m, float l) {
   const float inv_l = l > 0.f ? 1.f / l : 0.f;
-  const float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 #pragma unroll 1
   for (int c = 0; c < D / 32; ++c) {
     uint32_t o[32];
@@ -204,11 +207,7 @@ __device__ __forceinline__ void epilogue(const PrefillParams& p, const Row& row,
     float v[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv_l;
-    if (part_o) {
-      float4* dst = reinterpret_cast<float4*>(part_o + c * 32);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-    } else if (p.out_dtype == Dtype::FP32) {
+    if (p.out_dtype == Dtype::FP32) {
       float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + row.flat * D + c * 32);
 #pragma unroll
       for (int e = 0; e < 8; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
@@ -223,10 +222,7 @@ __device__ __forceinline__ void epilogue(const PrefillParams& p, const Row& row,
       for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
     }
   }
-  if (row.valid) {
-    if (part_o) *part_lse = lse_v;
-    else if (p.lse) p.lse[row.flat] = lse_v;
-  }
+  if (row.valid && p.lse) p.lse[row.flat] = row_lse(m, l);
 }
 
 // 4-D tiled TMA store from shared to global memory, completed through the bulk group
@@ -298,10 +294,6 @@ __device__ __forceinline__ void stage_slab16(const uint32_t (&o)[32], float inv_
   }
 }
 
-// log-sum-exp (natural log) of a row from its running max (log2 units) and sum
-__device__ __forceinline__ float row_lse(float m, float l) {
-  return l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-}
 
 // KV tiles [t_begin, t_end) of one split for a tile set whose last query is q_last, in a
 // sequence of Lkv keys.
