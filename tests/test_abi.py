@@ -101,6 +101,39 @@ def test_workspace_sizes_are_consistent(lib):
     assert 0 < tail < 768 * 64 * (512 + 1) * 4
 
 
+def test_prefill_split_plan(lib):
+    """The automatic KV split: none while the (query tile, kv head, batch) units cover half the
+    SMs; otherwise as many parts as still fit one wave, each of at least four KV tiles, never
+    more parts than KV tiles; and a forced count is taken as given (capped by the KV tiles)."""
+    sms = (torch.cuda.get_device_properties(0).multi_processor_count
+           if torch.cuda.is_available() else 148)
+    for B, Hq, Hkv, Lq, Lkv, D in ((1, 8, 1, 16, 16384, 256), (1, 8, 1, 64, 16384, 256),
+                                   (1, 8, 1, 256, 16384, 256), (1, 8, 1, 1024, 16384, 256),
+                                   (1, 32, 8, 512, 16384, 128), (2, 4, 4, 1, 300, 64),
+                                   (1, 4, 1, 8, 100, 128), (4, 16, 2, 100, 8192, 128)):
+        a = _args(B=B, Hq=Hq, Hkv=Hkv, Lq=Lq, Lkv=Lkv, D=D)
+        n = lib.fa_prefill_num_splits(ctypes.byref(a))
+        G = Hq // Hkv
+        q_per_tile = 128 // G
+        units = -(-Lq // q_per_tile) * Hkv * B
+        bn = 64 if D == 256 else 128
+        kv_tiles = -(-Lkv // bn)
+        assert 1 <= n <= max(1, kv_tiles), (B, Hq, Hkv, Lq, Lkv, D, n)
+        if units * 2 > sms:
+            assert n == 1, (Lq, n)
+        else:
+            assert n * units <= sms, (Lq, n)
+            assert n == 1 or kv_tiles // n >= 4, (Lq, n)
+            # as many parts as fit, unless the four-tile floor or the KV tiles cap it
+            assert n == min(sms // units, max(1, kv_tiles // 4)), (Lq, n)
+        ws = lib.fa_prefill_workspace_size(ctypes.byref(a))
+        assert (ws > 0) == (n > 1)
+        if n > 1:
+            assert ws >= B * Hq * Lq * n * (D + 1) * 4
+    a = _args(Lkv=300, num_splits=7)  # 3 KV tiles of 128 keys: seven parts become three
+    assert lib.fa_prefill_num_splits(ctypes.byref(a)) == 3
+
+
 @pytest.mark.parametrize("args,code", [
     (dict(D=80), fa.FA_ERR_UNSUPPORTED),
     (dict(Hq=32, Hkv=1, page_size=4, max_pages=1024), fa.FA_ERR_UNSUPPORTED),  # G=32
