@@ -13,9 +13,11 @@ pytestmark = pytest.mark.gpu
 
 
 # (rows, parts, D): one to eight warps per row (parts <= 8, 16, 32, more), one to four 16-byte
-# vectors per lane, D not a multiple of 128, row counts that leave a CTA partly empty.
+# vectors per lane, D not a multiple of 128, row counts that leave a CTA partly empty; 128 rows
+# of 64 parts at D=256 is the shape of the multi-query sweep's shortest size.
 @pytest.mark.parametrize("rows,S,D", [(37, 5, 128), (8, 40, 512), (3, 1, 64), (21, 12, 256),
-                                      (9, 30, 384), (5, 150, 100), (50, 16, 200), (17, 8, 4)])
+                                      (9, 30, 384), (5, 150, 100), (50, 16, 200), (17, 8, 4),
+                                      (128, 64, 256), (7, 33, 128)])
 def test_merge_parity(rows, S, D):
     g = torch.Generator().manual_seed(rows * S)
     o = torch.randn(rows, S, D, generator=g)
